@@ -1,0 +1,356 @@
+"""Pins for the fp64 oracle, independent of the oracle itself (CPU only).
+
+Each check ties the oracle to something other than its own code: a worked
+example from the pages' definition, a textbook/library routine that a special
+case reduces to, a brute-force definition on tiny inputs, a closed form, or an
+invariant the mathematics fixes.  Together they are chosen so that a dropped
+term, a wrong sign, a wrong index or a transposed operand in the oracle fails
+at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def e4m3_codes(values):
+    """Encode values that are exact in E4M3 through torch's own FP8 cast."""
+    t = torch.tensor(values, dtype=torch.float32).to(torch.float8_e4m3fn)
+    assert torch.equal(t.float(), torch.tensor(values, dtype=torch.float32)), "value not exact in E4M3"
+    return t.view(torch.uint8).numpy()
+
+
+def bf16_bits(x: torch.Tensor) -> np.ndarray:
+    return x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_values(bits: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+
+
+# ----------------------------------------------------------------- decoders
+
+def test_e4m3_decoder_matches_torch_all_codes():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).double().numpy()
+    mine = np.array([oracle.e4m3(c) for c in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(mine))
+    assert nan.sum() == 2  # 0x7F and 0xFF
+    assert np.array_equal(ref[~nan], mine[~nan])
+    assert mine[0x7E] == 448.0 and mine[0x01] == 2.0 ** -9
+
+
+def test_bf16_decoder_matches_torch():
+    g = torch.Generator().manual_seed(5)
+    x = torch.cat([torch.randn(4096, generator=g) * 10 ** torch.randint(-30, 30, (4096,), generator=g).float(),
+                   torch.tensor([0.0, -0.0, 1.0, -2.5, 65504.0, 1e-40, -1e-40])])
+    bits = bf16_bits(x)
+    ref = bf16_values(bits)
+    mine = np.array([oracle.bf16(int(b)) for b in bits])
+    assert np.array_equal(ref, mine)
+
+
+# ------------------------------------------------------------------ indexer
+
+def _hand_inputs(g, scaled=False):
+    keys = np.array(g["keys"], dtype=np.float32)
+    k8 = e4m3_codes(keys)
+    ks = np.ones(3, dtype=np.float32)
+    q = np.array([qq["q"] for qq in g["queries"]], dtype=np.float32)
+    q8 = e4m3_codes(q)
+    qs = np.ones(3, dtype=np.float32)
+    w = np.array([qq["w"] for qq in g["queries"]], dtype=np.float32)
+    if scaled:
+        v = g["scaled_variant"]
+        k8[0] = e4m3_codes(np.array(v["key0_codes"], dtype=np.float32))
+        ks[0] = v["key0_scale"]
+        q8[2] = e4m3_codes(np.array(v["query2_codes"], dtype=np.float32))
+        qs[2] = v["query2_scale"]
+    return q8, qs, w, k8, ks
+
+
+@pytest.mark.parametrize("scaled", [False, True])
+def test_indexer_hand_example(scaled):
+    g = _load("indexer_hand_example.json")
+    q8, qs, w, k8, ks = _hand_inputs(g, scaled)
+    out = oracle.indexer(q8, qs, w, np.arange(3), k8, ks)
+    for t, row in enumerate(g["logits"]):
+        assert np.array_equal(out[t, : t + 1], np.array(row, dtype=np.float64))
+        assert np.all(np.isnan(out[t, t + 1:]))  # nothing written past the causal bound
+
+
+def test_topk_hand_example():
+    g = _load("indexer_hand_example.json")
+    vals = np.full((3, 3), np.nan)
+    for t, row in enumerate(g["logits"]):
+        vals[t, : t + 1] = row
+    for k, exp in g["topk"].items():
+        got = oracle.topk(np.nan_to_num(vals, nan=-1e300), np.arange(1, 4), int(k))
+        assert got.tolist() == exp
+
+
+def _rand_indexer(seed, n, S, HI, dI, w_scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(n, HI, dI, generator=g)
+    k = torch.randn(S, dI, generator=g)
+    qs = q.reshape(n, -1).abs().amax(1) / 448
+    ks = k.abs().amax(1) / 448
+    q8 = (q / qs[:, None, None]).clamp(-448, 448).to(torch.float8_e4m3fn)
+    k8 = (k / ks[:, None]).clamp(-448, 448).to(torch.float8_e4m3fn)
+    w = torch.randn(n, HI, generator=g) * w_scale
+    return q8, qs, w, k8, ks
+
+
+def test_indexer_single_head_is_relu_of_matmul():
+    """H_I = 1, w = 1 reduces the index score to ReLU(Qdeq Kdeq^T): one library matmul."""
+    n, S, dI = 37, 53, 32
+    q8, qs, w, k8, ks = _rand_indexer(1, n, S, 1, dI)
+    w = torch.ones(n, 1)
+    q_pos = torch.randint(0, S, (n,), generator=torch.Generator().manual_seed(2)).int()
+    out = oracle.indexer(q8.view(torch.uint8).numpy(), qs.numpy(), w.numpy(), q_pos.numpy(),
+                         k8.view(torch.uint8).numpy(), ks.numpy())
+    qd = q8.double()[:, 0, :] * qs.double()[:, None]
+    kd = k8.double() * ks.double()[:, None]
+    ref = torch.relu(qd @ kd.T).numpy()
+    for r in range(n):
+        p = int(q_pos[r])
+        np.testing.assert_allclose(out[r, : p + 1], ref[r, : p + 1], rtol=1e-12, atol=1e-12)
+        assert np.all(np.isnan(out[r, p + 1:]))
+
+
+def test_indexer_head_weights_are_linear_and_heads_commute():
+    n, S, HI, dI = 9, 40, 4, 32
+    q8, qs, w, k8, ks = _rand_indexer(3, n, S, HI, dI)
+    w2 = torch.randn(n, HI, generator=torch.Generator().manual_seed(4))
+    pos = np.full(n, S - 1)
+    args = lambda qq, ww: (qq.view(torch.uint8).numpy(), qs.numpy(), ww.numpy(), pos,
+                           k8.view(torch.uint8).numpy(), ks.numpy())
+    a = oracle.indexer(*args(q8, w))
+    b = oracle.indexer(*args(q8, w2))
+    ab = oracle.indexer(*args(q8, w + w2))
+    np.testing.assert_allclose(ab, a + b, rtol=1e-5, atol=1e-5)  # w in fp32: sums round once
+    perm = torch.randperm(HI, generator=torch.Generator().manual_seed(6))
+    c = oracle.indexer(*args(q8[:, perm].contiguous(), w[:, perm].contiguous()))
+    np.testing.assert_allclose(c, a, rtol=1e-12, atol=1e-12)
+    # one head switched off by a zero weight equals dropping that head
+    w0 = w.clone()
+    w0[:, 0] = 0
+    d = oracle.indexer(*args(q8, w0))
+    e = oracle.indexer(*args(q8[:, 1:].contiguous(), w[:, 1:].contiguous()))
+    np.testing.assert_allclose(d, e, rtol=1e-12, atol=1e-12)
+
+
+def test_indexer_relu_sign():
+    """A key pointing against every head scores 0 for positive weights; along them, positive."""
+    HI, dI = 3, 32
+    q = np.ones((1, HI, dI), np.float32)
+    k = np.stack([np.ones(dI, np.float32), -np.ones(dI, np.float32)])
+    out = oracle.indexer(e4m3_codes(q), np.ones(1, np.float32), np.array([[1, 2, 3]], np.float32),
+                         np.array([1]), e4m3_codes(k), np.array([0.5, 0.5], np.float32))
+    assert out[0, 0] == pytest.approx(6 * dI * 0.5)
+    assert out[0, 1] == 0.0
+
+
+def test_indexer_paged_equals_contiguous():
+    HI, dI, ps = 4, 32, 16
+    g = torch.Generator().manual_seed(7)
+    ctx = np.array([1, 16, 17, 50, 33])
+    n = len(ctx)
+    pages = [(c + ps - 1) // ps for c in ctx]
+    P = sum(pages) + 3
+    perm = torch.randperm(P, generator=g).numpy()
+    bt = np.full((n, max(pages) + 1), -1, np.int32)
+    o = 0
+    for b in range(n):
+        bt[b, : pages[b]] = perm[o:o + pages[b]]
+        o += pages[b]
+    q8, qs, w, k8f, ksf = _rand_indexer(8, n, P * ps, HI, dI)
+    k8_pool = k8f.view(torch.uint8).numpy().reshape(P, ps, dI)
+    ks_pool = ksf.numpy().reshape(P, ps)
+    ld = 64
+    paged = oracle.indexer_paged(q8.view(torch.uint8).numpy(), qs.numpy(), w.numpy(), ctx, k8_pool, ks_pool, bt, ld)
+    for b in range(n):
+        rows = np.array([bt[b, s // ps] * ps + s % ps for s in range(ctx[b])])
+        cont = oracle.indexer(q8[b:b + 1].view(torch.uint8).numpy(), qs[b:b + 1].numpy(), w[b:b + 1].numpy(),
+                              np.array([ctx[b] - 1]), k8_pool.reshape(-1, dI)[rows], ks_pool.reshape(-1)[rows], ld=ld)
+        np.testing.assert_array_equal(paged[b], cont[0])
+
+
+# -------------------------------------------------------------------- top-k
+
+def brute_topk(vals, n, k):
+    """Definition on tiny inputs: s is kept iff fewer than k candidates beat it."""
+    keep = []
+    for s in range(n):
+        beats = sum(1 for j in range(n) if vals[j] > vals[s] or (vals[j] == vals[s] and j < s))
+        if beats < k:
+            keep.append(s)
+    return keep + [-1] * (k - len(keep))
+
+
+def test_topk_worked_tie_row():
+    g = _load("topk_tie_row.json")
+    row = np.array(g["row"])
+    assert math.copysign(1, row[3]) < 0  # the fixture really holds -0.0
+    for k, exp in g["expected"].items():
+        got = oracle.topk(row[None], np.array([len(row)]), int(k))
+        assert got[0].tolist() == exp
+        assert brute_topk(row, len(row), int(k)) == exp
+
+
+@pytest.mark.parametrize("ties", [False, True])
+def test_topk_matches_brute_force(ties):
+    g = torch.Generator().manual_seed(11 + ties)
+    rows, ld = 24, 97
+    if ties:
+        vals = torch.randint(-3, 4, (rows, ld), generator=g).double()
+        vals[vals == 0] = -0.0 * torch.randint(0, 2, (int((vals == 0).sum()),), generator=g).double()
+    else:
+        vals = torch.randn(rows, ld, generator=g, dtype=torch.float64)
+    n = torch.randint(0, ld + 1, (rows,), generator=g).numpy()
+    for k in (1, 5, 31, 97, 120):
+        got = oracle.topk(vals.numpy(), n, k)
+        for r in range(rows):
+            assert got[r].tolist() == brute_topk(vals[r].tolist(), int(n[r]), k)
+
+
+# --------------------------------------------------------------- sparse MLA
+
+def _mla_inputs(seed, n, S, H, D=576):
+    g = torch.Generator().manual_seed(seed)
+    q = bf16_bits(torch.randn(n, H, D, generator=g))
+    kv = bf16_bits(torch.randn(S, D, generator=g))
+    return q, kv
+
+
+def test_mla_equals_dense_causal_when_everything_is_selected():
+    """k >= t+1 keeps every prior token, so sparse MLA equals dense causal MQA
+    attention, here through torch's softmax/logsumexp in fp64."""
+    n, S, H = 12, 12, 4
+    scale = 1 / 24
+    q, kv = _mla_inputs(1, n, S, H)
+    k = 16
+    idx = np.full((n, k), -1, np.int32)
+    for t in range(n):
+        idx[t, : t + 1] = np.arange(t + 1)
+    out, lse = oracle.sparse_mla(q, kv, idx, scale)
+    qd = torch.from_numpy(bf16_values(q))
+    kd = torch.from_numpy(bf16_values(kv))
+    s = torch.einsum("thd,sd->ths", qd, kd) * scale
+    mask = torch.arange(S)[None, :] > torch.arange(n)[:, None]
+    s = s.masked_fill(mask[:, None, :], float("-inf"))
+    ref_o = torch.einsum("ths,sv->thv", torch.softmax(s, -1), kd[:, :512])
+    ref_lse = torch.logsumexp(s, -1)
+    np.testing.assert_allclose(out, ref_o.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_mla_permutation_invariance_and_padding():
+    n, S, H, k = 5, 300, 8, 40
+    q, kv = _mla_inputs(2, n, S, H)
+    g = torch.Generator().manual_seed(3)
+    idx = torch.stack([torch.randperm(S, generator=g)[:k] for _ in range(n)]).int().numpy()
+    out, lse = oracle.sparse_mla(q, kv, idx, 0.05)
+    perm = torch.randperm(k, generator=g).numpy()
+    out2, lse2 = oracle.sparse_mla(q, kv, idx[:, perm], 0.05)
+    np.testing.assert_allclose(out2, out, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(lse2, lse, rtol=1e-13)
+    # invalid entries (-1, >= S) are skipped wherever they stand
+    pad = np.concatenate([idx, np.full((n, 7), -1, np.int32), np.full((n, 2), S, np.int32)], 1)
+    out3, lse3 = oracle.sparse_mla(q, kv, pad[:, np.random.default_rng(0).permutation(k + 9)], 0.05)
+    np.testing.assert_allclose(out3, out, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(lse3, lse, rtol=1e-13)
+
+
+def test_mla_closed_forms():
+    H, S, D = 4, 50, 576
+    q, kv = _mla_inputs(4, 1, S, H)
+    qv, kvv = bf16_values(q), bf16_values(kv)
+    scale = 0.07
+    # one valid key: O is that row's first 512 columns, LSE is its score
+    idx = np.array([[-1, 17, -1, -1]], np.int32)
+    out, lse = oracle.sparse_mla(q, kv, idx, scale)
+    np.testing.assert_array_equal(out[0], np.broadcast_to(kvv[17, :512], (H, 512)))
+    np.testing.assert_allclose(lse[0], scale * qv[0] @ kvv[17], rtol=1e-13)
+    # n identical keys: O = c[:512], LSE = score + ln n
+    kv_same = kv.copy()
+    kv_same[:10] = kv[3]
+    idx = np.arange(10, dtype=np.int32)[None]
+    out, lse = oracle.sparse_mla(q, kv_same, idx, scale)
+    np.testing.assert_allclose(out[0], np.broadcast_to(kvv[3, :512], (H, 512)), rtol=1e-13)
+    np.testing.assert_allclose(lse[0], scale * qv[0] @ kvv[3] + math.log(10), rtol=1e-13)
+    # q = 0: uniform weights, O = mean of V rows, LSE = ln n
+    qz = np.zeros_like(q)
+    idx = np.array([[4, 9, 11, 30, 31]], np.int32)
+    out, lse = oracle.sparse_mla(qz, kv, idx, scale)
+    np.testing.assert_allclose(out[0], np.broadcast_to(kvv[idx[0], :512].mean(0), (H, 512)), rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(lse[0], math.log(5), rtol=1e-14)
+    # nothing valid: O = 0, LSE = -inf
+    out, lse = oracle.sparse_mla(q, kv, np.array([[-1, S, -5]], np.int32), scale)
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
+    # the RoPE columns (512..575) enter the scores only
+    kv_r = kv.copy()
+    kv_r[:, 512:] = 0
+    q_r = q.copy()
+    q_r[:, :, 512:] = 0
+    idx = np.arange(20, dtype=np.int32)[None]
+    o1, l1 = oracle.sparse_mla(q_r, kv, idx, scale)
+    o2, l2 = oracle.sparse_mla(q_r, kv_r, idx, scale)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+def test_mla_split_and_combine():
+    """Attention over A u B equals the LSE-weighted merge of A and B (disjoint)."""
+    H, S, k = 6, 200, 64
+    q, kv = _mla_inputs(5, 1, S, H)
+    idx = np.random.default_rng(1).permutation(S)[:k].astype(np.int32)[None]
+    out, lse = oracle.sparse_mla(q, kv, idx, 0.04)
+    oa, la = oracle.sparse_mla(q, kv, idx[:, :25], 0.04)
+    ob, lb = oracle.sparse_mla(q, kv, idx[:, 25:], 0.04)
+    l = np.logaddexp(la, lb)
+    o = np.exp(la - l)[..., None] * oa + np.exp(lb - l)[..., None] * ob
+    np.testing.assert_allclose(lse, l, rtol=1e-13)
+    np.testing.assert_allclose(out, o, rtol=1e-10, atol=1e-13)
+
+
+def test_mla_paged_equals_contiguous():
+    H, D, ps = 4, 576, 16
+    ctx = np.array([5, 16, 40])
+    n = len(ctx)
+    pages = [(c + ps - 1) // ps for c in ctx]
+    P = sum(pages) + 2
+    perm = np.random.default_rng(2).permutation(P)
+    bt = np.full((n, max(pages)), -1, np.int32)
+    o = 0
+    for b in range(n):
+        bt[b, : pages[b]] = perm[o:o + pages[b]]
+        o += pages[b]
+    q, kvf = _mla_inputs(6, n, P * ps, H)
+    pool = kvf.reshape(P, ps, D)
+    k = 24
+    idx = np.full((n, k), -1, np.int32)
+    rng = np.random.default_rng(3)
+    for b in range(n):
+        m = min(k, ctx[b])
+        idx[b, :m] = np.sort(rng.permutation(ctx[b])[:m])
+    idx[2, -1] = ctx[2] + 3  # beyond the context: skipped
+    out, lse = oracle.sparse_mla_paged(q, pool, bt, ctx, idx, 0.05)
+    for b in range(n):
+        rows = np.array([bt[b, s // ps] * ps + s % ps if 0 <= s < ctx[b] else -1 for s in idx[b]], np.int32)
+        oc, lc = oracle.sparse_mla(q[b:b + 1], kvf, rows[None], 0.05)
+        np.testing.assert_array_equal(out[b], oc[0])
+        np.testing.assert_array_equal(lse[b], lc[0])
