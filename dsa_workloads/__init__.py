@@ -136,7 +136,7 @@ def prefill_inputs(cfg: Config, device, L: int | None = None, seed: int | None =
 
 
 def decode_layout(cfg: Config, seed: int | None = None, B: int | None = None,
-                  ctx_lo: int | None = None, ctx_hi: int | None = None):
+                  ctx_lo: int | None = None, ctx_hi: int | None = None, ctx=None):
     """Context lengths and a shuffled page pool (CPU tensors).
 
     Returns ctx [B] int32, block_table [B, max_pages] int32 (-1 past each
@@ -144,11 +144,14 @@ def decode_layout(cfg: Config, seed: int | None = None, B: int | None = None,
     permutation of 0..num_pages-1.
     """
     seed = cfg.seed if seed is None else seed
-    B = cfg.B if B is None else B
+    B = (cfg.B if B is None else B) if ctx is None else len(ctx)
     lo = cfg.ctx_lo if ctx_lo is None else ctx_lo
     hi = cfg.ctx_hi if ctx_hi is None else ctx_hi
-    g = _gen("cpu", seed, 30, 0)
-    ctx = torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)
+    if ctx is None:
+        g = _gen("cpu", seed, 30, 0)
+        ctx = torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)
+    else:
+        ctx = torch.as_tensor(ctx, dtype=torch.int32)
     ps = cfg.page_size
     npages = (ctx.to(torch.int64) + ps - 1) // ps
     num_pages = int(npages.sum())
@@ -164,7 +167,7 @@ def decode_layout(cfg: Config, seed: int | None = None, B: int | None = None,
 
 
 def decode_inputs(cfg: Config, device, seed: int | None = None, B: int | None = None,
-                  ctx_lo: int | None = None, ctx_hi: int | None = None, poison: bool = True):
+                  ctx_lo: int | None = None, ctx_hi: int | None = None, poison: bool = True, ctx=None):
     """One decode step over a paged cache.
 
     Pools: FP8 key codes [P, page, dI] with scales [P, page]; bf16 latent KV
@@ -173,7 +176,7 @@ def decode_inputs(cfg: Config, device, seed: int | None = None, B: int | None = 
     Queries: one token per sequence at position ctx-1.
     """
     seed = cfg.seed if seed is None else seed
-    ctx, bt, P = decode_layout(cfg, seed, B, ctx_lo, ctx_hi)
+    ctx, bt, P = decode_layout(cfg, seed, B, ctx_lo, ctx_hi, ctx)
     B = ctx.shape[0]
     ps = cfg.page_size
     kI = randn((P * ps, cfg.dI), device, seed, 12)

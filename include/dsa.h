@@ -1,0 +1,189 @@
+/*
+ * dsa.h: C ABI of libdsa.so, the GB300 (sm_103a) hot path of DeepSeek Sparse
+ * Attention (DSA).
+ *
+ * The method (release summary "DeepSeek-V3.2-Exp: Boosting Long-Context
+ * Efficiency with DeepSeek Sparse Attention", section "Method"; AMD article
+ * "AMD Instinct MI355X GPUs Power DeepSeek-V3.2-Exp", section "DeepSeek Sparse
+ * Attention (DSA)") has three stages, one entry point each, plus the paged
+ * decode form of the attention stage:
+ *   1. lightning indexer   I[t,s] = sum_j w[t,j] * ReLU(q[t,j] . k[s]), in FP8
+ *   2. top-k selection     the k (= 2048) highest-scoring prior tokens per query
+ *   3. sparse MLA          MQA-mode attention over only the selected latent rows
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer named as a tensor is a DEVICE pointer; shapes are row-major
+ *     and contiguous unless a leading dimension is given.  The caller owns every
+ *     buffer; the library allocates nothing, frees nothing and keeps no pointer
+ *     after a call returns.
+ *   - Work is enqueued asynchronously on `stream` (0 = legacy default stream).
+ *     Nothing synchronises inside the library and nothing falls back to the
+ *     host.
+ *   - Arguments are checked on the host before any launch.  On error the call
+ *     returns a non-zero dsa_status, launches nothing, leaves outputs untouched
+ *     and records a message for dsa_last_error().
+ *   - Data-dependent problems that only the device can see (a bad page id, a
+ *     position past the buffer, a pipeline wait that ran out of time) never
+ *     cause an out-of-bounds access: the kernel skips the offending element and
+ *     sets a bit in a per-device status word, read with dsa_get_device_status().
+ *   - "FP8" is E4M3 (OCP "fn" variant, max 448), passed as raw bytes.  "bf16" is
+ *     IEEE binary32 truncated to its upper 16 bits, passed as raw uint16.
+ */
+#ifndef DSA_H
+#define DSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *dsa_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    DSA_OK = 0,
+    DSA_ERR_INVALID_ARG = 1, /* null pointer, negative size, inconsistent shapes   */
+    DSA_ERR_UNSUPPORTED = 2, /* a size this build has no kernel for (see below)     */
+    DSA_ERR_ALIGNMENT = 3,   /* a pointer or stride breaks a 16-byte TMA rule       */
+    DSA_ERR_WORKSPACE = 4,   /* workspace missing or smaller than the query says    */
+    DSA_ERR_CUDA = 5,        /* a CUDA runtime/driver call or a launch failed       */
+    DSA_ERR_DEVICE = 6       /* dsa_get_device_status() found a device-side error   */
+} dsa_status;
+
+/* Bits of the device status word (dsa_get_device_status). */
+#define DSA_DEV_TIMEOUT      0x1u /* a bounded pipeline wait gave up; outputs of that CTA are invalid */
+#define DSA_DEV_BAD_POSITION 0x2u /* a query position / valid length exceeded the key range or ld     */
+#define DSA_DEV_BAD_PAGE     0x4u /* a block-table entry outside [0, num_pages); those keys skipped    */
+
+/* Message for the last failing call on this host thread ("" if none). */
+const char *dsa_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int dsa_version(void);
+
+/*
+ * dsa_get_device_status: copy the device status word of the current device to
+ * *status_out (DSA_DEV_* bits, 0 = clean) and clear it.  Enqueued on `stream`
+ * and then waits for that stream, so it sees every earlier kernel on it.
+ * Returns DSA_ERR_CUDA if the copy fails.
+ */
+int dsa_get_device_status(dsa_stream_t stream, uint32_t *status_out);
+
+/*
+ * dsa_indexer_logits: lightning-indexer scores (stage 1).
+ *
+ * Defines, for each query row r at absolute position p = q_pos[r] and each key
+ * position s in [0, p]:
+ *     logits[r*ld_logits + s] = sum_{j<H_I} w[r,j] * ReLU( sum_{d<d_I}
+ *                               (q8[r,j,d]*q_scale[r]) * (k8[s,d]*k_scale[s]) )
+ * ("DeepSeek-V3.2-Exp: Boosting Long-Context Efficiency with DeepSeek Sparse
+ * Attention", section "Method": index score against all prior tokens, ReLU,
+ * FP8, few heads).  The query's own position is included (causal s <= p).
+ * Entries with s > p are unspecified (the kernel may write -inf there, but
+ * never at or past ld_logits).
+ *
+ *   q8        [T, H_I, d_I]  FP8 codes of the indexer queries
+ *   q_scale   [T]            fp32, > 0: one dequantisation scale per query token
+ *   w         [T, H_I]       fp32 head weights (any sign)
+ *   q_pos     [T]            int32 absolute position of each query row
+ *   logits    [T, ld_logits] fp32 output, ld_logits >= 1 + max position used
+ *
+ * Keys, contiguous form (block_table == NULL):
+ *   k8        [S, d_I]       FP8 codes;   k_scale [S] fp32 > 0
+ *   A position q_pos[r] >= S is clamped to S-1 and flagged DSA_DEV_BAD_POSITION.
+ * Keys, paged form (block_table != NULL; used by decode, "indexer-logit kernels
+ * (incl. paged versions)", same page, "Key claims"):
+ *   k8        [num_pages, page_size, d_I] pool of FP8 codes
+ *   k_scale   [num_pages, page_size]      fp32 scales
+ *   block_table [T, max_pages] int32: row r's logical page i lives in pool page
+ *             block_table[r*max_pages + i]; a key at logical position s lives at
+ *             slot s % page_size of page block_table[r*max_pages + s/page_size].
+ *   S is ignored.  Each row is its own sequence.  An out-of-range page id is
+ *   skipped (its logits are left unwritten) and flagged DSA_DEV_BAD_PAGE.
+ *
+ * Supported sizes: (H_I, d_I) in {(64,128), (32,128), (4,32), (8,64), (16,64)};
+ * page_size in {32, 64, 128}; T >= 0 (T = 0 is a no-op).
+ * Alignment: q8 and k8 16-byte aligned; ld_logits >= 1.
+ */
+int dsa_indexer_logits(const void *q8, const float *q_scale, const float *w,
+                       int T, int H_I, int d_I,
+                       const void *k8, const float *k_scale, int S,
+                       const int32_t *block_table, int max_pages, int num_pages, int page_size,
+                       const int32_t *q_pos,
+                       float *logits, int64_t ld_logits, dsa_stream_t stream);
+
+/*
+ * dsa_topk: fine-grained token selection (stage 2).
+ *
+ * For each row t with n = valid_len[t] candidates logits[t*ld + s], s in [0, n):
+ * keeps the min(k, n) candidates ranked first by (score descending, index
+ * ascending) and writes their indices to idx[t*k ...] in ASCENDING index
+ * order, padded with -1 ("AMD Instinct MI355X GPUs Power DeepSeek-V3.2-Exp",
+ * section "DeepSeek Sparse Attention (DSA)", item 2: top-2048 per query).
+ * -0.0 and +0.0 compare equal.  Scores must be finite (a NaN makes that row's
+ * result unspecified, never out of bounds).  n > ld is clamped to ld and
+ * flagged DSA_DEV_BAD_POSITION; n < 0 counts as 0.
+ *
+ *   logits    [T, ld] fp32;  valid_len [T] int32;  idx [T, k] int32 output.
+ * Supported: 1 <= k <= 4096, ld >= 1, ld <= 2^28.  Deterministic: the same
+ * inputs give the same bytes.
+ */
+int dsa_topk(const float *logits, int64_t ld, int T, const int32_t *valid_len,
+             int k, int32_t *idx, dsa_stream_t stream);
+
+/*
+ * dsa_sparse_mla_prefill: MQA-mode sparse MLA over the selected rows (stage 3).
+ *
+ * For query row t, head h and its valid selected rows s_i = idx[t*k + i]
+ * (0 <= s_i < S; other entries are skipped wherever they stand):
+ *     S_i      = sm_scale * sum_{d<576} q[t,h,d] * kv[s_i,d]
+ *     out[t,h,v] = sum_i softmax(S)_i * kv[s_i,v]          (v < 512)
+ *     lse[t,h] = ln sum_i exp(S_i)
+ * ("DeepSeek-V3.2-Exp: Boosting Long-Context Efficiency with DeepSeek Sparse
+ * Attention", section "Method": main attention reads only the top-k entries,
+ * in MLA's MQA mode so one latent row is shared by all heads of a token; the
+ * first 512 columns are V, the last 64 are the RoPE part used only in scores.)
+ * A row with no valid entry gets out = 0 and lse = -inf.
+ *
+ *   q    [T, H, 576] bf16;  kv [S, 576] bf16;  idx [T, k] int32
+ *   out  [T, H, 512] bf16 (rounded to nearest even);  lse [T, H] fp32
+ * Supported: H = 128 or 64 or 16... see dsa_sparse_mla_supported(); D = 576,
+ * Dv = 512 fixed; 1 <= k <= 4096.  q, kv, out 16-byte aligned.
+ */
+int dsa_sparse_mla_prefill(const void *q, const void *kv, int S,
+                           const int32_t *idx, int T, int H, int k, float sm_scale,
+                           void *out, float *lse, dsa_stream_t stream);
+
+/*
+ * dsa_sparse_mla_decode_paged: the same attention for one new token per
+ * sequence over a paged latent cache (decode form of stage 3).
+ *
+ * Row b's query sits at position ctx_len[b]-1; idx[b*k + i] holds LOGICAL
+ * positions, read from slot s % page_size of pool page
+ * block_table[b*max_pages + s/page_size].  Entries outside [0, ctx_len[b]) are
+ * skipped; a page id outside [0, num_pages) is skipped and flagged
+ * DSA_DEV_BAD_PAGE.  The k selected rows are split across CTAs; partial
+ * results go to `workspace` and are merged by their LSE in a second kernel.
+ *
+ *   q       [B, H, 576] bf16;  kv_pool [num_pages, page_size, 576] bf16
+ *   block_table [B, max_pages] int32;  ctx_len [B] int32;  idx [B, k] int32
+ *   out     [B, H, 512] bf16;  lse [B, H] fp32
+ *   workspace: device buffer of at least
+ *           dsa_sparse_mla_decode_workspace_size(B, H, k) bytes, 256-byte
+ *           aligned, owned by the caller, contents need not be initialised;
+ *           two calls in flight at once need two workspaces.
+ */
+int dsa_sparse_mla_decode_paged(const void *q, const void *kv_pool, int num_pages, int page_size,
+                                const int32_t *block_table, int max_pages, const int32_t *ctx_len,
+                                const int32_t *idx, int B, int H, int k, float sm_scale,
+                                void *out, float *lse, void *workspace, size_t workspace_bytes,
+                                dsa_stream_t stream);
+
+/* Bytes of workspace dsa_sparse_mla_decode_paged needs for (B, H, k); 0 on bad input. */
+size_t dsa_sparse_mla_decode_workspace_size(int B, int H, int k);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSA_H */

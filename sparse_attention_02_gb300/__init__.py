@@ -1,0 +1,196 @@
+"""Python binding of libdsa.so, the GB300 (sm_103a) DSA hot path.
+
+Argument marshalling only: each function checks dtypes/shapes, passes raw
+device pointers and the current CUDA stream to the C entry point of the same
+name (declared in include/dsa.h) and raises ``DsaError`` on a non-zero status.
+Every step of the computation runs in the library's CUDA kernels; there is no
+host or PyTorch fallback, and importing this package fails loudly when the
+library has not been built.
+
+PyTorch is used only for device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdsa.so")
+
+DSA_OK = 0
+DSA_DEV_TIMEOUT = 0x1
+DSA_DEV_BAD_POSITION = 0x2
+DSA_DEV_BAD_PAGE = 0x4
+
+_lib = None
+
+
+class DsaError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"dsa error {code}: {msg}")
+        self.code = code
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libdsa.so (built by ``sparse_attention_02_gb300.build``)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build it with `python -m sparse_attention_02_gb300.build` "
+                           "(or __graft_entry__.build()); there is no fallback path")
+    lib = ctypes.CDLL(p)
+    P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.dsa_last_error.restype = ctypes.c_char_p
+    lib.dsa_version.restype = i32
+    lib.dsa_get_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+    lib.dsa_indexer_logits.argtypes = [P, P, P, i32, i32, i32, P, P, i32, P, i32, i32, i32, P, P, i64, P]
+    lib.dsa_topk.argtypes = [P, i64, i32, P, i32, P, P]
+    lib.dsa_sparse_mla_prefill.argtypes = [P, P, i32, P, i32, i32, i32, f32, P, P, P]
+    lib.dsa_sparse_mla_decode_paged.argtypes = [P, P, i32, i32, P, i32, P, P, i32, i32, i32, f32, P, P, P, sz, P]
+    lib.dsa_sparse_mla_decode_workspace_size.restype = sz
+    lib.dsa_sparse_mla_decode_workspace_size.argtypes = [i32, i32, i32]
+    for name in ("dsa_indexer_logits", "dsa_topk", "dsa_sparse_mla_prefill", "dsa_sparse_mla_decode_paged",
+                 "dsa_get_device_status"):
+        getattr(lib, name).restype = i32
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(rc: int):
+    if rc != DSA_OK:
+        raise DsaError(rc, load_library().dsa_last_error().decode())
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype, name: str, dim: int | None = None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dim is not None and t.dim() != dim:
+        raise ValueError(f"{name}: expected {dim} dims, got {t.dim()}")
+
+
+def dsa_indexer_logits(q8, q_scale, w, k8, k_scale, q_pos, logits, block_table=None, stream=None):
+    """Lightning-indexer scores into ``logits`` [T, ld] (fp32).
+
+    q8 uint8 [T, H_I, d_I] (E4M3 codes), q_scale fp32 [T], w fp32 [T, H_I], q_pos int32 [T].
+    Contiguous keys: k8 uint8 [S, d_I], k_scale fp32 [S].  Paged keys: k8 uint8
+    [num_pages, page_size, d_I], k_scale fp32 [num_pages, page_size] and
+    block_table int32 [T, max_pages].
+    """
+    _need(q8, torch.uint8, "q8", 3)
+    T, HI, dI = q8.shape
+    _need(q_scale, torch.float32, "q_scale", 1)
+    _need(w, torch.float32, "w", 2)
+    _need(q_pos, torch.int32, "q_pos", 1)
+    _need(logits, torch.float32, "logits", 2)
+    _need(k8, torch.uint8, "k8")
+    _need(k_scale, torch.float32, "k_scale")
+    if q_scale.shape[0] != T or tuple(w.shape) != (T, HI) or q_pos.shape[0] != T or logits.shape[0] != T:
+        raise ValueError("inconsistent query shapes")
+    if block_table is None:
+        if k8.dim() != 2 or k8.shape[1] != dI or k_scale.shape != (k8.shape[0],):
+            raise ValueError("k8 must be [S, d_I] and k_scale [S]")
+        S, mp, npg, ps = k8.shape[0], 0, 0, 0
+    else:
+        _need(block_table, torch.int32, "block_table", 2)
+        if k8.dim() != 3 or k8.shape[2] != dI or tuple(k_scale.shape) != tuple(k8.shape[:2]):
+            raise ValueError("paged: k8 must be [P, page, d_I] and k_scale [P, page]")
+        if block_table.shape[0] != T:
+            raise ValueError("block_table must have one row per query")
+        S, mp, npg, ps = 0, block_table.shape[1], k8.shape[0], k8.shape[1]
+    lib = load_library()
+    _check(lib.dsa_indexer_logits(_ptr(q8), _ptr(q_scale), _ptr(w), T, HI, dI, _ptr(k8), _ptr(k_scale), S,
+                                  _ptr(block_table), mp, npg, ps, _ptr(q_pos), _ptr(logits), logits.stride(0),
+                                  _stream(stream)))
+    return logits
+
+
+def dsa_topk(logits, valid_len, k: int, idx, stream=None):
+    """Top-k indices (ascending, -1 padded) of each row of ``logits`` [T, ld] into ``idx`` [T, k]."""
+    _need(logits, torch.float32, "logits", 2)
+    _need(valid_len, torch.int32, "valid_len", 1)
+    _need(idx, torch.int32, "idx", 2)
+    T = logits.shape[0]
+    if valid_len.shape[0] != T or tuple(idx.shape) != (T, k):
+        raise ValueError("inconsistent shapes")
+    _check(load_library().dsa_topk(_ptr(logits), logits.stride(0), T, _ptr(valid_len), k, _ptr(idx),
+                                   _stream(stream)))
+    return idx
+
+
+def dsa_sparse_mla_prefill(q, kv, idx, sm_scale: float, out, lse, stream=None):
+    """Sparse MQA-mode MLA: q bf16 [T, H, 576], kv bf16 [S, 576], idx int32 [T, k]
+    -> out bf16 [T, H, 512], lse fp32 [T, H]."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(kv, torch.bfloat16, "kv", 2)
+    _need(idx, torch.int32, "idx", 2)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(lse, torch.float32, "lse", 2)
+    T, H, D = q.shape
+    S = kv.shape[0]
+    k = idx.shape[1]
+    if D != 576 or kv.shape[1] != 576 or idx.shape[0] != T or tuple(out.shape) != (T, H, 512) \
+            or tuple(lse.shape) != (T, H):
+        raise ValueError("inconsistent shapes (D must be 576, Dv 512)")
+    _check(load_library().dsa_sparse_mla_prefill(_ptr(q), _ptr(kv), S, _ptr(idx), T, H, k, float(sm_scale),
+                                                 _ptr(out), _ptr(lse), _stream(stream)))
+    return out, lse
+
+
+def dsa_sparse_mla_decode_workspace_size(B: int, H: int, k: int) -> int:
+    return int(load_library().dsa_sparse_mla_decode_workspace_size(B, H, k))
+
+
+def dsa_sparse_mla_decode_paged(q, kv_pool, block_table, ctx_len, idx, sm_scale: float, out, lse,
+                                workspace=None, stream=None):
+    """Paged decode attention: q bf16 [B, H, 576], kv_pool bf16 [P, page, 576],
+    block_table int32 [B, max_pages], ctx_len int32 [B], idx int32 [B, k] (logical positions)."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(kv_pool, torch.bfloat16, "kv_pool", 3)
+    _need(block_table, torch.int32, "block_table", 2)
+    _need(ctx_len, torch.int32, "ctx_len", 1)
+    _need(idx, torch.int32, "idx", 2)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(lse, torch.float32, "lse", 2)
+    B, H, D = q.shape
+    P, ps, D2 = kv_pool.shape
+    k = idx.shape[1]
+    if D != 576 or D2 != 576 or block_table.shape[0] != B or ctx_len.shape[0] != B or idx.shape[0] != B \
+            or tuple(out.shape) != (B, H, 512) or tuple(lse.shape) != (B, H):
+        raise ValueError("inconsistent shapes")
+    ws_bytes = 0
+    if workspace is not None:
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load_library().dsa_sparse_mla_decode_paged(_ptr(q), _ptr(kv_pool), P, ps, _ptr(block_table),
+                                                      block_table.shape[1], _ptr(ctx_len), _ptr(idx), B, H, k,
+                                                      float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                                      ws_bytes, _stream(stream)))
+    return out, lse
+
+
+def dsa_get_device_status(stream=None) -> int:
+    """Read and clear the device status word (DSA_DEV_* bits)."""
+    v = ctypes.c_uint32(0)
+    _check(load_library().dsa_get_device_status(_stream(stream), ctypes.byref(v)))
+    return int(v.value)

@@ -1,0 +1,66 @@
+// Host-side interfaces between the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dsa {
+
+// Encodes a 2-D tiled tensor map (dims/box in elements, row stride in bytes).
+// Returns false and fills `err` on failure.
+bool encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t inner,
+                    uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,
+                    CUtensorMapSwizzle swizzle, char *err, size_t errlen);
+
+int num_sms();
+unsigned *device_status_ptr(); // address of this device's status word, or null
+
+struct IndexerArgs {
+    const void *q8;
+    const float *q_scale;
+    const float *w;
+    int T, HI, dI;
+    const void *k8;
+    const float *k_scale;
+    int S;
+    const int32_t *block_table;
+    int max_pages, num_pages, page_size;
+    const int32_t *q_pos;
+    float *logits;
+    int64_t ld;
+};
+// Returns 0 on success, else a dsa_status with `err` filled.
+int launch_indexer(const IndexerArgs &a, cudaStream_t stream, char *err, size_t errlen);
+
+struct TopkArgs {
+    const float *logits;
+    int64_t ld;
+    int T;
+    const int32_t *valid_len;
+    int k;
+    int32_t *idx;
+};
+int launch_topk(const TopkArgs &a, cudaStream_t stream, char *err, size_t errlen);
+
+struct MlaArgs {
+    const void *q;      // [T, H, 576] bf16
+    const void *kv;     // [S, 576] bf16, or pool [num_pages, page_size, 576]
+    int S;              // rows of kv (prefill) / num_pages * page_size (paged)
+    const int32_t *idx; // [T, k]
+    int T, H, k;
+    float sm_scale;
+    void *out;          // [T, H, 512] bf16
+    float *lse;         // [T, H]
+    // paged decode
+    const int32_t *block_table;
+    int max_pages, num_pages, page_size;
+    const int32_t *ctx_len;
+    void *workspace;
+    size_t workspace_bytes;
+};
+int launch_mla_prefill(const MlaArgs &a, cudaStream_t stream, char *err, size_t errlen);
+int launch_mla_decode(const MlaArgs &a, cudaStream_t stream, char *err, size_t errlen);
+size_t mla_decode_workspace_bytes(int B, int H, int k);
+
+} // namespace dsa

@@ -1,0 +1,193 @@
+"""GPU parity of each stage against the fp64 oracle, through the C ABI.
+
+Sizes are chosen so the oracle finishes in seconds while still spanning several
+tiles and a ragged tail (query rows, key tiles of 128, attention blocks of 64,
+pages of 64).  Seeded synthetic inputs only.
+"""
+import numpy as np
+import pytest
+import torch
+
+import dsa_workloads as W
+import oracle
+from tests.gpu_util import bits16, check_attention, check_logits, lib
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _indexer_case(cfg, L, rows=None):
+    dsa = lib()
+    x = W.prefill_inputs(cfg, DEV, L=L)
+    logits = torch.full((L, L + 3), float("nan"), device=DEV)  # ld not a multiple of 4
+    dsa.dsa_indexer_logits(x["q8"], x["qs"], x["w"], x["k8"], x["ks"], x["q_pos"], logits)
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_device_status() == 0
+    rows = np.arange(L) if rows is None else np.asarray(rows)
+    h = {k: v.cpu() for k, v in x.items()}
+    ref = oracle.indexer(h["q8"][rows].numpy(), h["qs"][rows].numpy(), h["w"][rows].numpy(), rows,
+                         h["k8"].numpy(), h["ks"].numpy(), ld=L + 3)
+    got = logits.cpu().double().numpy()[rows]
+    check_logits(got, ref, rows)
+    return x, logits
+
+
+def test_indexer_tiny_all_rows():
+    _indexer_case(W.CONFIGS["tiny"], 256)
+
+
+@pytest.mark.parametrize("L", [1, 7, 129, 700])
+def test_indexer_h64_ragged(L):
+    rng = np.random.default_rng(L)
+    rows = np.unique(np.concatenate([[0, L - 1, min(127, L - 1), min(128, L - 1)], rng.integers(0, L, 40)]))
+    _indexer_case(W.CONFIGS["prefill_4k"], L, rows)
+
+
+def test_topk_from_gpu_logits_bit_exact():
+    cfg = W.CONFIGS["tiny"]
+    dsa = lib()
+    x, logits = _indexer_case(cfg, 256)
+    for k in (1, 64, 100, 256, 300):
+        idx = torch.empty((256, k), dtype=torch.int32, device=DEV)
+        dsa.dsa_topk(logits, x["q_pos"] + 1, k, idx)
+        torch.cuda.synchronize()
+        ref = oracle.topk(np.nan_to_num(logits.cpu().double().numpy(), nan=0.0), np.arange(1, 257), k)
+        assert np.array_equal(idx.cpu().numpy(), ref), f"k={k}"
+
+
+@pytest.mark.parametrize("ld", [4099, 4096])
+def test_topk_edge_rows_and_ties(ld):
+    """Valid lengths 0, 1, k-1, k, k+1, ld; tie-heavy integer scores with -0/+0;
+    ld both aligned and unaligned (vector and scalar paths)."""
+    dsa = lib()
+    g = torch.Generator(device=DEV).manual_seed(3)
+    T = 24
+    vals = torch.randint(-20, 21, (T, ld), generator=g, device=DEV).float() * 0.5
+    vals[vals == 0] = torch.where(torch.rand((T, ld), generator=g, device=DEV) < 0.5, -0.0, 0.0)[vals == 0]
+    vals[5:10] = torch.randn((5, ld), generator=g, device=DEV)
+    k = 2048
+    n = torch.tensor([0, 1, k - 1, k, k + 1, ld, ld, 3000, 2049, 4000, 7, ld - 1] * 2, dtype=torch.int32)
+    # poison past the valid length: any read of it would change the result
+    for r in range(T):
+        vals[r, int(n[r]):] = float("nan")
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    dsa.dsa_topk(vals, n.to(DEV), k, idx)
+    torch.cuda.synchronize()
+    v = vals.cpu().double().numpy()
+    ref = oracle.topk(np.nan_to_num(v, nan=-np.inf), n.numpy(), k)
+    assert np.array_equal(idx.cpu().numpy(), ref)
+    assert dsa.dsa_get_device_status() == 0
+
+
+def test_topk_deterministic_large_row():
+    dsa = lib()
+    T, ld = 8, 131072
+    g = torch.Generator(device=DEV).manual_seed(4)
+    vals = torch.randn((T, ld), generator=g, device=DEV)
+    vals[:, ::7] = 0.25  # a large tie block straddling the threshold
+    n = torch.tensor([ld, ld - 5, 70000, 2049, 65536, 131071, 4096, 100000], dtype=torch.int32, device=DEV)
+    a = torch.empty((T, 2048), dtype=torch.int32, device=DEV)
+    b = torch.empty_like(a)
+    dsa.dsa_topk(vals, n, 2048, a)
+    dsa.dsa_topk(vals, n, 2048, b)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    ref = oracle.topk(vals.cpu().double().numpy(), n.cpu().numpy(), 2048)
+    assert np.array_equal(a.cpu().numpy(), ref)
+
+
+def _mla_case(T, S, H, k, seed, invalid_frac=0.0, rows=None):
+    dsa = lib()
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    q = torch.randn((T, H, 576), generator=g, device=DEV).to(torch.bfloat16)
+    kv = torch.randn((S, 576), generator=g, device=DEV).to(torch.bfloat16)
+    idx = torch.stack([torch.randperm(S, generator=g, device=DEV)[:k] for _ in range(T)]).int()
+    idx = torch.sort(idx, dim=1).values
+    if invalid_frac > 0:
+        drop = torch.rand((T, k), generator=g, device=DEV) < invalid_frac
+        idx[drop] = -1
+        idx[0, :] = -1          # a row with nothing valid
+        idx[1, 1:] = -1         # a row with a single valid entry
+        idx[2, 5] = S + 7       # out of range: skipped
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((T, H), dtype=torch.float32, device=DEV)
+    dsa.dsa_sparse_mla_prefill(q, kv, idx, 1 / 24, out, lse)
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_device_status() == 0
+    rows = np.arange(T) if rows is None else np.asarray(rows)
+    o_ref, l_ref = oracle.sparse_mla(bits16(q)[rows], bits16(kv), idx.cpu().numpy()[rows], 1 / 24)
+    o = out.cpu().double().numpy()[rows]
+    l = lse.cpu().double().numpy()[rows]
+    if invalid_frac > 0:
+        assert np.all(o[0] == 0) and np.all(np.isneginf(l[0]))
+    return check_attention(o, l, o_ref, l_ref)
+
+
+@pytest.mark.parametrize("H", [128, 16, 64])
+def test_mla_prefill_small(H):
+    _mla_case(T=6, S=300, H=H, k=64, seed=H)
+
+
+def test_mla_prefill_ragged_k_and_invalid():
+    _mla_case(T=5, S=1000, H=128, k=200, seed=1, invalid_frac=0.3)
+
+
+def test_mla_prefill_k2048():
+    _mla_case(T=9, S=5000, H=128, k=2048, seed=2, rows=[0, 4, 8])
+
+
+def test_pipeline_tiny_end_to_end():
+    """indexer -> top-k -> sparse MLA on the tiny workload, every row."""
+    cfg = W.CONFIGS["tiny"]
+    dsa = lib()
+    x, logits = _indexer_case(cfg, 256)
+    idx = torch.empty((256, cfg.k), dtype=torch.int32, device=DEV)
+    dsa.dsa_topk(logits, x["q_pos"] + 1, cfg.k, idx)
+    out = torch.empty((256, cfg.H, 512), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((256, cfg.H), dtype=torch.float32, device=DEV)
+    dsa.dsa_sparse_mla_prefill(x["q"], x["kv"], idx, cfg.sm_scale, out, lse)
+    torch.cuda.synchronize()
+    ref_idx = oracle.topk(np.nan_to_num(logits.cpu().double().numpy(), nan=0.0), np.arange(1, 257), cfg.k)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    o_ref, l_ref = oracle.sparse_mla(bits16(x["q"]), bits16(x["kv"]), ref_idx, cfg.sm_scale)
+    check_attention(out.cpu().double().numpy(), lse.cpu().double().numpy(), o_ref, l_ref)
+    # rows t <= 63 select every prior token: sparse equals dense there (checked in the oracle pins)
+
+
+def test_decode_paged_pipeline():
+    """Paged indexer -> top-k -> paged sparse MLA for one new token per sequence.
+
+    Context lengths cover one token, page boundaries, fewer than k and more
+    than k candidates; pages are a shuffled pool and unused slots hold NaN."""
+    cfg = W.CONFIGS["decode_paged"]
+    dsa = lib()
+    ctx = [1, 64, 65, 2047, 2048, 2049, 3001, 5000]
+    d = W.decode_inputs(cfg, DEV, ctx=ctx)
+    B = len(ctx)
+    ld = max(ctx) + 5
+    logits = torch.full((B, ld), float("nan"), device=DEV)
+    dsa.dsa_indexer_logits(d["q8"], d["qs"], d["w"], d["k8_pool"], d["ks_pool"], d["q_pos"], logits,
+                           block_table=d["block_table"])
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_device_status() == 0
+    h = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in d.items()}
+    ref = oracle.indexer_paged(h["q8"].numpy(), h["qs"].numpy(), h["w"].numpy(), h["ctx"].numpy(),
+                               h["k8_pool"].numpy(), h["ks_pool"].numpy(), h["block_table"].numpy(), ld)
+    got = logits.cpu().double().numpy()
+    check_logits(got, ref, h["q_pos"].numpy())
+    idx = torch.empty((B, cfg.k), dtype=torch.int32, device=DEV)
+    dsa.dsa_topk(logits, d["ctx"], cfg.k, idx)
+    torch.cuda.synchronize()
+    ref_idx = oracle.topk(np.nan_to_num(got, nan=0.0), h["ctx"].numpy(), cfg.k)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    out = torch.empty((B, cfg.H, 512), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((B, cfg.H), dtype=torch.float32, device=DEV)
+    ws_n = dsa.dsa_sparse_mla_decode_workspace_size(B, cfg.H, cfg.k)
+    ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device=DEV) if ws_n else None
+    dsa.dsa_sparse_mla_decode_paged(d["q"], d["kv_pool"], d["block_table"], d["ctx"], idx, cfg.sm_scale,
+                                    out, lse, workspace=ws)
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_device_status() == 0
+    o_ref, l_ref = oracle.sparse_mla_paged(bits16(d["q"]), bits16(d["kv_pool"]), h["block_table"].numpy(),
+                                           h["ctx"].numpy(), ref_idx, cfg.sm_scale)
+    check_attention(out.cpu().double().numpy(), lse.cpu().double().numpy(), o_ref, l_ref)
