@@ -155,6 +155,27 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Four rows of one 2-D tensor (rows y0..y3, innermost coordinate x) into
+// consecutive smem rows; the tensor map's box must be one row high.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t x,
+                                            int32_t y0, int32_t y1, int32_t y2, int32_t y3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
+        : "memory");
+}
+
+// Pull a tile into L2 ahead of use (no smem, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32_t c0, int32_t c1)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 // --------------------------------------------------------------- cp.async 16B
 
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src)
@@ -309,6 +330,17 @@ __device__ __forceinline__ void cluster_sync_all()
 __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d)
 {
     asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+// Asynchronous store of 16 bytes into a peer CTA's shared memory; completion
+// is counted in bytes on the peer's mbarrier (no fence needed).
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float a, float b, float c, float d,
+                                            uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     remote_addr),
+                 "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
                  : "memory");
 }
 
