@@ -65,6 +65,13 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
+// Remote arrive without a release fence (used when the data the arrival
+// announces has already been consumed, so nothing needs ordering).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_bar)
+{
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
@@ -182,6 +189,21 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src)
 {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
+
+// 16-byte copy; `bytes` = 0 reads nothing and fills the destination with zeros.
+__device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the barrier's expected count includes these arrivals).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
@@ -341,6 +363,15 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float a, float
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
                      remote_addr),
                  "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_async_v4_b32(uint32_t remote_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                                uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     remote_addr),
+                 "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
                  : "memory");
 }
 

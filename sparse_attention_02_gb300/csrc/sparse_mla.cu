@@ -13,26 +13,33 @@
 // SM's TMEM.  Each token therefore runs on a cluster of two CTAs (two SMs):
 //   CTA r keeps O[:, 256r : 256r+256) in TMEM and gathers latent columns
 //   [256r, 256r+320) of every selected row (five 64-column swizzle atoms);
-//   it computes the PARTIAL scores over latent columns [288r, 288r+288) (K-split
-//   of QK^T, no duplicated MMA work), the two CTAs swap their 128 x 64 fp32
-//   partial-score tiles through distributed shared memory, and each adds the
-//   other's half.  Both then hold the same full scores, run the same softmax
-//   (so both see identical P, m and l), and apply P to their own V half.
+//   it computes the PARTIAL scores over latent columns [288r, 288r+288) (a
+//   K-split of QK^T, no duplicated MMA work), and the two CTAs swap their
+//   partial-score tiles through distributed shared memory.  Both CTAs then
+//   add the same two halves in the same way, so they hold bit-identical
+//   scores, run the same softmax (identical P, m and l) and each applies P to
+//   its own V half.
 //
-// Per 64-key block j (double-buffered S, P and KV stage):
-//   producer warp   resolves the 64 selected rows and gathers them with TMA
-//                   gather4 (4 rows x 128 B per instruction, 16 lanes x 5 atoms);
-//                   an invalid entry re-reads the token's first valid row (an
-//                   in-bounds, finite row whose score is masked, so P = 0);
-//   MMA warp        S_j = Q_half . KV_j^T   (M=128 heads, N=64, K=288; A and B
+// The swap carries the log2-scaled partial scores rounded to fp16 (saturating,
+// 16 KB per 64-key block instead of 32 KB in fp32); each CTA rounds its own
+// half the same way before adding.  At the scores' scale (|s| of a few units
+// in log2 terms) this perturbs each softmax weight by ~2^-11 relative, below
+// the bf16 rounding of P that the PV product applies anyway.
+//
+// Per 64-key block j (double-buffered S, P and swap buffers, three KV stages):
+//   producer warps  four warps cp.async the 64 selected rows x 640 B into the
+//                   SW128 K-major layout (one 128-byte line per 8 lanes), zero-
+//                   fill invalid entries, and arrive on the stage's mbarrier as
+//                   their copies land (cp.async.mbarrier.arrive.noinc);
+//   MMA warp        S_j = Q_half . KV_j^T   (M=128 heads, N=64, K=288; A, B
 //                   K-major in smem) issued one block ahead of
 //                   O += P_j . V_j          (M=128, N=256, K=64; A = P from
 //                   TMEM, B = the same KV stage read MN-major);
-//   softmax warps   thread = head: partial S from TMEM, swap with the peer by
-//                   st.async (completion counted in bytes on the peer's
-//                   mbarrier), mask, max, exp2, running sum; P (bf16) back into
-//                   TMEM.  The running max is only moved when a block exceeds it
-//                   by more than 2^8 (then O is rescaled in TMEM), so P <= 256.
+//   softmax warps   thread = head: partial S from TMEM, st.async swap with the
+//                   peer (completion counted in bytes on the peer's mbarrier),
+//                   mask, max, exp2, running sum; P (bf16) back into TMEM.  The
+//                   running max only moves when a block exceeds it by more than
+//                   2^8 (then O is rescaled in TMEM), so P stays <= 256.
 // The kernel is persistent: each cluster walks tokens t = c, c + C, ... with
 // one barrier/TMEM setup, prefetches the next token's Q into L2, and the
 // softmax warps store a token's output (O / l in bf16, LSE from CTA 0) while
@@ -40,6 +47,7 @@
 #include "common.cuh"
 #include "launch.h"
 
+#include <cuda_fp16.h>
 #include <stdio.h>
 
 namespace dsa {
@@ -47,26 +55,33 @@ namespace {
 
 constexpr int kD = 576;
 constexpr int kDv = 512;
-constexpr int kBN = 64;        // keys per block
-constexpr int kAtoms = 5;      // 64-column atoms gathered per CTA
-constexpr int kQAtom = 128 * 128;       // bytes of one Q atom (128 rows)
-constexpr int kKVAtom = kBN * 128;      // bytes of one KV atom (64 rows)
+constexpr int kBN = 64;                  // keys per block
+constexpr int kAtoms = 5;                // 64-column atoms gathered per CTA
+constexpr int kQAtom = 128 * 128;        // bytes of one full Q atom (128 rows x 128 B, SW128)
+constexpr int kQHalf = 128 * 64;         // bytes of the half atom (128 rows x 64 B, SW64)
+constexpr int kKVAtom = kBN * 128;       // bytes of one KV atom (64 rows)
 constexpr int kStage = kAtoms * kKVAtom; // 40 KB
-constexpr int kXStride = 68;           // floats per row of the swap buffer (pad: no bank conflicts)
-constexpr int kThreads = 192;          // producer, MMA, 4 softmax warps
-constexpr float kRescaleLog2 = 8.f;    // move the running max only when exceeded by this
+constexpr int kNStage = 3;
+constexpr int kXBuf = 128 * kBN * 2;     // one swap buffer: 128 heads x 64 fp16
+constexpr int kProdWarps = 4;
+constexpr int kMmaWarp = kProdWarps;
+constexpr int kSoftWarp0 = kProdWarps + 1;
+constexpr int kThreads = 32 * (kProdWarps + 1 + 4);
+constexpr int kSoftThread0 = 32 * kSoftWarp0;
+constexpr float kRescaleLog2 = 8.f;      // move the running max only when exceeded by this
 
-constexpr int OFF_Q = 0;
-constexpr int OFF_KV = OFF_Q + kAtoms * kQAtom;          // 80 KB
-constexpr int OFF_X = OFF_KV + 2 * kStage;               // 160 KB
-constexpr int OFF_BAR = OFF_X + 128 * kXStride * 4;      // + 34 KB
-constexpr int NBAR = 20;
+constexpr int OFF_Q = 0;                                  // 4 full atoms
+constexpr int OFF_QH = OFF_Q + 4 * kQAtom;               // half atom
+constexpr int OFF_KV = OFF_QH + kQHalf;                  // 72 KB
+constexpr int OFF_X = OFF_KV + kNStage * kStage;         // 192 KB
+constexpr int OFF_BAR = OFF_X + 2 * kXBuf;               // 224 KB
+constexpr int NBAR = 24;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int kSmem = OFF_MISC + 64 + 1024;
 
 // barrier slots
-constexpr int B_KVF = 0, B_KVE = 2, B_SF = 4, B_SE = 6, B_PF = 8, B_PE = 10, B_XF = 12, B_XE = 13, B_QF = 14,
-              B_QE = 15, B_OF = 16, B_OE = 17, B_DONE = 18, B_QA = 19;
+constexpr int B_KVF = 0, B_KVE = 3, B_SF = 6, B_SE = 8, B_PF = 10, B_PE = 12, B_XF = 14, B_XE = 16, B_QF = 18,
+              B_QE = 19, B_QA = 20, B_OF = 21, B_OE = 22, B_DONE = 23;
 
 // TMEM columns
 constexpr uint32_t TM_O = 0;
@@ -75,6 +90,7 @@ constexpr uint32_t TM_P = 384;  // two buffers of 32 (bf16 pairs)
 constexpr uint32_t kTmemCols = 512;
 
 struct Params {
+    const __nv_bfloat16 *kv;   // [S, 576] or pool [num_pages * page_size, 576]
     const int32_t *idx;        // [T, k]
     int S, T, H, k;
     float scale_log2;          // sm_scale * log2(e)
@@ -124,9 +140,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return r;
 }
 
+// Two fp32 -> one f16x2 word, round to nearest even, saturating to +-65504.
+__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t w)
+{
+    return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+}
+
 template <bool PAGED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv, Params p)
+    sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qh, Params p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -146,35 +175,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     // ---- one-time setup
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(B_KVF + i), 1);
+        for (int i = 0; i < kNStage; ++i) {
+            mbar_init(bar(B_KVF + i), 32 * kProdWarps);
             mbar_init(bar(B_KVE + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_SF + i), 1);
             mbar_init(bar(B_SE + i), 4);
             mbar_init(bar(B_PF + i), 4);
             mbar_init(bar(B_PE + i), 1);
+            mbar_init(bar(B_XF + i), 1);
+            mbar_init(bar(B_XE + i), 4);
         }
-        mbar_init(bar(B_XF), 1);
-        mbar_init(bar(B_XE), 4);
         mbar_init(bar(B_QF), 1);
         mbar_init(bar(B_QE), 1);
+        mbar_init(bar(B_QA), 4);
         mbar_init(bar(B_OF), 1);
         mbar_init(bar(B_OE), 4);
         mbar_init(bar(B_DONE), 1);
-        mbar_init(bar(B_QA), 4);
         *abort_flag = 0;
         fence_mbar_init();
     }
     // Q rows >= H stay zero (their scores are computed but never stored).
     if (p.H < 128) {
-        for (int i = threadIdx.x; i < kAtoms * (128 - p.H) * 8; i += kThreads) {
-            const int a = i / ((128 - p.H) * 8), rem = i % ((128 - p.H) * 8);
-            const int row = p.H + rem / 8, c = rem % 8;
-            *reinterpret_cast<uint4 *>(smem + OFF_Q + a * kQAtom + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+        const int nz = 128 - p.H;
+        for (int i = threadIdx.x; i < 4 * nz * 8; i += kThreads) {
+            const int a = i / (nz * 8), rem = i % (nz * 8);
+            *reinterpret_cast<uint4 *>(smem + OFF_Q + a * kQAtom + (p.H + rem / 8) * 128 + (rem % 8) * 16) =
+                make_uint4(0, 0, 0, 0);
         }
+        for (int i = threadIdx.x; i < nz * 4; i += kThreads)
+            *reinterpret_cast<uint4 *>(smem + OFF_QH + (p.H + i / 4) * 64 + (i % 4) * 16) = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
     }
-    if (warp == 1)
+    if (warp == kMmaWarp)
         tmem_alloc(sbase + OFF_MISC, kTmemCols);
     tc_fence_before();
     __syncthreads();
@@ -182,130 +216,131 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == 0) {
-        // ------------------------------------------------------- producer
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_kv);
+    if (warp < kProdWarps) {
+        // ------------------------------------------------------ producers
+        // Warp pw fills rows [16 pw, 16 pw + 16) of each stage.  Lanes 0..15
+        // hold those rows' latent-row indices; one cp.async instruction moves
+        // four rows x 128 B (lane = 8 x row-in-4 + 16-byte chunk).
+        const int pw = warp;
+        const int q_row0 = 16 * pw;
+        const __nv_bfloat16 *kv_cols = p.kv + 256 * rank;
         uint32_t J = 0;
         int u = 0;
         bool ok = true;
         for (int t = cid; ok && t < p.T; t += ncl, ++u) {
             const int32_t *idx_row = p.idx + (int64_t)t * p.k;
             const int ctx = PAGED ? p.ctx_len[t] : 0;
-            // blocks up to the last in-range entry; the first one gives a fallback row
-            int last = -1, first = 0x7fffffff;
+            // blocks up to the last in-range entry
+            int last = -1;
 #pragma unroll 8
             for (int i = lane; i < p.k; i += 32)
-                if (in_range<PAGED>(p, idx_row[i], ctx)) {
+                if (in_range<PAGED>(p, idx_row[i], ctx))
                     last = i;
-                    first = first < i ? first : i;
-                }
             for (int o = 16; o > 0; o >>= 1) {
                 const int y = __shfl_xor_sync(0xffffffffu, last, o);
-                const int z = __shfl_xor_sync(0xffffffffu, first, o);
                 last = y > last ? y : last;
-                first = z < first ? z : first;
             }
             const int nb = last < 0 ? 0 : last / kBN + 1;
-            int fb_row = nb > 0 ? latent_row<PAGED>(p, t, idx_row[first], ctx) : 0;
-            if (fb_row < 0)
-                fb_row = 0;
-            // the Q buffer and the nb slot are reused: the MMA warp must be done
-            // reading Q and the softmax warps must have taken the previous token
-            if (u >= 1 && (!mbar_wait_warp(bar(B_QE), (u - 1) & 1, abort_flag, p.status) ||
-                           !mbar_wait_warp(bar(B_QA), (u - 1) & 1, abort_flag, p.status))) {
-                ok = false;
-                break;
-            }
-            if (lane == 0) {
-                nb_s[u & 1] = nb;
-                if (nb > 0) {
-                    mbar_arrive_expect_tx(bar(B_QF), kAtoms * p.H * 128);
-                    for (int a = 0; a < kAtoms; ++a)
-                        tma_load_2d(sbase + OFF_Q + a * kQAtom, &tm_q, bar(B_QF), (int)(256 * rank) + 64 * a,
-                                    t * p.H);
-                } else {
-                    mbar_arrive(bar(B_QF));
+            if (pw == 0) {
+                // the Q buffer and the nb slot are reused: the MMA warp must be
+                // done reading Q and the softmax warps must have taken the
+                // previous token
+                if (u >= 1 && (!mbar_wait_warp(bar(B_QE), (u - 1) & 1, abort_flag, p.status) ||
+                               !mbar_wait_warp(bar(B_QA), (u - 1) & 1, abort_flag, p.status))) {
+                    ok = false;
+                    break;
                 }
-                if (t + ncl < p.T)
-                    for (int a = 0; a < kAtoms; ++a)
-                        tma_prefetch_l2_2d(&tm_q, (int)(256 * rank) + 64 * a, (t + ncl) * p.H);
+                if (lane == 0) {
+                    nb_s[u & 1] = nb;
+                    const int x_half = rank == 0 ? 256 : 288;
+                    const int x_full0 = rank == 0 ? 0 : 320;
+                    if (nb > 0) {
+                        mbar_arrive_expect_tx(bar(B_QF), 4 * p.H * 128 + p.H * 64);
+                        for (int a = 0; a < 4; ++a)
+                            tma_load_2d(sbase + OFF_Q + a * kQAtom, &tm_q, bar(B_QF), x_full0 + 64 * a, t * p.H);
+                        tma_load_2d(sbase + OFF_QH, &tm_qh, bar(B_QF), x_half, t * p.H);
+                    } else {
+                        mbar_arrive(bar(B_QF));
+                    }
+                    if (t + ncl < p.T) {
+                        for (int a = 0; a < 4; ++a)
+                            tma_prefetch_l2_2d(&tm_q, x_full0 + 64 * a, (t + ncl) * p.H);
+                        tma_prefetch_l2_2d(&tm_qh, x_half, (t + ncl) * p.H);
+                    }
+                }
+                __syncwarp();
             }
-            __syncwarp();
-            // rows of block 0; each later block's rows are resolved while the
-            // stage it will use is still busy
-            auto resolve = [&](int j, int &rl, int &rh) {
-                const int i0 = j * kBN + lane, i1 = i0 + 32;
-                rl = i0 < p.k ? latent_row<PAGED>(p, t, idx_row[i0], ctx) : -1;
-                rh = i1 < p.k ? latent_row<PAGED>(p, t, idx_row[i1], ctx) : -1;
-                if (PAGED && (rl == -2 || rh == -2))
+            auto resolve = [&](int j) -> int {
+                const int i = j * kBN + q_row0 + (lane & 15);
+                const int r = i < p.k ? latent_row<PAGED>(p, t, idx_row[i], ctx) : -1;
+                if (PAGED && r == -2 && lane < 16)
                     atomicOr(p.status, DSA_DEV_BAD_PAGE);
-                if (rl < 0) rl = fb_row; // masked in the softmax
-                if (rh < 0) rh = fb_row;
+                return r;
             };
-            int r_lo = 0, r_hi = 0;
-            if (nb > 0)
-                resolve(0, r_lo, r_hi);
+            int my_row = nb > 0 ? resolve(0) : -1;
             for (int j = 0; j < nb; ++j, ++J) {
-                const int st = J & 1;
-                int rows[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int src = (4 * lane + e) & 31;
-                    const int vlo = __shfl_sync(0xffffffffu, r_lo, src);
-                    const int vhi = __shfl_sync(0xffffffffu, r_hi, src);
-                    rows[e] = lane < 8 ? vlo : vhi;
-                }
+                const int st = J % kNStage;
+                const int cur = my_row;
                 if (j + 1 < nb)
-                    resolve(j + 1, r_lo, r_hi);
-                if (J >= 2 && !mbar_wait_warp(bar(B_KVE + st), ((J >> 1) - 1) & 1, abort_flag, p.status)) {
+                    my_row = resolve(j + 1); // next block's rows, ahead of the stage wait
+                if (J >= kNStage &&
+                    !mbar_wait_warp(bar(B_KVE + st), ((J / kNStage) - 1) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 const uint32_t stage = sbase + OFF_KV + st * kStage;
-                if (lane == 0)
-                    mbar_arrive_expect_tx(bar(B_KVF + st), kStage);
-                __syncwarp();
-                if (lane < 16) {
+                const int cc = lane & 7;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int il = 4 * m + (lane >> 3);
+                    const int row = __shfl_sync(0xffffffffu, cur, il);
+                    const int rl = q_row0 + il;
+                    const __nv_bfloat16 *src = kv_cols + (int64_t)(row >= 0 ? row : 0) * kD + cc * 8;
+                    const uint32_t dst = stage + rl * 128 + ((cc ^ (rl & 7)) << 4);
+                    const uint32_t bytes = row >= 0 ? 16u : 0u;
 #pragma unroll
                     for (int a = 0; a < kAtoms; ++a)
-                        tma_gather4(stage + a * kKVAtom + lane * 4 * 128, &tm_kv, bar(B_KVF + st),
-                                    (int)(256 * rank) + 64 * a, rows[0], rows[1], rows[2], rows[3]);
+                        cp_async_16_zfill(dst + a * kKVAtom, src + a * 64, bytes);
                 }
-                __syncwarp();
+                cp_async_arrive_noinc(bar(B_KVF + st));
             }
         }
-        // drain: every copy this warp issued has landed before the CTA exits
-        if (lane == 0) {
-            for (uint32_t i = J >= 2 ? J - 2 : 0; i < J; ++i)
-                mbar_drain(bar(B_KVF + (i & 1)), (i >> 1) & 1);
-            if (u >= 1)
-                mbar_drain(bar(B_QF), (u - 1) & 1);
-        }
+        cp_async_wait_all(); // every copy this warp issued has landed before the CTA exits
+        if (pw == 0 && lane == 0 && u >= 1)
+            mbar_drain(bar(B_QF), (u - 1) & 1);
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------- MMA issuer
         constexpr uint32_t idesc_qk = idesc_f32acc(128, kBN, 1u, false, false);
         constexpr uint32_t idesc_pv = idesc_f32acc(128, 256, 1u, false, true);
-        const int ks0 = 2 * (int)rank; // first 16-column k-step of this CTA's score half
         uint32_t J = 0;
         int u = 0, v = 0;
         bool ok = true;
+        // A operand of score k-step s (16 latent columns): the SW64 half atom
+        // holds this CTA's 32 columns that do not fill a whole 64-column atom.
+        auto q_desc = [&](int s) -> uint64_t {
+            const int fs = rank == 0 ? s : s - 2; // k-step within the full atoms
+            if (fs < 0 || fs >= 16) {
+                const int hs = rank == 0 ? s - 16 : s;
+                return sdesc(sbase + OFF_QH + hs * 32, 16, 512, 4);
+            }
+            return sdesc(sbase + OFF_Q + (fs >> 2) * kQAtom + (fs & 3) * 32, 16, 1024, 2);
+        };
         auto issue_qk = [&](uint32_t Jq) -> bool {
-            const int st = Jq & 1, b = Jq & 1;
-            if (!mbar_wait_warp(bar(B_KVF + st), (Jq >> 1) & 1, abort_flag, p.status))
+            const int st = Jq % kNStage, b = Jq & 1;
+            if (!mbar_wait_warp(bar(B_KVF + st), (Jq / kNStage) & 1, abort_flag, p.status))
                 return false;
             if (Jq >= 2 && !mbar_wait_warp(bar(B_SE + b), ((Jq >> 1) - 1) & 1, abort_flag, p.status))
                 return false;
+            fence_proxy_async_smem(); // the stage was written by cp.async (generic proxy)
             tc_fence_after();
             if (lane == 0) {
                 const uint32_t stage = sbase + OFF_KV + st * kStage;
 #pragma unroll
-                for (int kk = 0; kk < 18; ++kk) {
-                    const int ks = ks0 + kk, a = ks >> 2, w = ks & 3;
-                    const uint64_t ad = sdesc(sbase + OFF_Q + a * kQAtom + w * 32, 16, 1024, 2);
-                    const uint64_t bd = sdesc(stage + a * kKVAtom + w * 32, 16, 1024, 2);
-                    umma_f16_ss(tmem + TM_S + 64 * b, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                for (int s = 0; s < 18; ++s) {
+                    const int ks = s + 2 * (int)rank; // k-step within the gathered columns
+                    const uint64_t bd = sdesc(stage + (ks >> 2) * kKVAtom + (ks & 3) * 32, 16, 1024, 2);
+                    umma_f16_ss(tmem + TM_S + 64 * b, q_desc(s), bd, idesc_qk, s > 0 ? 1u : 0u);
                 }
                 umma_commit(bar(B_SF + b));
             }
@@ -349,7 +384,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t stage = sbase + OFF_KV + b * kStage;
+                    const int st = J % kNStage;
+                    const uint32_t stage = sbase + OFF_KV + st * kStage;
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk) {
                         const uint64_t bd = sdesc(stage + kk * 16 * 128, kKVAtom, 1024, 2);
@@ -357,7 +393,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                     (j > 0 || kk > 0) ? 1u : 0u);
                     }
                     umma_commit(bar(B_PE + b));
-                    umma_commit(bar(B_KVE + b));
+                    umma_commit(bar(B_KVE + st));
                     if (j + 1 == nb)
                         umma_commit(bar(B_OF));
                 }
@@ -375,10 +411,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int quad = warp & 3;
         const int h = quad * 32 + lane;                  // head = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-        float *xrow = reinterpret_cast<float *>(smem + OFF_X) + h * kXStride;
-        const uint32_t x_remote = mapa_shared(smem_u32(xrow), peer);
-        const uint32_t xf_remote = mapa_shared(bar(B_XF), peer);
-        const uint32_t xe_remote = mapa_shared(bar(B_XE), peer);
+        const uint32_t hsw = static_cast<uint32_t>(h & 7); // swap-buffer chunk swizzle (bank spread)
+        const uint32_t x_local0 = sbase + OFF_X + h * 128;
+        const uint32_t x_remote0 = mapa_shared(x_local0, peer);
+        const uint32_t xf_remote0 = mapa_shared(bar(B_XF), peer);
+        const uint32_t xe_remote0 = mapa_shared(bar(B_XE), peer);
         uint32_t J = 0;
         int u = 0, v = 0;
         bool ok = true;
@@ -407,59 +444,69 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     raw0 = n0 < p.k ? idx_row[n0] : -1;
                     raw1 = n0 + 32 < p.k ? idx_row[n0 + 32] : -1;
                 }
-                // 1. partial scores of this CTA
+                // 1. this CTA's partial scores, log2-scaled, rounded to fp16 pairs
                 if (!mbar_wait_warp(bar(B_SF + b), (J >> 1) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                float sc[kBN];
+                uint32_t own[32];
                 {
                     uint32_t r0[32], r1[32];
                     tmem_ld32(tmem + lane_off + TM_S + 64 * b, r0);
                     tmem_ld32(tmem + lane_off + TM_S + 64 * b + 32, r1);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        sc[c] = __uint_as_float(r0[c]);
-                        sc[c + 32] = __uint_as_float(r1[c]);
+                    for (int c = 0; c < 16; ++c) {
+                        own[c] = pack_f16x2_sat(__uint_as_float(r0[2 * c]) * p.scale_log2,
+                                                __uint_as_float(r0[2 * c + 1]) * p.scale_log2);
+                        own[c + 16] = pack_f16x2_sat(__uint_as_float(r1[2 * c]) * p.scale_log2,
+                                                     __uint_as_float(r1[2 * c + 1]) * p.scale_log2);
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(bar(B_SE + b));
-                // 2. swap partial scores with the peer CTA
-                if (J >= 1 && !mbar_wait_warp<true>(bar(B_XE), (J - 1) & 1, abort_flag, p.status)) {
+                // 2. swap with the peer: its buffer b must be free (it read block J-2)
+                if (J >= 2 && !mbar_wait_warp<true>(bar(B_XE + b), ((J >> 1) - 1) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
+                const uint32_t xr = x_remote0 + b * kXBuf, xfr = xf_remote0 + 8u * b;
 #pragma unroll
-                for (int c = 0; c < kBN; c += 4)
-                    st_async_v4(x_remote + c * 4, sc[c], sc[c + 1], sc[c + 2], sc[c + 3], xf_remote);
-                if (threadIdx.x == 64)
-                    mbar_arrive_expect_tx(bar(B_XF), 128 * kBN * 4);
-                if (!mbar_wait_warp<true>(bar(B_XF), J & 1, abort_flag, p.status)) {
+                for (int c = 0; c < 8; ++c)
+                    st_async_v4_b32(xr + ((c ^ hsw) << 4), own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3],
+                                    xfr);
+                if (threadIdx.x == kSoftThread0)
+                    mbar_arrive_expect_tx(bar(B_XF + b), kXBuf);
+                if (!mbar_wait_warp<true>(bar(B_XF + b), (J >> 1) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
+                // 3. scores = own half + peer half (the same sum in both CTAs), mask, block max
+                float sc[kBN];
 #pragma unroll
-                for (int c = 0; c < kBN; c += 4) {
-                    const float4 x = *reinterpret_cast<const float4 *>(xrow + c);
-                    sc[c] += x.x;
-                    sc[c + 1] += x.y;
-                    sc[c + 2] += x.z;
-                    sc[c + 3] += x.w;
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 pw = *reinterpret_cast<const uint4 *>(smem + OFF_X + b * kXBuf + h * 128 +
+                                                                      ((c ^ hsw) << 4));
+                    const uint32_t pws[4] = {pw.x, pw.y, pw.z, pw.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 a = unpack_f16x2(own[4 * c + e]);
+                        const float2 o = unpack_f16x2(pws[e]);
+                        sc[8 * c + 2 * e] = a.x + o.x;
+                        sc[8 * c + 2 * e + 1] = a.y + o.y;
+                    }
                 }
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive_remote(xe_remote);
-                // 3. mask, block max (log2 domain)
+                    mbar_arrive_remote_relaxed(xe_remote0 + 8u * b); // our buffer b is free again
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                 for (int c = 0; c < kBN; ++c) {
                     const bool vld = ((c < 32 ? vm_lo : vm_hi) >> (c & 31)) & 1u;
-                    sc[c] = vld ? sc[c] * p.scale_log2 : -INFINITY;
+                    sc[c] = vld ? sc[c] : -INFINITY;
                     mx[c & 3] = fmaxf(mx[c & 3], sc[c]);
                 }
                 const float bmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
@@ -565,7 +612,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     cluster_sync_all(); // no CTA leaves while its peer may still touch its smem
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -586,15 +633,16 @@ int launch(const MlaArgs &a, cudaStream_t stream, char *err, size_t errlen)
         }
         attr_set[dev] = true;
     }
-    CUtensorMap tq, tkv;
+    // Q as [T*H rows, 576 cols]: 64-column boxes (SW128) and one 32-column box (SW64)
+    CUtensorMap tq, tqh;
     if (!encode_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, kD, (uint64_t)a.T * a.H, kD * 2, 64, a.H,
                         CU_TENSOR_MAP_SWIZZLE_128B, err, errlen))
         return DSA_ERR_CUDA;
-    // one row high: the box of a gather4 load
-    if (!encode_tmap_2d(&tkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.kv, kD, (uint64_t)(a.S > 0 ? a.S : 1), kD * 2, 64,
-                        1, CU_TENSOR_MAP_SWIZZLE_128B, err, errlen))
+    if (!encode_tmap_2d(&tqh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, kD, (uint64_t)a.T * a.H, kD * 2, 32, a.H,
+                        CU_TENSOR_MAP_SWIZZLE_64B, err, errlen))
         return DSA_ERR_CUDA;
     Params p;
+    p.kv = static_cast<const __nv_bfloat16 *>(a.kv);
     p.idx = a.idx;
     p.S = a.S;
     p.T = a.T;
@@ -613,17 +661,13 @@ int launch(const MlaArgs &a, cudaStream_t stream, char *err, size_t errlen)
         snprintf(err, errlen, "device status word unavailable");
         return DSA_ERR_CUDA;
     }
-    if ((int64_t)a.T * 2 > (int64_t)INT32_MAX) {
-        snprintf(err, errlen, "sparse_mla: T too large");
-        return DSA_ERR_UNSUPPORTED;
-    }
     // persistent: one cluster per pair of SMs, each walking tokens c, c + C, ...
     int clusters = num_sms() / 2;
     if (clusters > a.T)
         clusters = a.T;
     if (clusters < 1)
         clusters = 1;
-    sparse_mla_kernel<PAGED><<<dim3(2 * clusters), kThreads, kSmem, stream>>>(tq, tkv, p);
+    sparse_mla_kernel<PAGED><<<dim3(2 * clusters), kThreads, kSmem, stream>>>(tq, tqh, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(err, errlen, "sparse_mla launch: %s", cudaGetErrorString(e));
