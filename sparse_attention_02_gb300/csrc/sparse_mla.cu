@@ -31,15 +31,20 @@
 //                   SW128 K-major layout (one 128-byte line per 8 lanes), zero-
 //                   fill invalid entries, and arrive on the stage's mbarrier as
 //                   their copies land (cp.async.mbarrier.arrive.noinc);
-//   MMA warp        S_j = Q_half . KV_j^T   (M=128 heads, N=64, K=288; A, B
-//                   K-major in smem) issued one block ahead of
+//   MMA warps       S_j = Q_half . KV_j^T   (M=128 heads, N=64, K=288; A, B
+//                   K-major in smem), even and odd blocks from two warps, and
 //                   O += P_j . V_j          (M=128, N=256, K=64; A = P from
-//                   TMEM, B = the same KV stage read MN-major);
-//   softmax warps   thread = head: partial S from TMEM, st.async swap with the
-//                   peer (completion counted in bytes on the peer's mbarrier),
-//                   mask, max, exp2, running sum; P (bf16) back into TMEM.  The
-//                   running max only moves when a block exceeds it by more than
-//                   2^8 (then O is rescaled in TMEM), so P stays <= 256.
+//                   TMEM, B = the same KV stage read MN-major) from a third.
+//                   One thread serialises its tcgen05.mma issue at ~100 cycles
+//                   per instruction whatever N is, so the N=64 score MMAs need
+//                   two issuing warps to keep the tensor pipe fed;
+//   softmax warps   thread = head, two warps per TMEM lane quadrant, each with
+//                   32 of the block's keys: partial S from TMEM, st.async swap
+//                   with the peer (completion counted in bytes on the peer's
+//                   mbarrier), mask, max (agreed with the sibling warp through
+//                   a spare TMEM column), exp2, running sum; P (bf16) back into
+//                   TMEM.  The running max only moves when a block exceeds it
+//                   by more than 2^8 (then O is rescaled in TMEM), so P <= 256.
 // The kernel is persistent: each cluster walks tokens t = c, c + C, ... with
 // one barrier/TMEM setup, prefetches the next token's Q into L2, and the
 // softmax warps store a token's output (O / l in bf16, LSE from CTA 0) while
@@ -64,9 +69,11 @@ constexpr int kStage = kAtoms * kKVAtom; // 40 KB
 constexpr int kNStage = 3;
 constexpr int kXBuf = 128 * kBN * 2;     // one swap buffer: 128 heads x 64 fp16
 constexpr int kProdWarps = 4;
-constexpr int kMmaWarp = kProdWarps;
-constexpr int kSoftWarp0 = kProdWarps + 1;
-constexpr int kThreads = 32 * (kProdWarps + 1 + 4);
+constexpr int kPvWarp = kProdWarps;      // all PV MMAs (fixed accumulation order) + TMEM owner
+constexpr int kQkWarp0 = kProdWarps + 1; // score MMAs of even blocks; kQkWarp0 + 1: odd blocks
+constexpr int kSoftWarp0 = kProdWarps + 3;
+constexpr int kSoftWarps = 8;            // two per TMEM lane quadrant, 32 keys of each block apiece
+constexpr int kThreads = 32 * (kProdWarps + 3 + kSoftWarps);
 constexpr int kSoftThread0 = 32 * kSoftWarp0;
 constexpr float kRescaleLog2 = 8.f;      // move the running max only when exceeded by this
 
@@ -75,18 +82,21 @@ constexpr int OFF_QH = OFF_Q + 4 * kQAtom;               // half atom
 constexpr int OFF_KV = OFF_QH + kQHalf;                  // 72 KB
 constexpr int OFF_X = OFF_KV + kNStage * kStage;         // 192 KB
 constexpr int OFF_BAR = OFF_X + 2 * kXBuf;               // 224 KB
-constexpr int NBAR = 24;
+constexpr int NBAR = 36;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int kSmem = OFF_MISC + 64 + 1024;
 
 // barrier slots
 constexpr int B_KVF = 0, B_KVE = 3, B_SF = 6, B_SE = 8, B_PF = 10, B_PE = 12, B_XF = 14, B_XE = 16, B_QF = 18,
-              B_QE = 19, B_QA = 20, B_OF = 21, B_OE = 22, B_DONE = 23;
+              B_QE = 19, B_QA = 20, B_OF = 21, B_OE = 22, B_DONE = 23,
+              B_RB = 24,  // [quad][parity]: sibling softmax warps swapped their block max
+              B_RL = 32;  // [quad]: sibling softmax warps swapped their row sums
 
 // TMEM columns
 constexpr uint32_t TM_O = 0;
 constexpr uint32_t TM_S = 256;  // two buffers of 64
 constexpr uint32_t TM_P = 384;  // two buffers of 32 (bf16 pairs)
+constexpr uint32_t TM_RED = 448; // per-head values swapped between the two softmax warps of a quadrant
 constexpr uint32_t kTmemCols = 512;
 
 struct Params {
@@ -181,18 +191,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_SF + i), 1);
-            mbar_init(bar(B_SE + i), 4);
-            mbar_init(bar(B_PF + i), 4);
+            mbar_init(bar(B_SE + i), kSoftWarps);
+            mbar_init(bar(B_PF + i), kSoftWarps);
             mbar_init(bar(B_PE + i), 1);
             mbar_init(bar(B_XF + i), 1);
-            mbar_init(bar(B_XE + i), 4);
+            mbar_init(bar(B_XE + i), kSoftWarps);
         }
         mbar_init(bar(B_QF), 1);
-        mbar_init(bar(B_QE), 1);
-        mbar_init(bar(B_QA), 4);
+        mbar_init(bar(B_QE), 2);
+        mbar_init(bar(B_QA), kSoftWarps + 1); // softmax warps + the PV warp read each token's nb slot
         mbar_init(bar(B_OF), 1);
-        mbar_init(bar(B_OE), 4);
-        mbar_init(bar(B_DONE), 1);
+        mbar_init(bar(B_OE), kSoftWarps);
+        mbar_init(bar(B_DONE), 3);
+        for (int i = 0; i < 8; ++i)
+            mbar_init(bar(B_RB + i), 2);
+        for (int i = 0; i < 4; ++i)
+            mbar_init(bar(B_RL + i), 2);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -208,7 +222,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4 *>(smem + OFF_QH + (p.H + i / 4) * 64 + (i % 4) * 16) = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
     }
-    if (warp == kMmaWarp)
+    if (warp == kPvWarp)
         tmem_alloc(sbase + OFF_MISC, kTmemCols);
     tc_fence_before();
     __syncthreads();
@@ -309,72 +323,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (pw == 0 && lane == 0 && u >= 1)
             mbar_drain(bar(B_QF), (u - 1) & 1);
         __syncwarp();
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------- MMA issuer
-        constexpr uint32_t idesc_qk = idesc_f32acc(128, kBN, 1u, false, false);
+    } else if (warp == kPvWarp) {
+        // -------------------------------------------------- PV MMA issuer
         constexpr uint32_t idesc_pv = idesc_f32acc(128, 256, 1u, false, true);
         uint32_t J = 0;
         int u = 0, v = 0;
         bool ok = true;
-        // A operand of score k-step s (16 latent columns): the SW64 half atom
-        // holds this CTA's 32 columns that do not fill a whole 64-column atom.
-        auto q_desc = [&](int s) -> uint64_t {
-            const int fs = rank == 0 ? s : s - 2; // k-step within the full atoms
-            if (fs < 0 || fs >= 16) {
-                const int hs = rank == 0 ? s - 16 : s;
-                return sdesc(sbase + OFF_QH + hs * 32, 16, 512, 4);
-            }
-            return sdesc(sbase + OFF_Q + (fs >> 2) * kQAtom + (fs & 3) * 32, 16, 1024, 2);
-        };
-        auto issue_qk = [&](uint32_t Jq) -> bool {
-            const int st = Jq % kNStage, b = Jq & 1;
-            if (!mbar_wait_warp(bar(B_KVF + st), (Jq / kNStage) & 1, abort_flag, p.status))
-                return false;
-            if (Jq >= 2 && !mbar_wait_warp(bar(B_SE + b), ((Jq >> 1) - 1) & 1, abort_flag, p.status))
-                return false;
-            fence_proxy_async_smem(); // the stage was written by cp.async (generic proxy)
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t stage = sbase + OFF_KV + st * kStage;
-#pragma unroll
-                for (int s = 0; s < 18; ++s) {
-                    const int ks = s + 2 * (int)rank; // k-step within the gathered columns
-                    const uint64_t bd = sdesc(stage + (ks >> 2) * kKVAtom + (ks & 3) * 32, 16, 1024, 2);
-                    umma_f16_ss(tmem + TM_S + 64 * b, q_desc(s), bd, idesc_qk, s > 0 ? 1u : 0u);
-                }
-                umma_commit(bar(B_SF + b));
-            }
-            __syncwarp();
-            return true;
-        };
         for (int t = cid; ok && t < p.T; t += ncl, ++u) {
             if (!mbar_wait_warp(bar(B_QF), u & 1, abort_flag, p.status)) {
                 ok = false;
                 break;
             }
             const int nb = nb_s[u & 1];
-            if (nb == 0) {
-                if (lane == 0)
-                    umma_commit(bar(B_QE));
-                __syncwarp();
-                continue;
-            }
-            tc_fence_after();
-            if (!issue_qk(J)) {
-                ok = false;
-                break;
-            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar(B_QA));
             for (int j = 0; j < nb; ++j, ++J) {
-                if (j + 1 < nb) {
-                    if (!issue_qk(J + 1)) {
-                        ok = false;
-                        break;
-                    }
-                } else if (lane == 0) {
-                    umma_commit(bar(B_QE)); // Q no longer read once these MMAs complete
-                }
-                const int b = J & 1;
-                if (!mbar_wait_warp(bar(B_PF + b), (J >> 1) & 1, abort_flag, p.status)) {
+                const int b = J & 1, st = J % kNStage;
+                if (!mbar_wait_warp(bar(B_PF + b), (J >> 1) & 1, abort_flag, p.status) ||
+                    !mbar_wait_warp(bar(B_KVF + st), (J / kNStage) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
@@ -382,9 +349,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
+                fence_proxy_async_smem(); // the stage was written by cp.async (generic proxy)
                 tc_fence_after();
                 if (lane == 0) {
-                    const int st = J % kNStage;
                     const uint32_t stage = sbase + OFF_KV + st * kStage;
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk) {
@@ -399,7 +366,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
             }
-            ++v;
+            if (nb > 0)
+                ++v;
+        }
+        if (lane == 0) {
+            umma_commit(bar(B_DONE));
+            mbar_drain(bar(B_DONE), 0);
+        }
+        __syncwarp();
+    } else if (warp < kSoftWarp0) {
+        // -------------------------------- score MMA issuers (block parity)
+        const uint32_t par = static_cast<uint32_t>(warp - kQkWarp0);
+        constexpr uint32_t idesc_qk = idesc_f32acc(128, kBN, 1u, false, false);
+        uint32_t J = 0;
+        int u = 0;
+        bool ok = true;
+        // A operand of score k-step s (16 latent columns): the SW64 half atom
+        // holds this CTA's 32 columns that do not fill a whole 64-column atom.
+        auto q_desc = [&](int s) -> uint64_t {
+            const int fs = rank == 0 ? s : s - 2; // k-step within the full atoms
+            if (fs < 0 || fs >= 16) {
+                const int hs = rank == 0 ? s - 16 : s;
+                return sdesc(sbase + OFF_QH + hs * 32, 16, 512, 4);
+            }
+            return sdesc(sbase + OFF_Q + (fs >> 2) * kQAtom + (fs & 3) * 32, 16, 1024, 2);
+        };
+        for (int t = cid; ok && t < p.T; t += ncl, ++u) {
+            if (!mbar_wait_warp(bar(B_QF), u & 1, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            const int nb = nb_s[u & 1];
+            tc_fence_after();
+            for (int j = 0; j < nb; ++j, ++J) {
+                if ((J & 1u) != par)
+                    continue;
+                const int st = J % kNStage, b = J & 1;
+                if (!mbar_wait_warp(bar(B_KVF + st), (J / kNStage) & 1, abort_flag, p.status) ||
+                    (J >= 2 && !mbar_wait_warp(bar(B_SE + b), ((J >> 1) - 1) & 1, abort_flag, p.status))) {
+                    ok = false;
+                    break;
+                }
+                fence_proxy_async_smem(); // the stage was written by cp.async (generic proxy)
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t stage = sbase + OFF_KV + st * kStage;
+#pragma unroll
+                    for (int s = 0; s < 18; ++s) {
+                        const int ks = s + 2 * (int)rank; // k-step within the gathered columns
+                        const uint64_t bd = sdesc(stage + (ks >> 2) * kKVAtom + (ks & 3) * 32, 16, 1024, 2);
+                        umma_f16_ss(tmem + TM_S + 64 * b, q_desc(s), bd, idesc_qk, s > 0 ? 1u : 0u);
+                    }
+                    umma_commit(bar(B_SF + b));
+                }
+                __syncwarp();
+            }
+            // Q is free for the next token once this warp's score MMAs complete
+            if (lane == 0)
+                umma_commit(bar(B_QE));
+            __syncwarp();
         }
         if (lane == 0) {
             umma_commit(bar(B_DONE));
@@ -408,14 +433,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------ softmax + epilogue
+        // Warp half hf of a lane quadrant owns keys [32 hf, 32 hf + 32) of every
+        // block, O columns [128 hf, 128 hf + 128) in the epilogue and a partial
+        // row sum; the two warps agree on each block's max before exponentiating.
+        const int sw = warp - kSoftWarp0;
         const int quad = warp & 3;
+        const int hf = sw >> 2;
         const int h = quad * 32 + lane;                  // head = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t hsw = static_cast<uint32_t>(h & 7); // swap-buffer chunk swizzle (bank spread)
-        const uint32_t x_local0 = sbase + OFF_X + h * 128;
-        const uint32_t x_remote0 = mapa_shared(x_local0, peer);
+        const uint32_t x_remote0 = mapa_shared(sbase + OFF_X + h * 128, peer);
         const uint32_t xf_remote0 = mapa_shared(bar(B_XF), peer);
         const uint32_t xe_remote0 = mapa_shared(bar(B_XE), peer);
+        const uint32_t red = tmem + lane_off + TM_RED;
         uint32_t J = 0;
         int u = 0, v = 0;
         bool ok = true;
@@ -430,19 +460,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(bar(B_QA)); // this token's nb slot has been read
-            float m_run = -INFINITY; // running max, log2 domain
-            float l_run = 0.f;
-            int32_t raw0 = lane < p.k ? idx_row[lane] : -1;
-            int32_t raw1 = lane + 32 < p.k ? idx_row[lane + 32] : -1;
+            float m_run = -INFINITY; // running max, log2 domain (same in both sibling warps)
+            float l_run = 0.f;       // this warp's partial row sum
+            int32_t raw = 32 * hf + lane < p.k ? idx_row[32 * hf + lane] : -1;
             for (int j = 0; j < nb; ++j, ++J) {
                 const int b = J & 1;
-                // validity of this block's 64 entries; prefetch the next block's indices
-                const uint32_t vm_lo = __ballot_sync(0xffffffffu, latent_row<PAGED>(p, t, raw0, ctx) >= 0);
-                const uint32_t vm_hi = __ballot_sync(0xffffffffu, latent_row<PAGED>(p, t, raw1, ctx) >= 0);
+                // validity of this warp's 32 entries; prefetch the next block's index
+                const uint32_t vmask = __ballot_sync(0xffffffffu, latent_row<PAGED>(p, t, raw, ctx) >= 0);
                 {
-                    const int n0 = (j + 1) * kBN + lane;
-                    raw0 = n0 < p.k ? idx_row[n0] : -1;
-                    raw1 = n0 + 32 < p.k ? idx_row[n0 + 32] : -1;
+                    const int n0 = (j + 1) * kBN + 32 * hf + lane;
+                    raw = n0 < p.k ? idx_row[n0] : -1;
                 }
                 // 1. this CTA's partial scores, log2-scaled, rounded to fp16 pairs
                 if (!mbar_wait_warp(bar(B_SF + b), (J >> 1) & 1, abort_flag, p.status)) {
@@ -450,18 +477,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                uint32_t own[32];
+                uint32_t own[16];
                 {
-                    uint32_t r0[32], r1[32];
-                    tmem_ld32(tmem + lane_off + TM_S + 64 * b, r0);
-                    tmem_ld32(tmem + lane_off + TM_S + 64 * b + 32, r1);
+                    uint32_t r0[16], r1[16];
+                    tmem_ld16(tmem + lane_off + TM_S + 64 * b + 32 * hf, r0);
+                    tmem_ld16(tmem + lane_off + TM_S + 64 * b + 32 * hf + 16, r1);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
+                    for (int c = 0; c < 8; ++c) {
                         own[c] = pack_f16x2_sat(__uint_as_float(r0[2 * c]) * p.scale_log2,
                                                 __uint_as_float(r0[2 * c + 1]) * p.scale_log2);
-                        own[c + 16] = pack_f16x2_sat(__uint_as_float(r1[2 * c]) * p.scale_log2,
-                                                     __uint_as_float(r1[2 * c + 1]) * p.scale_log2);
+                        own[c + 8] = pack_f16x2_sat(__uint_as_float(r1[2 * c]) * p.scale_log2,
+                                                    __uint_as_float(r1[2 * c + 1]) * p.scale_log2);
                     }
                 }
                 tc_fence_before();
@@ -475,21 +502,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 const uint32_t xr = x_remote0 + b * kXBuf, xfr = xf_remote0 + 8u * b;
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    st_async_v4_b32(xr + ((c ^ hsw) << 4), own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3],
-                                    xfr);
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t cc = 4u * hf + c;
+                    st_async_v4_b32(xr + ((cc ^ hsw) << 4), own[4 * c], own[4 * c + 1], own[4 * c + 2],
+                                    own[4 * c + 3], xfr);
+                }
                 if (threadIdx.x == kSoftThread0)
                     mbar_arrive_expect_tx(bar(B_XF + b), kXBuf);
                 if (!mbar_wait_warp<true>(bar(B_XF + b), (J >> 1) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
-                // 3. scores = own half + peer half (the same sum in both CTAs), mask, block max
-                float sc[kBN];
+                // 3. scores = own half + peer half (the same sum in both CTAs), mask
+                float sc[32];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t cc = 4u * hf + c;
                     const uint4 pw = *reinterpret_cast<const uint4 *>(smem + OFF_X + b * kXBuf + h * 128 +
-                                                                      ((c ^ hsw) << 4));
+                                                                      ((cc ^ hsw) << 4));
                     const uint32_t pws[4] = {pw.x, pw.y, pw.z, pw.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -504,14 +534,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     mbar_arrive_remote_relaxed(xe_remote0 + 8u * b); // our buffer b is free again
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int c = 0; c < kBN; ++c) {
-                    const bool vld = ((c < 32 ? vm_lo : vm_hi) >> (c & 31)) & 1u;
-                    sc[c] = vld ? sc[c] : -INFINITY;
+                for (int c = 0; c < 32; ++c) {
+                    sc[c] = ((vmask >> c) & 1u) ? sc[c] : -INFINITY;
                     mx[c & 3] = fmaxf(mx[c & 3], sc[c]);
                 }
-                const float bmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-                // 4. move the running max only when it is exceeded by more than 2^8
-                //    (per head; the TMEM rescale below is warp-collective)
+                const float hmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                // 4. block max over both halves: swap through a spare TMEM column
+                tmem_st1(red + 2 * b + hf, __float_as_uint(hmax));
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(bar(B_RB + 2 * quad + b));
+                if (!mbar_wait_warp(bar(B_RB + 2 * quad + b), (J >> 1) & 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t omax_bits = tmem_ld1(red + 2 * b + (hf ^ 1));
+                tmem_ld_wait();
+                const float bmax = fmaxf(hmax, __uint_as_float(omax_bits));
+                // 5. move the running max only when it is exceeded by more than 2^8
+                //    (same decision in both sibling warps; each rescales its O half)
                 float alpha = 1.f;
                 bool scale_o = false;
                 if (bmax > m_run + kRescaleLog2) {
@@ -530,7 +574,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
 #pragma unroll 1
-                    for (int c0 = 0; c0 < 256; c0 += 32) {
+                    for (int c0 = 128 * hf; c0 < 128 * hf + 128; c0 += 32) {
                         uint32_t r[32];
                         tmem_ld32(tmem + lane_off + TM_O + c0, r);
                         tmem_ld_wait();
@@ -542,11 +586,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tmem_st_wait();
                 }
                 const float m_use = m_run == -INFINITY ? 0.f : m_run;
-                // 5. P = exp2(S - m), running sum, bf16 pairs into TMEM
-                uint32_t pk[32];
+                // 6. P = exp2(S - m), partial sum, bf16 pairs into this warp's half of P
+                uint32_t pk[16];
                 float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int c = 0; c < kBN; c += 2) {
+                for (int c = 0; c < 32; c += 2) {
                     const float p0 = fast_exp2(sc[c] - m_use);
                     const float p1 = fast_exp2(sc[c + 1] - m_use);
                     ls[(c >> 1) & 3] += p0 + p1;
@@ -558,7 +602,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                tmem_st32(tmem + lane_off + TM_P + 32 * b, pk);
+                tmem_st16(tmem + lane_off + TM_P + 32 * b + 16 * hf, pk);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -567,9 +611,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             if (!ok)
                 break;
-            // ---- epilogue: O / l -> bf16, LSE
+            // ---- epilogue: row sum of both halves (fixed order), O / l -> bf16, LSE
+            tmem_st1(red + 4 + 2 * (u & 1) + hf, __float_as_uint(l_run));
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar(B_RL + quad));
+            if (!mbar_wait_warp(bar(B_RL + quad), u & 1, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float l_other = __uint_as_float(tmem_ld1(red + 4 + 2 * (u & 1) + (hf ^ 1)));
+            tmem_ld_wait();
+            const float l_tot = hf == 0 ? l_run + l_other : l_other + l_run;
             const bool store = h < p.H;
-            __nv_bfloat16 *orow = p.out + ((int64_t)t * p.H + h) * kDv + 256 * rank;
+            __nv_bfloat16 *orow = p.out + ((int64_t)t * p.H + h) * kDv + 256 * rank + 128 * hf;
             if (nb > 0) {
                 if (!mbar_wait_warp(bar(B_OF), v & 1, abort_flag, p.status)) {
                     ok = false;
@@ -577,11 +635,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 ++v;
                 tc_fence_after();
-                const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+                const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
 #pragma unroll 1
-                for (int c0 = 0; c0 < 256; c0 += 32) {
+                for (int c0 = 0; c0 < 128; c0 += 32) {
                     uint32_t r[32];
-                    tmem_ld32(tmem + lane_off + TM_O + c0, r);
+                    tmem_ld32(tmem + lane_off + TM_O + 128 * hf + c0, r);
                     tmem_ld_wait();
                     uint32_t o[16];
 #pragma unroll
@@ -600,19 +658,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     mbar_arrive(bar(B_OE));
             } else if (store) {
                 uint4 *dst = reinterpret_cast<uint4 *>(orow);
-                for (int c = 0; c < 256 / 8; ++c)
+                for (int c = 0; c < 128 / 8; ++c)
                     dst[c] = make_uint4(0, 0, 0, 0);
             }
-            if (store && rank == 0)
+            if (store && rank == 0 && hf == 0)
                 p.lse[(int64_t)t * p.H + h] =
-                    l_run > 0.f ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+                    l_tot > 0.f ? (m_run + __log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
         }
     }
 
     tc_fence_before();
     __syncthreads();
     cluster_sync_all(); // no CTA leaves while its peer may still touch its smem
-    if (warp == kMmaWarp) {
+    if (warp == kPvWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
