@@ -326,6 +326,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp == kPvWarp) {
         // -------------------------------------------------- PV MMA issuer
         constexpr uint32_t idesc_pv = idesc_f32acc(128, 256, 1u, false, true);
+        // B of PV k-step kk: 16 keys further down the stage (kk * 16 rows * 128 B = kk * 128 units)
+        const uint64_t pv_desc0 = sdesc(sbase + OFF_KV, kKVAtom, 1024, 2);
         uint32_t J = 0;
         int u = 0, v = 0;
         bool ok = true;
@@ -352,13 +354,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem(); // the stage was written by cp.async (generic proxy)
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t stage = sbase + OFF_KV + st * kStage;
+                    const uint64_t vd = pv_desc0 + static_cast<uint64_t>((st * kStage) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk) {
-                        const uint64_t bd = sdesc(stage + kk * 16 * 128, kKVAtom, 1024, 2);
-                        umma_f16_ts(tmem + TM_O, tmem + TM_P + 32 * b + 8 * kk, bd, idesc_pv,
-                                    (j > 0 || kk > 0) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        umma_f16_ts(tmem + TM_O, tmem + TM_P + 32 * b + 8 * kk, vd + static_cast<uint64_t>(kk * 128),
+                                    idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
                     umma_commit(bar(B_PE + b));
                     umma_commit(bar(B_KVE + st));
                     if (j + 1 == nb)
@@ -381,16 +381,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t J = 0;
         int u = 0;
         bool ok = true;
-        // A operand of score k-step s (16 latent columns): the SW64 half atom
-        // holds this CTA's 32 columns that do not fill a whole 64-column atom.
-        auto q_desc = [&](int s) -> uint64_t {
+        // Descriptors are precomputed once: the issue loop below is one add and
+        // one tcgen05.mma per k-step (the issuing warp shares its SMSP with busy
+        // softmax and producer warps).  A operand of score k-step s (16 latent
+        // columns): the SW64 half atom holds this CTA's 32 columns that do not
+        // fill a whole 64-column atom.
+        uint64_t qd[18];
+        uint32_t bofs[18]; // B offset of k-step s within a KV stage, 16-byte units
+#pragma unroll
+        for (int s = 0; s < 18; ++s) {
             const int fs = rank == 0 ? s : s - 2; // k-step within the full atoms
             if (fs < 0 || fs >= 16) {
                 const int hs = rank == 0 ? s - 16 : s;
-                return sdesc(sbase + OFF_QH + hs * 32, 16, 512, 4);
+                qd[s] = sdesc(sbase + OFF_QH + hs * 32, 16, 512, 4);
+            } else {
+                qd[s] = sdesc(sbase + OFF_Q + (fs >> 2) * kQAtom + (fs & 3) * 32, 16, 1024, 2);
             }
-            return sdesc(sbase + OFF_Q + (fs >> 2) * kQAtom + (fs & 3) * 32, 16, 1024, 2);
-        };
+            const int ks = s + 2 * (int)rank; // k-step within the gathered columns
+            bofs[s] = static_cast<uint32_t>(((ks >> 2) * kKVAtom + (ks & 3) * 32) >> 4);
+        }
+        const uint64_t kv_desc0 = sdesc(sbase + OFF_KV, 16, 1024, 2);
         for (int t = cid; ok && t < p.T; t += ncl, ++u) {
             if (!mbar_wait_warp(bar(B_QF), u & 1, abort_flag, p.status)) {
                 ok = false;
@@ -410,13 +420,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem(); // the stage was written by cp.async (generic proxy)
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t stage = sbase + OFF_KV + st * kStage;
+                    const uint64_t sd = kv_desc0 + static_cast<uint64_t>((st * kStage) >> 4);
+                    const uint32_t d_tmem = tmem + TM_S + 64 * b;
+                    umma_f16_ss(d_tmem, qd[0], sd + bofs[0], idesc_qk, 0u);
 #pragma unroll
-                    for (int s = 0; s < 18; ++s) {
-                        const int ks = s + 2 * (int)rank; // k-step within the gathered columns
-                        const uint64_t bd = sdesc(stage + (ks >> 2) * kKVAtom + (ks & 3) * 32, 16, 1024, 2);
-                        umma_f16_ss(tmem + TM_S + 64 * b, q_desc(s), bd, idesc_qk, s > 0 ? 1u : 0u);
-                    }
+                    for (int s = 1; s < 18; ++s)
+                        umma_f16_ss(d_tmem, qd[s], sd + bofs[s], idesc_qk, 1u);
                     umma_commit(bar(B_SF + b));
                 }
                 __syncwarp();
