@@ -139,6 +139,18 @@ def recorded_traffic(name: str, sources):
     return d.get("dram_bytes_per_launch")
 
 
+def aggregate_over_ranks(ms_local: float, tokens_local: int, dist=None, device=None):
+    """Whole-job timing: the slowest rank's ms per step and all ranks' tokens per second."""
+    ms = float(ms_local)
+    world = 1
+    if dist is not None and dist.is_initialized():
+        world = dist.get_world_size()
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * tokens_local / (ms / 1e3)
+
+
 # ------------------------------------------------------------ CPU baseline
 
 def oracle_sample(cfg: W.Config, rows: np.ndarray, x):
@@ -406,11 +418,7 @@ def main():
     status = dsa.dsa_get_device_status()
 
     stage_ms = st.mean(0)
-    ms = float(st.sum(1).mean())
-    if dist:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms, value = aggregate_over_ranks(float(st.sum(1).mean()), L, dist, dev)
     work = prefill_work(L, cfg.k, cfg.HI, cfg.dI, cfg.H)
     bf16_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     fp8_peak = FP8_OVER_BF16 * bf16_peak
@@ -429,7 +437,7 @@ def main():
 
     line = {
         "metric": METRIC,
-        "value": world * L / (ms / 1e3),
+        "value": value,
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,

@@ -1,0 +1,82 @@
+"""C ABI checks that need no GPU: every declared symbol is exported, and bad
+arguments are rejected on the host (before any CUDA call) with a message."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_attention_02_gb300 import build
+
+    path = build.build()
+    import sparse_attention_02_gb300 as dsa
+
+    return dsa.load_library(path)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"dsa_indexer_logits", "dsa_topk", "dsa_sparse_mla_prefill", "dsa_sparse_mla_decode_paged"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in dsa.h but not exported"
+
+
+def test_version_and_workspace_query(lib):
+    assert lib.dsa_version() >= 100
+    assert lib.dsa_sparse_mla_decode_workspace_size(64, 128, 2048) == 0
+    assert lib.dsa_sparse_mla_decode_workspace_size(64, 129, 2048) == 0  # unsupported H: 0
+
+
+def _err(lib):
+    return lib.dsa_last_error().decode()
+
+
+def test_host_validation_rejects_bad_arguments(lib):
+    P = ctypes.c_void_p
+    fake = P(4096)  # never dereferenced: every call below fails its host checks first
+    # top-k: k out of range, null pointers, T < 0; T == 0 is a no-op
+    assert lib.dsa_topk(fake, 16, 4, fake, 0, fake, None) == 2
+    assert "k must be" in _err(lib)
+    assert lib.dsa_topk(None, 16, 4, fake, 8, fake, None) == 1
+    assert lib.dsa_topk(fake, 16, -1, fake, 8, fake, None) == 1
+    assert lib.dsa_topk(fake, 16, 0, fake, 8, fake, None) == 0
+    assert lib.dsa_topk(fake, 1 << 29, 4, fake, 8, fake, None) == 2
+    # indexer: misaligned q8, bad page size, missing S
+    assert lib.dsa_indexer_logits(P(4097), fake, fake, 4, 64, 128, fake, fake, 16, None, 0, 0, 0, fake, fake, 16,
+                                  None) == 3
+    assert lib.dsa_indexer_logits(fake, fake, fake, 4, 64, 128, fake, fake, 16, fake, 4, 4, 48, fake, fake, 16,
+                                  None) == 2
+    assert lib.dsa_indexer_logits(fake, fake, fake, 4, 64, 128, fake, fake, 0, None, 0, 0, 0, fake, fake, 16,
+                                  None) == 1
+    assert lib.dsa_indexer_logits(fake, fake, fake, 0, 64, 128, fake, fake, 16, None, 0, 0, 0, fake, fake, 16,
+                                  None) == 0
+    # sparse MLA: heads out of range, non-positive scale, misaligned output
+    f = ctypes.c_float
+    assert lib.dsa_sparse_mla_prefill(fake, fake, 8, fake, 4, 129, 64, f(0.04), fake, fake, None) == 2
+    assert lib.dsa_sparse_mla_prefill(fake, fake, 8, fake, 4, 128, 64, f(0.0), fake, fake, None) == 1
+    assert lib.dsa_sparse_mla_prefill(fake, fake, 8, fake, 4, 128, 64, f(0.04), P(4098), fake, None) == 3
+    assert lib.dsa_sparse_mla_prefill(fake, fake, 8, fake, 0, 128, 64, f(0.04), fake, fake, None) == 0
+    # paged decode: workspace check and misaligned pool
+    assert lib.dsa_sparse_mla_decode_paged(fake, P(4100), 4, 64, fake, 2, fake, fake, 2, 128, 64, f(0.04), fake,
+                                           fake, None, 0, None) == 3
+    assert lib.dsa_sparse_mla_decode_paged(fake, fake, 0, 64, fake, 2, fake, fake, 2, 128, 64, f(0.04), fake,
+                                           fake, None, 0, None) == 1
+
+
+def test_binding_raises_without_the_library(tmp_path):
+    import sparse_attention_02_gb300 as dsa
+
+    with pytest.raises(RuntimeError, match="missing"):
+        dsa.load_library(str(tmp_path / "nope.so"))
