@@ -20,7 +20,8 @@
  * quantity is computed from its formula in fp64 after decoding the stored FP8
  * and BF16 bits with this file's own decoders.  Rows (and heads) are
  * independent, so any subset of query rows can be computed exactly; OpenMP
- * only splits the outer loop.
+ * only splits independent loops (the keys of an index row, rows and heads of
+ * attention).
  *
  * Only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline leg may
  * load this library.  It shares no code, header, table or constant with the
@@ -119,13 +120,13 @@ void dsa_oracle_indexer(const uint8_t *q8, const float *q_scale, const float *w,
                         const uint8_t *k8, const float *k_scale, int S,
                         double *out, int64_t ld)
 {
-#pragma omp parallel for schedule(dynamic, 1)
     for (int r = 0; r < n; ++r) {
         const uint8_t *q8t = q8 + (int64_t)r * HI * dI;
         const float *wt = w + (int64_t)r * HI;
         int last = q_pos[r];
         if (last > S - 1)
             last = S - 1;
+#pragma omp parallel for schedule(dynamic, 64)
         for (int s = 0; s <= last; ++s)
             out[(int64_t)r * ld + s] =
                 index_score(q8t, q_scale[r], wt, HI, dI, k8 + (int64_t)s * dI, k_scale[s]);
@@ -146,15 +147,15 @@ void dsa_oracle_indexer_paged(const uint8_t *q8, const float *q_scale, const flo
                               const int32_t *block_table, int max_pages,
                               double *out, int64_t ld)
 {
-#pragma omp parallel for schedule(dynamic, 1)
     for (int r = 0; r < n; ++r) {
         const uint8_t *q8t = q8 + (int64_t)r * HI * dI;
         const float *wt = w + (int64_t)r * HI;
-        for (int s = 0; s < ctx_len[r]; ++s) {
-            int logical_page = s / page_size;
-            if (logical_page >= max_pages)
-                break;
-            int page = block_table[(int64_t)r * max_pages + logical_page];
+        int len = ctx_len[r];
+        if (len > max_pages * page_size)
+            len = max_pages * page_size;
+#pragma omp parallel for schedule(dynamic, 64)
+        for (int s = 0; s < len; ++s) {
+            int page = block_table[(int64_t)r * max_pages + s / page_size];
             if (page < 0 || page >= num_pages)
                 continue;
             int64_t slot = (int64_t)page * page_size + s % page_size;

@@ -88,20 +88,29 @@ def _need(t: torch.Tensor, dtype, name: str, dim: int | None = None):
         raise ValueError(f"{name}: expected {dim} dims, got {t.dim()}")
 
 
+def _need_rows(t: torch.Tensor, dtype, name: str):
+    """A 2-D tensor whose rows may be strided (leading dimension >= width)."""
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or not t.is_cuda or t.dim() != 2:
+        raise TypeError(f"{name}: expected a 2-D CUDA {dtype} tensor")
+    if t.stride(1) != 1 or t.stride(0) < t.shape[1]:
+        raise ValueError(f"{name}: rows must be contiguous with a leading dimension >= width")
+
+
 def dsa_indexer_logits(q8, q_scale, w, k8, k_scale, q_pos, logits, block_table=None, stream=None):
     """Lightning-indexer scores into ``logits`` [T, ld] (fp32).
 
     q8 uint8 [T, H_I, d_I] (E4M3 codes), q_scale fp32 [T], w fp32 [T, H_I], q_pos int32 [T].
     Contiguous keys: k8 uint8 [S, d_I], k_scale fp32 [S].  Paged keys: k8 uint8
     [num_pages, page_size, d_I], k_scale fp32 [num_pages, page_size] and
-    block_table int32 [T, max_pages].
+    block_table int32 [T, max_pages].  ``logits`` rows may be strided
+    (leading dimension = logits.stride(0)).
     """
     _need(q8, torch.uint8, "q8", 3)
     T, HI, dI = q8.shape
     _need(q_scale, torch.float32, "q_scale", 1)
     _need(w, torch.float32, "w", 2)
     _need(q_pos, torch.int32, "q_pos", 1)
-    _need(logits, torch.float32, "logits", 2)
+    _need_rows(logits, torch.float32, "logits")
     _need(k8, torch.uint8, "k8")
     _need(k_scale, torch.float32, "k_scale")
     if q_scale.shape[0] != T or tuple(w.shape) != (T, HI) or q_pos.shape[0] != T or logits.shape[0] != T:
@@ -125,8 +134,9 @@ def dsa_indexer_logits(q8, q_scale, w, k8, k_scale, q_pos, logits, block_table=N
 
 
 def dsa_topk(logits, valid_len, k: int, idx, stream=None):
-    """Top-k indices (ascending, -1 padded) of each row of ``logits`` [T, ld] into ``idx`` [T, k]."""
-    _need(logits, torch.float32, "logits", 2)
+    """Top-k indices (ascending, -1 padded) of each row of ``logits`` [T, >= max valid_len]
+    (rows may be strided) into ``idx`` [T, k]."""
+    _need_rows(logits, torch.float32, "logits")
     _need(valid_len, torch.int32, "valid_len", 1)
     _need(idx, torch.int32, "idx", 2)
     T = logits.shape[0]
