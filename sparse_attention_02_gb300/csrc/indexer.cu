@@ -23,9 +23,11 @@
 //   warp 0      TMA producer: the CTA's query tiles once, then key tiles
 //               through an NSTAGE ring (paged: one TMA per page of the tile).
 //   warp 1      TMEM allocator and MMA issuer (one elected lane).
-//   warps 2..   epilogue: TMEM -> registers, ReLU, weighted head sum, key
-//               scale, masked store.  Two TMEM accumulators alternate so the
-//               MMA of one item overlaps the epilogue of the other.
+//   warps 2..   epilogue, up to four warps per TMEM lane quadrant: TMEM ->
+//               registers (all columns in flight, one wait), ReLU, weighted
+//               head sum (w read as float4 broadcasts), key scale, masked
+//               store.  Two TMEM accumulators alternate so the MMA of one item
+//               overlaps the epilogue of the other.
 #include "common.cuh"
 #include "launch.h"
 
@@ -42,7 +44,7 @@ struct IdxCfg {
     static constexpr int NGROUP = PAGED ? 1 : 2;          // token groups sharing a key tile
     static constexpr int R = G * NGROUP;                  // query rows per CTA
     static constexpr int N = G * HI;                      // MMA N
-    static constexpr int EPI_SPLIT = N >= 128 ? 2 : 1;    // warps per TMEM lane quadrant
+    static constexpr int EPI_SPLIT = N >= 256 ? 4 : (N >= 128 ? 2 : 1); // warps per TMEM lane quadrant
     static constexpr int NEPI = 4 * EPI_SPLIT;            // epilogue warps
     static constexpr int THREADS = 64 + 32 * NEPI;
     static constexpr int NSTAGE = PAGED ? 6 : 4;
@@ -282,26 +284,33 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI, PAGED>::THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                float acc[C::TPT];
-#pragma unroll
-                for (int t = 0; t < C::TPT; ++t)
-                    acc[t] = 0.f;
                 const int row_base = g * C::G + half * C::TPT; // CTA-local row of token 0
                 const uint32_t cbase = lane_base + a * C::ACC_COLS + half * C::NC;
+                // all of this thread's columns in flight at once, one wait; the
+                // accumulator is released as soon as the values are in registers
+                uint32_t r[C::NC];
 #pragma unroll
-                for (int c0 = 0; c0 < C::NC; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(cbase + c0, r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int col = c0 + j;
-                        const int t = col / HI, h = col % HI;
-                        acc[t] = fmaf(fmaxf(__uint_as_float(r[j]), 0.f), wq_s[(row_base + t) * HI + h], acc[t]);
-                    }
-                }
+                for (int c0 = 0; c0 < C::NC; c0 += 32)
+                    tmem_ld32(cbase + c0, *reinterpret_cast<uint32_t(*)[32]>(r + c0));
+                tmem_ld_wait();
                 tc_fence_before();
                 mbar_arrive(acce_bar(a));
+                float acc[C::TPT];
+#pragma unroll
+                for (int t = 0; t < C::TPT; ++t) {
+                    const float4 *w4 = reinterpret_cast<const float4 *>(wq_s + (row_base + t) * HI);
+                    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                    for (int h4 = 0; h4 < HI / 4; ++h4) {
+                        const float4 wv = w4[h4];
+                        const int col = t * HI + 4 * h4;
+                        a0 = fmaf(fmaxf(__uint_as_float(r[col]), 0.f), wv.x, a0);
+                        a1 = fmaf(fmaxf(__uint_as_float(r[col + 1]), 0.f), wv.y, a1);
+                        a0 = fmaf(fmaxf(__uint_as_float(r[col + 2]), 0.f), wv.z, a0);
+                        a1 = fmaf(fmaxf(__uint_as_float(r[col + 3]), 0.f), wv.w, a1);
+                    }
+                    acc[t] = a0 + a1;
+                }
                 if (key_ok) {
 #pragma unroll
                     for (int t = 0; t < C::TPT; ++t) {
