@@ -15,22 +15,25 @@
 //     A = 128 key rows of k8   (K-major, TMA tile, swizzle = d_I bytes)
 //     B = N query rows of q8   (row = token * H_I + head, K-major)
 //     D = TMEM [128 lanes = keys] x [N columns = (token, head)] fp32
-// With keys on the lanes, the sum over heads is a loop over the columns a
-// thread reads from its own TMEM lane, and the 32 threads of a warp store 32
-// consecutive keys of a logits row (128 coalesced bytes).
+// With keys on the lanes, the sum over heads runs along a thread's own TMEM
+// columns.
 //
 // Roles (one CTA, warp-specialised):
 //   warp 0      TMA producer: the CTA's query tiles once, then key tiles
 //               through an NSTAGE ring (paged: one TMA per page of the tile).
 //   warp 1      TMEM allocator and MMA issuer (one elected lane).
-//   warps 2..   epilogue, up to four warps per TMEM lane quadrant: TMEM ->
-//               registers (all columns in flight, one wait), ReLU, weighted
-//               head sum (w read as float4 broadcasts), key scale, masked
-//               store.  Two TMEM accumulators alternate so the MMA of one item
-//               overlaps the epilogue of the other.
+//   warps 2..   epilogue, up to four warps per TMEM lane quadrant.  Two TMEM
+//               accumulators alternate so the MMA of one item overlaps the
+//               epilogue of the other.  For H_I a multiple of 8 the epilogue
+//               reads 16-lane x 256-bit fragments: each thread holds two keys
+//               and a fixed quarter of every 8-column block, so its head
+//               weights stay in registers; the head sum ends in a four-lane
+//               shuffle reduce.  Otherwise (H_I = 4) each thread owns one key
+//               lane and reads the weights from shared memory.
 #include "common.cuh"
 #include "launch.h"
 
+#include <limits.h>
 #include <stdio.h>
 
 namespace dsa {
@@ -40,16 +43,29 @@ constexpr int kTileKeys = 128;
 
 template <int HI, int DI, bool PAGED>
 struct IdxCfg {
+    // Fragment epilogue (16x256b TMEM loads, head weights held in registers)
+    // whenever each token's head block is a whole number of 8-column repeats.
+    static constexpr bool FRAG = HI % 8 == 0;
     static constexpr int G = PAGED ? 1 : 256 / HI;        // tokens per accumulator
-    static constexpr int NGROUP = PAGED ? 1 : 2;          // token groups sharing a key tile
+    static constexpr int NGROUP = (PAGED || FRAG) ? 1 : 2; // token groups sharing a key tile
     static constexpr int R = G * NGROUP;                  // query rows per CTA
     static constexpr int N = G * HI;                      // MMA N
     static constexpr int EPI_SPLIT = N >= 256 ? 4 : (N >= 128 ? 2 : 1); // warps per TMEM lane quadrant
     static constexpr int NEPI = 4 * EPI_SPLIT;            // epilogue warps
     static constexpr int THREADS = 64 + 32 * NEPI;
-    static constexpr int NSTAGE = PAGED ? 6 : 4;
-    static constexpr int NC = N / EPI_SPLIT;              // TMEM columns per epilogue thread
-    static constexpr int TPT = NC / HI;                   // tokens per epilogue thread
+    static constexpr int NSTAGE = PAGED ? 6 : (NGROUP == 1 ? 8 : 4); // key tiles in flight
+    // 32x32b epilogue: TMEM columns and tokens per thread
+    static constexpr int NC = N / EPI_SPLIT;
+    static constexpr int TPT = NC / HI;
+    // fragment epilogue: lane halves per warp, columns per warp, 8-column
+    // repeats per warp, tokens per warp, repeats per token, 64-column chunks
+    static constexpr int NLH = EPI_SPLIT >= 2 ? 1 : 2;
+    static constexpr int NCW = N / (EPI_SPLIT >= 2 ? EPI_SPLIT / 2 : 1);
+    static constexpr int REPS = NCW / 8;
+    static constexpr int TPW = NCW / HI;
+    static constexpr int RPT = HI / 8;
+    static constexpr int CHUNK_REPS = REPS >= 8 ? 8 : REPS;
+    static constexpr int NCHUNK = REPS / CHUNK_REPS;
     static constexpr int QTILE = N * DI;                  // bytes
     static constexpr int KSTAGE = kTileKeys * DI;         // bytes
     static constexpr int ACC_COLS = N < 32 ? 32 : N;
@@ -65,9 +81,16 @@ struct IdxCfg {
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 64 + 1024; // + slack for 1024-B alignment of the base
     static_assert(N >= 16 && N <= 256 && N % 16 == 0, "MMA N");
-    static_assert(NC % 32 == 0 && NC % HI == 0, "epilogue split");
+    static_assert(FRAG || (NC % 32 == 0 && NC % HI == 0), "epilogue split");
+    static_assert(!FRAG || ((CHUNK_REPS == 8 || CHUNK_REPS == 4) && REPS % CHUNK_REPS == 0 && TPW >= 1 &&
+                            (TPW == 1 || TPW % 2 == 0) && CHUNK_REPS % RPT == 0), "fragment epilogue split");
     static_assert(DI == 32 || DI == 64 || DI == 128, "d_I");
 };
+
+// In the fragment epilogue every kAbsEvery-th column repeat forms ReLU(x) * w
+// as (x + |x|) * (w / 2), which is the same rounded product and FMA, on the FMA
+// pipe instead of the ALU pipe that carries the max of the other repeats.
+constexpr int kAbsEvery = 4;
 
 struct Params {
     const float *q_scale;
@@ -134,7 +157,7 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI, PAGED>::THREADS, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(accf_bar(a), 1);
-            mbar_init(acce_bar(a), C::NEPI * 32);
+            mbar_init(acce_bar(a), C::NEPI); // one arrival per epilogue warp
         }
         mbar_init(q_bar, 1);
         mbar_init(done_bar, 1);
@@ -253,6 +276,181 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI, PAGED>::THREADS, 1)
             mbar_drain(done_bar, 0);
         }
         __syncwarp();
+    } else if constexpr (C::FRAG) {
+        // ------------------------------------------- epilogue (fragment form)
+        // Warp (quad, j) reads TMEM lanes quad*32 + 16*lh .. +16 and the column
+        // block [cb, cb + NCW).  Thread (g, tq) = (lane / 4, lane % 4) holds keys
+        // g and g + 8 of that lane half and, of every 8-column repeat, the two
+        // columns 2*tq and 2*tq + 1, so its head weights are fixed for the whole
+        // CTA and live in registers; the two keys share them.  The sum over the
+        // heads finishes with a reduce-scatter over the four lanes of a group:
+        // afterwards lane (g, tq) owns key g + 8*(tq >> 1).
+        //
+        // TMEM is read in 32-column chunks through two register buffers: the
+        // load of chunk k+1 is in flight while chunk k is summed, and the first
+        // chunk of the next item is loaded before this item's reduce and store.
+        constexpr int CPL = C::REPS / 4;      // chunks per lane half
+        constexpr int NCH = C::NLH * CPL;     // chunks per item
+        static_assert(NCH % 2 == 0, "chunk double buffer");
+        const int quad = warp & 3;
+        const int j = (warp - 2) >> 2;
+        const int lh0 = C::NLH == 1 ? (j & 1) : 0;
+        const int cb = (C::NLH == 1 ? (j >> 1) : 0) * C::NCW;
+        const int tb = cb / HI; // CTA-local row of the warp's first token
+        const int g = lane >> 2, tq = lane & 3;
+        const int b1 = tq >> 1, b0 = tq & 1;
+        uint64_t w2[C::REPS];
+#pragma unroll
+        for (int m = 0; m < C::REPS; ++m) {
+            const int c = cb + 8 * m + 2 * tq;
+            const float sc = (m % kAbsEvery == kAbsEvery - 1) ? 0.5f : 1.f;
+            w2[m] = f32x2_pack(wq_s[c] * sc, wq_s[c + 1] * sc);
+        }
+        auto chunk_addr = [&](int acc_slot, int k) -> uint32_t {
+            const int lh = C::NLH == 1 ? lh0 : k / CPL;
+            return tmem + (static_cast<uint32_t>(quad * 32 + 16 * lh) << 16) + acc_slot * C::ACC_COLS + cb +
+                   32 * (k % CPL);
+        };
+        // the key this thread stores for each lane half of tile kt and its scale;
+        // a key without storage (past S, or on a missing page) gets INT_MAX, which
+        // fails every causal test below
+        auto key_info = [&](int kt, int (&sk)[C::NLH], float (&ksc)[C::NLH]) {
+#pragma unroll
+            for (int l = 0; l < C::NLH; ++l) {
+                const int lh = C::NLH == 1 ? lh0 : l;
+                const int s = kt * kTileKeys + quad * 32 + 16 * lh + g + 8 * b1;
+                bool kok;
+                if (!PAGED) {
+                    kok = s < p.S;
+                    ksc[l] = kok ? p.k_scale[s] : 0.f;
+                } else {
+                    const int lp = s / p.page_size;
+                    const int page = lp < p.max_pages ? p.block_table[(int64_t)r0 * p.max_pages + lp] : -1;
+                    kok = page >= 0 && page < p.num_pages;
+                    if (!kok && s <= pos_s[0])
+                        atomicOr(p.status, DSA_DEV_BAD_PAGE);
+                    ksc[l] = kok ? p.k_scale[(int64_t)page * p.page_size + s % p.page_size] : 0.f;
+                }
+                sk[l] = kok ? s : INT_MAX;
+            }
+        };
+        uint32_t buf0[16], buf1[16];
+        // key index and scale of the current item and the next two (loads in flight)
+        int skey[C::NLH], skey1[C::NLH];
+        float ks[C::NLH], ks1[C::NLH];
+        key_info(kt0, skey, ks);
+        if (ntiles > 1)
+            key_info(kt0 + 1, skey1, ks1);
+        bool ok = mbar_wait_warp(accf_bar(0), 0, abort_flag, p.status);
+        if (ok) {
+            tc_fence_after();
+            tmem_ld16x256b_x4(chunk_addr(0, 0), buf0);
+        }
+        for (int it = 0; ok && it < ntiles; ++it) {
+            const int a = it & 1;
+            int skey2[C::NLH];
+            float ks2[C::NLH];
+            if (it + 2 < ntiles)
+                key_info(kt0 + it + 2, skey2, ks2);
+            uint64_t acc[C::NLH][2][C::TPW];
+#pragma unroll
+            for (int l = 0; l < C::NLH; ++l)
+#pragma unroll
+                for (int row = 0; row < 2; ++row)
+#pragma unroll
+                    for (int t = 0; t < C::TPW; ++t)
+                        acc[l][row][t] = 0ull;
+#pragma unroll
+            for (int k = 0; k < NCH; ++k) {
+                uint32_t(&cur)[16] = (k & 1) ? buf1 : buf0;
+                uint32_t(&nxt)[16] = (k & 1) ? buf0 : buf1;
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    asm volatile("" : "+r"(cur[i])); // consumers stay behind the wait
+                if (k == NCH - 1) {
+                    // every chunk of this item is in the warp's registers
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(acce_bar(a));
+                }
+                if (k + 1 < NCH) {
+                    tmem_ld16x256b_x4(chunk_addr(a, k + 1), nxt);
+                } else if (it + 1 < ntiles) {
+                    if (mbar_wait_warp(accf_bar(a ^ 1), ((it + 1) >> 1) & 1, abort_flag, p.status)) {
+                        tc_fence_after();
+                        tmem_ld16x256b_x4(chunk_addr(a ^ 1, 0), nxt);
+                    } else {
+                        ok = false;
+                    }
+                }
+                const int l = k / CPL;
+#pragma unroll
+                for (int mm = 0; mm < 4; ++mm) {
+                    const int m = (k % CPL) * 4 + mm;
+                    const int tc = m / C::RPT;
+#pragma unroll
+                    for (int row = 0; row < 2; ++row) {
+                        float x0 = __uint_as_float(cur[4 * mm + 2 * row]);
+                        float x1 = __uint_as_float(cur[4 * mm + 2 * row + 1]);
+                        if (m % kAbsEvery == kAbsEvery - 1) {
+                            x0 = x0 + fabsf(x0);
+                            x1 = x1 + fabsf(x1);
+                        } else {
+                            x0 = fmaxf(x0, 0.f);
+                            x1 = fmaxf(x1, 0.f);
+                        }
+                        f32x2_fma(acc[l][row][tc], f32x2_pack(x0, x1), w2[m]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int l = 0; l < C::NLH; ++l) {
+                // reduce-scatter over lanes tq = 0..3: bit 1 picks the key row,
+                // bit 0 the half of the token list
+                float u[C::TPW];
+#pragma unroll
+                for (int i = 0; i < C::TPW; ++i) {
+                    const float2 e0 = f32x2_unpack(acc[l][0][i]);
+                    const float2 e1 = f32x2_unpack(acc[l][1][i]);
+                    const float v0 = e0.x + e0.y, v1 = e1.x + e1.y;
+                    const float keep = b1 ? v1 : v0;
+                    const float send = b1 ? v0 : v1;
+                    u[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+                }
+                constexpr int H = C::TPW >= 2 ? C::TPW / 2 : 1;
+                float y[H];
+                if constexpr (C::TPW >= 2) {
+#pragma unroll
+                    for (int i = 0; i < H; ++i) {
+                        const float keep = b0 ? u[H + i] : u[i];
+                        const float send = b0 ? u[i] : u[H + i];
+                        y[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+                    }
+                } else {
+                    y[0] = u[0] + __shfl_xor_sync(0xffffffffu, u[0], 1);
+                }
+                const int s = skey[l];
+                if (C::TPW >= 2 || b0 == 0) {
+#pragma unroll
+                    for (int i = 0; i < H; ++i) {
+                        const int lr = tb + (C::TPW >= 2 ? b0 * H : 0) + i;
+                        const int rg = r0 + lr;
+                        if (rg < p.T && s <= pos_s[lr])
+                            p.logits[(int64_t)rg * p.ld + s] = y[i] * ks[l];
+                    }
+                }
+            }
+#pragma unroll
+            for (int l = 0; l < C::NLH; ++l) {
+                skey[l] = skey1[l];
+                ks[l] = ks1[l];
+                skey1[l] = skey2[l];
+                ks1[l] = ks2[l];
+            }
+        }
+        tmem_ld_wait(); // no load of this warp outlives the loop
     } else {
         // --------------------------------------------------------- epilogue
         const int quad = warp & 3;
@@ -294,7 +492,9 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI, PAGED>::THREADS, 1)
                     tmem_ld32(cbase + c0, *reinterpret_cast<uint32_t(*)[32]>(r + c0));
                 tmem_ld_wait();
                 tc_fence_before();
-                mbar_arrive(acce_bar(a));
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(acce_bar(a));
                 float acc[C::TPT];
 #pragma unroll
                 for (int t = 0; t < C::TPT; ++t) {
