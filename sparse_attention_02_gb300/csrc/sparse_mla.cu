@@ -38,13 +38,20 @@
 //                   One thread serialises its tcgen05.mma issue at ~100 cycles
 //                   per instruction whatever N is, so the N=64 score MMAs need
 //                   two issuing warps to keep the tensor pipe fed;
+//   sender warps    thread = head, one warp per TMEM lane quadrant: the
+//                   block's partial S from TMEM, log2-scaled and rounded to
+//                   fp16 pairs, st.async to the peer (completion counted in
+//                   bytes on the peer's mbarrier) and parked in the block's P
+//                   columns.  They run ahead of the softmax, so the swap of one
+//                   block overlaps the softmax of the previous one and the
+//                   softmax warps never stall on the slow DSMEM stores;
 //   softmax warps   thread = head, two warps per TMEM lane quadrant, each with
-//                   32 of the block's keys: partial S from TMEM, st.async swap
-//                   with the peer (completion counted in bytes on the peer's
-//                   mbarrier), mask, max (agreed with the sibling warp through
-//                   a spare TMEM column), exp2, running sum; P (bf16) back into
-//                   TMEM.  The running max only moves when a block exceeds it
-//                   by more than 2^8 (then O is rescaled in TMEM), so P <= 256.
+//                   32 of the block's keys: own half from the P columns, peer
+//                   half from the swap buffer, mask, max (agreed with the
+//                   sibling warp through a spare TMEM column), exp2, running
+//                   sum; P (bf16) back into TMEM over the parked half.  The
+//                   running max only moves when a block exceeds it by more
+//                   than 2^8 (then O is rescaled in TMEM), so P <= 256.
 // The kernel is persistent: each cluster walks tokens t = c, c + C, ... with
 // one barrier/TMEM setup, prefetches the next token's Q into L2, and the
 // softmax warps store a token's output (O / l in bf16, LSE from CTA 0) while
@@ -71,9 +78,11 @@ constexpr int kXBuf = 128 * kBN * 2;     // one swap buffer: 128 heads x 64 fp16
 constexpr int kProdWarps = 4;
 constexpr int kPvWarp = kProdWarps;      // all PV MMAs (fixed accumulation order) + TMEM owner
 constexpr int kQkWarp0 = kProdWarps + 1; // score MMAs of even blocks; kQkWarp0 + 1: odd blocks
-constexpr int kSoftWarp0 = kProdWarps + 3;
+constexpr int kSendWarp0 = kProdWarps + 3;
+constexpr int kSendWarps = 4;            // one per TMEM lane quadrant: partial scores out to the peer
+constexpr int kSoftWarp0 = kSendWarp0 + kSendWarps;
 constexpr int kSoftWarps = 8;            // two per TMEM lane quadrant, 32 keys of each block apiece
-constexpr int kThreads = 32 * (kProdWarps + 3 + kSoftWarps);
+constexpr int kThreads = 32 * (kSoftWarp0 + kSoftWarps);
 constexpr int kSoftThread0 = 32 * kSoftWarp0;
 constexpr float kRescaleLog2 = 8.f;      // move the running max only when exceeded by this
 
@@ -82,7 +91,7 @@ constexpr int OFF_QH = OFF_Q + 4 * kQAtom;               // half atom
 constexpr int OFF_KV = OFF_QH + kQHalf;                  // 72 KB
 constexpr int OFF_X = OFF_KV + kNStage * kStage;         // 192 KB
 constexpr int OFF_BAR = OFF_X + 2 * kXBuf;               // 224 KB
-constexpr int NBAR = 36;
+constexpr int NBAR = 38;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int kSmem = OFF_MISC + 64 + 1024;
 
@@ -90,7 +99,8 @@ constexpr int kSmem = OFF_MISC + 64 + 1024;
 constexpr int B_KVF = 0, B_KVE = 3, B_SF = 6, B_SE = 8, B_PF = 10, B_PE = 12, B_XF = 14, B_XE = 16, B_QF = 18,
               B_QE = 19, B_QA = 20, B_OF = 21, B_OE = 22, B_DONE = 23,
               B_RB = 24,  // [quad][parity]: sibling softmax warps swapped their block max
-              B_RL = 32;  // [quad]: sibling softmax warps swapped their row sums
+              B_RL = 32,  // [quad]: sibling softmax warps swapped their row sums
+              B_PK = 36;  // [parity]: senders parked the block's own fp16 partial scores in its P buffer
 
 // TMEM columns
 constexpr uint32_t TM_O = 0;
@@ -191,7 +201,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_SF + i), 1);
-            mbar_init(bar(B_SE + i), kSoftWarps);
+            mbar_init(bar(B_SE + i), kSendWarps);
+            mbar_init(bar(B_PK + i), kSendWarps);
             mbar_init(bar(B_PF + i), kSoftWarps);
             mbar_init(bar(B_PE + i), 1);
             mbar_init(bar(B_XF + i), 1);
@@ -199,7 +210,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         mbar_init(bar(B_QF), 1);
         mbar_init(bar(B_QE), 2);
-        mbar_init(bar(B_QA), kSoftWarps + 1); // softmax warps + the PV warp read each token's nb slot
+        mbar_init(bar(B_QA), kSoftWarps + kSendWarps + 1); // softmax, sender and PV warps read each token's nb slot
         mbar_init(bar(B_OF), 1);
         mbar_init(bar(B_OE), kSoftWarps);
         mbar_init(bar(B_DONE), 3);
@@ -374,7 +385,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_drain(bar(B_DONE), 0);
         }
         __syncwarp();
-    } else if (warp < kSoftWarp0) {
+    } else if (warp < kSendWarp0) {
         // -------------------------------- score MMA issuers (block parity)
         const uint32_t par = static_cast<uint32_t>(warp - kQkWarp0);
         constexpr uint32_t idesc_qk = idesc_f32acc(128, kBN, 1u, false, false);
@@ -440,6 +451,76 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_drain(bar(B_DONE), 0);
         }
         __syncwarp();
+    } else if (warp < kSoftWarp0) {
+        // ------------------------------------------------- score senders
+        // Thread = head (TMEM lane), all 64 keys of each block: this CTA's
+        // partial scores, log2-scaled and rounded to fp16 pairs, go to the peer
+        // by st.async (completion counted in bytes on the peer's mbarrier) and
+        // into this CTA's P buffer of the block, where the softmax warps read
+        // them back; the P buffer is free once PV of block J - 2 is done.
+        const int quad = warp & 3;
+        const int h = quad * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t hsw = static_cast<uint32_t>(h & 7); // swap-buffer chunk swizzle (bank spread)
+        const uint32_t x_remote0 = mapa_shared(sbase + OFF_X + h * 128, peer);
+        const uint32_t xf_remote0 = mapa_shared(bar(B_XF), peer);
+        uint32_t J = 0;
+        int u = 0;
+        bool ok = true;
+        for (int t = cid; ok && t < p.T; t += ncl, ++u) {
+            if (!mbar_wait_warp(bar(B_QF), u & 1, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            const int nb = nb_s[u & 1];
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar(B_QA)); // this token's nb slot has been read
+            for (int j = 0; j < nb; ++j, ++J) {
+                const int b = J & 1;
+                if (!mbar_wait_warp(bar(B_SF + b), (J >> 1) & 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t own[32];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_off + TM_S + 64 * b + 32 * hh, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        own[16 * hh + c] = pack_f16x2_sat(__uint_as_float(r[2 * c]) * p.scale_log2,
+                                                          __uint_as_float(r[2 * c + 1]) * p.scale_log2);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(bar(B_SE + b));
+                // the peer's buffer b must be free (its softmax warps read block J-2)
+                if (J >= 2 && !mbar_wait_warp<true>(bar(B_XE + b), ((J >> 1) - 1) & 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t xr = x_remote0 + b * kXBuf, xfr = xf_remote0 + 8u * b;
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc)
+                    st_async_v4_b32(xr + ((static_cast<uint32_t>(cc) ^ hsw) << 4), own[4 * cc], own[4 * cc + 1],
+                                    own[4 * cc + 2], own[4 * cc + 3], xfr);
+                if (J >= 2 && !mbar_wait_warp(bar(B_PE + b), ((J >> 1) - 1) & 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                tmem_st32(tmem + lane_off + TM_P + 32 * b, own);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(bar(B_PK + b));
+            }
+        }
     } else {
         // ------------------------------------------------ softmax + epilogue
         // Warp half hf of a lane quadrant owns keys [32 hf, 32 hf + 32) of every
@@ -451,8 +532,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int h = quad * 32 + lane;                  // head = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t hsw = static_cast<uint32_t>(h & 7); // swap-buffer chunk swizzle (bank spread)
-        const uint32_t x_remote0 = mapa_shared(sbase + OFF_X + h * 128, peer);
-        const uint32_t xf_remote0 = mapa_shared(bar(B_XF), peer);
         const uint32_t xe_remote0 = mapa_shared(bar(B_XE), peer);
         const uint32_t red = tmem + lane_off + TM_RED;
         uint32_t J = 0;
@@ -480,42 +559,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int n0 = (j + 1) * kBN + 32 * hf + lane;
                     raw = n0 < p.k ? idx_row[n0] : -1;
                 }
-                // 1. this CTA's partial scores, log2-scaled, rounded to fp16 pairs
-                if (!mbar_wait_warp(bar(B_SF + b), (J >> 1) & 1, abort_flag, p.status)) {
+                // 1. this CTA's partial scores (fp16 pairs parked by the senders) and the peer's half
+                if (!mbar_wait_warp(bar(B_PK + b), (J >> 1) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 uint32_t own[16];
-                {
-                    uint32_t r0[16], r1[16];
-                    tmem_ld16(tmem + lane_off + TM_S + 64 * b + 32 * hf, r0);
-                    tmem_ld16(tmem + lane_off + TM_S + 64 * b + 32 * hf + 16, r1);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        own[c] = pack_f16x2_sat(__uint_as_float(r0[2 * c]) * p.scale_log2,
-                                                __uint_as_float(r0[2 * c + 1]) * p.scale_log2);
-                        own[c + 8] = pack_f16x2_sat(__uint_as_float(r1[2 * c]) * p.scale_log2,
-                                                    __uint_as_float(r1[2 * c + 1]) * p.scale_log2);
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(bar(B_SE + b));
-                // 2. swap with the peer: its buffer b must be free (it read block J-2)
-                if (J >= 2 && !mbar_wait_warp<true>(bar(B_XE + b), ((J >> 1) - 1) & 1, abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t xr = x_remote0 + b * kXBuf, xfr = xf_remote0 + 8u * b;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint32_t cc = 4u * hf + c;
-                    st_async_v4_b32(xr + ((cc ^ hsw) << 4), own[4 * c], own[4 * c + 1], own[4 * c + 2],
-                                    own[4 * c + 3], xfr);
-                }
+                tmem_ld16(tmem + lane_off + TM_P + 32 * b + 16 * hf, own);
+                tmem_ld_wait();
+                // arm buffer b for the peer's half of block J (its bytes may already be landing);
+                // this thread has seen the phase of block J-2 complete
                 if (threadIdx.x == kSoftThread0)
                     mbar_arrive_expect_tx(bar(B_XF + b), kXBuf);
                 if (!mbar_wait_warp<true>(bar(B_XF + b), (J >> 1) & 1, abort_flag, p.status)) {
@@ -606,11 +660,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     pk[c >> 1] = pack_bf16x2(p0, p1);
                 }
                 l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-                if (J >= 2 && !mbar_wait_warp(bar(B_PE + b), ((J >> 1) - 1) & 1, abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
+                // P over this warp's parked half (the P buffer was freed before the senders parked)
                 tmem_st16(tmem + lane_off + TM_P + 32 * b + 16 * hf, pk);
                 tmem_st_wait();
                 tc_fence_before();
