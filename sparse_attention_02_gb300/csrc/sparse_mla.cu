@@ -26,7 +26,8 @@
 // in log2 terms) this perturbs each softmax weight by ~2^-11 relative, below
 // the bf16 rounding of P that the PV product applies anyway.
 //
-// Per 64-key block j (double-buffered S, P and swap buffers, three KV stages):
+// Per 64-key block j (double-buffered S and swap buffers, three P buffers,
+// three KV stages):
 //   producer warps  four warps cp.async the 64 selected rows x 640 B into the
 //                   SW128 K-major layout (one 128-byte line per 8 lanes), zero-
 //                   fill invalid entries, and arrive on the stage's mbarrier as
@@ -91,22 +92,24 @@ constexpr int OFF_QH = OFF_Q + 4 * kQAtom;               // half atom
 constexpr int OFF_KV = OFF_QH + kQHalf;                  // 72 KB
 constexpr int OFF_X = OFF_KV + kNStage * kStage;         // 192 KB
 constexpr int OFF_BAR = OFF_X + 2 * kXBuf;               // 224 KB
-constexpr int NBAR = 38;
+constexpr int NBAR = 41;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int kSmem = OFF_MISC + 64 + 1024;
 
 // barrier slots
-constexpr int B_KVF = 0, B_KVE = 3, B_SF = 6, B_SE = 8, B_PF = 10, B_PE = 12, B_XF = 14, B_XE = 16, B_QF = 18,
-              B_QE = 19, B_QA = 20, B_OF = 21, B_OE = 22, B_DONE = 23,
-              B_RB = 24,  // [quad][parity]: sibling softmax warps swapped their block max
-              B_RL = 32,  // [quad]: sibling softmax warps swapped their row sums
-              B_PK = 36;  // [parity]: senders parked the block's own fp16 partial scores in its P buffer
+// [parity] for S and swap buffers, [J % kNP] for P buffers
+constexpr int kNP = 3; // P buffers in TMEM
+constexpr int B_KVF = 0, B_KVE = 3, B_SF = 6, B_SE = 8, B_XF = 10, B_XE = 12, B_PF = 14, B_PE = 17,
+              B_PK = 20,  // senders parked the block's own fp16 partial scores in its P buffer
+              B_QF = 23, B_QE = 24, B_QA = 25, B_OF = 26, B_OE = 27, B_DONE = 28,
+              B_RB = 29,  // [quad][parity]: sibling softmax warps swapped their block max
+              B_RL = 37;  // [quad]: sibling softmax warps swapped their row sums
 
 // TMEM columns
 constexpr uint32_t TM_O = 0;
 constexpr uint32_t TM_S = 256;  // two buffers of 64
-constexpr uint32_t TM_P = 384;  // two buffers of 32 (bf16 pairs)
-constexpr uint32_t TM_RED = 448; // per-head values swapped between the two softmax warps of a quadrant
+constexpr uint32_t TM_P = 384;  // kNP buffers of 32 (bf16 pairs)
+constexpr uint32_t TM_RED = 480; // per-head values swapped between the two softmax warps of a quadrant
 constexpr uint32_t kTmemCols = 512;
 
 struct Params {
@@ -202,11 +205,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_SF + i), 1);
             mbar_init(bar(B_SE + i), kSendWarps);
+            mbar_init(bar(B_XF + i), 1);
+            mbar_init(bar(B_XE + i), kSoftWarps);
+        }
+        for (int i = 0; i < kNP; ++i) {
             mbar_init(bar(B_PK + i), kSendWarps);
             mbar_init(bar(B_PF + i), kSoftWarps);
             mbar_init(bar(B_PE + i), 1);
-            mbar_init(bar(B_XF + i), 1);
-            mbar_init(bar(B_XE + i), kSoftWarps);
         }
         mbar_init(bar(B_QF), 1);
         mbar_init(bar(B_QE), 2);
@@ -352,8 +357,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (lane == 0)
                 mbar_arrive(bar(B_QA));
             for (int j = 0; j < nb; ++j, ++J) {
-                const int b = J & 1, st = J % kNStage;
-                if (!mbar_wait_warp(bar(B_PF + b), (J >> 1) & 1, abort_flag, p.status) ||
+                const int pb = J % kNP, st = J % kNStage;
+                if (!mbar_wait_warp(bar(B_PF + pb), (J / kNP) & 1, abort_flag, p.status) ||
                     !mbar_wait_warp(bar(B_KVF + st), (J / kNStage) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
@@ -368,9 +373,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint64_t vd = pv_desc0 + static_cast<uint64_t>((st * kStage) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk)
-                        umma_f16_ts(tmem + TM_O, tmem + TM_P + 32 * b + 8 * kk, vd + static_cast<uint64_t>(kk * 128),
+                        umma_f16_ts(tmem + TM_O, tmem + TM_P + 32 * pb + 8 * kk, vd + static_cast<uint64_t>(kk * 128),
                                     idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-                    umma_commit(bar(B_PE + b));
+                    umma_commit(bar(B_PE + pb));
                     umma_commit(bar(B_KVE + st));
                     if (j + 1 == nb)
                         umma_commit(bar(B_OF));
@@ -457,7 +462,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // partial scores, log2-scaled and rounded to fp16 pairs, go to the peer
         // by st.async (completion counted in bytes on the peer's mbarrier) and
         // into this CTA's P buffer of the block, where the softmax warps read
-        // them back; the P buffer is free once PV of block J - 2 is done.
+        // them back; P buffer J % kNP is free once PV of block J - kNP is done.
         const int quad = warp & 3;
         const int h = quad * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
@@ -508,17 +513,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int cc = 0; cc < 8; ++cc)
                     st_async_v4_b32(xr + ((static_cast<uint32_t>(cc) ^ hsw) << 4), own[4 * cc], own[4 * cc + 1],
                                     own[4 * cc + 2], own[4 * cc + 3], xfr);
-                if (J >= 2 && !mbar_wait_warp(bar(B_PE + b), ((J >> 1) - 1) & 1, abort_flag, p.status)) {
+                const int pb = J % kNP;
+                if (J >= kNP && !mbar_wait_warp(bar(B_PE + pb), ((J / kNP) - 1) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                tmem_st32(tmem + lane_off + TM_P + 32 * b, own);
+                tmem_st32(tmem + lane_off + TM_P + 32 * pb, own);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(bar(B_PK + b));
+                    mbar_arrive(bar(B_PK + pb));
             }
         }
     } else {
@@ -560,13 +566,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     raw = n0 < p.k ? idx_row[n0] : -1;
                 }
                 // 1. this CTA's partial scores (fp16 pairs parked by the senders) and the peer's half
-                if (!mbar_wait_warp(bar(B_PK + b), (J >> 1) & 1, abort_flag, p.status)) {
+                const int pb = J % kNP;
+                if (!mbar_wait_warp(bar(B_PK + pb), (J / kNP) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 uint32_t own[16];
-                tmem_ld16(tmem + lane_off + TM_P + 32 * b + 16 * hf, own);
+                tmem_ld16(tmem + lane_off + TM_P + 32 * pb + 16 * hf, own);
                 tmem_ld_wait();
                 // arm buffer b for the peer's half of block J (its bytes may already be landing);
                 // this thread has seen the phase of block J-2 complete
@@ -631,7 +638,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 l_run *= alpha;
                 if (__any_sync(0xffffffffu, scale_o)) {
                     // O holds this token's blocks < j (j >= 1 here): wait for PV_{J-1}, scale rows
-                    if (!mbar_wait_warp(bar(B_PE + ((J - 1) & 1)), ((J - 1) >> 1) & 1, abort_flag, p.status)) {
+                    if (!mbar_wait_warp(bar(B_PE + (J - 1) % kNP), ((J - 1) / kNP) & 1, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
@@ -661,12 +668,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
                 // P over this warp's parked half (the P buffer was freed before the senders parked)
-                tmem_st16(tmem + lane_off + TM_P + 32 * b + 16 * hf, pk);
+                tmem_st16(tmem + lane_off + TM_P + 32 * pb + 16 * hf, pk);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(bar(B_PF + b));
+                    mbar_arrive(bar(B_PF + pb));
             }
             if (!ok)
                 break;
