@@ -24,12 +24,13 @@
 //   warp 1      TMEM allocator and MMA issuer (one elected lane).
 //   warps 2..   epilogue, up to four warps per TMEM lane quadrant.  Two TMEM
 //               accumulators alternate so the MMA of one item overlaps the
-//               epilogue of the other.  For H_I a multiple of 8 the epilogue
-//               reads 16-lane x 256-bit fragments: each thread holds two keys
-//               and a fixed quarter of every 8-column block, so its head
-//               weights stay in registers; the head sum ends in a four-lane
-//               shuffle reduce.  Otherwise (H_I = 4) each thread owns one key
-//               lane and reads the weights from shared memory.
+//               epilogue of the other.  Contiguous keys with H_I a multiple of
+//               8 (prefill): the epilogue reads 16-lane x 256-bit fragments,
+//               each thread holds two keys and a fixed quarter of every
+//               8-column block, so its head weights stay in registers; the
+//               head sum ends in a four-lane shuffle reduce.  Otherwise (paged
+//               decode, H_I = 4) each thread owns one key lane and reads the
+//               weights from shared memory.
 #include "common.cuh"
 #include "launch.h"
 
@@ -45,7 +46,7 @@ template <int HI, int DI, bool PAGED>
 struct IdxCfg {
     // Fragment epilogue (16x256b TMEM loads, head weights held in registers)
     // whenever each token's head block is a whole number of 8-column repeats.
-    static constexpr bool FRAG = HI % 8 == 0;
+    static constexpr bool FRAG = HI % 8 == 0 && !PAGED;
     static constexpr int G = PAGED ? 1 : 256 / HI;        // tokens per accumulator
     static constexpr int NGROUP = (PAGED || FRAG) ? 1 : 2; // token groups sharing a key tile
     static constexpr int R = G * NGROUP;                  // query rows per CTA
