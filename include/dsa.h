@@ -102,7 +102,8 @@ int dsa_get_device_status(dsa_stream_t stream, uint32_t *status_out);
  *   S is ignored.  Each row is its own sequence.  An out-of-range page id is
  *   skipped (its logits are left unwritten) and flagged DSA_DEV_BAD_PAGE.
  *
- * Supported sizes: (H_I, d_I) in {(64,128), (32,128), (4,32), (8,64), (16,64)};
+ * Supported sizes: (H_I, d_I) = (64,128) or (32,128), contiguous or paged;
+ * (4,32) contiguous only; any other pair returns DSA_ERR_UNSUPPORTED.
  * page_size in {32, 64, 128}; T >= 0 (T = 0 is a no-op).
  * Alignment: q8 and k8 16-byte aligned; ld_logits >= 1.
  */
@@ -148,8 +149,9 @@ int dsa_topk(const float *logits, int64_t ld, int T, const int32_t *valid_len,
  *
  *   q    [T, H, 576] bf16;  kv [S, 576] bf16;  idx [T, k] int32
  *   out  [T, H, 512] bf16 (rounded to nearest even);  lse [T, H] fp32
- * Supported: H = 128 or 64 or 16... see dsa_sparse_mla_supported(); D = 576,
- * Dv = 512 fixed; 1 <= k <= 4096.  q, kv, out 16-byte aligned.
+ * Supported: 1 <= H <= 128 (fewer than 128 heads run as zero-padded rows
+ * that are never stored); D = 576, Dv = 512 fixed; 1 <= k <= 4096.  q, kv, out
+ * 16-byte aligned.
  */
 int dsa_sparse_mla_prefill(const void *q, const void *kv, int S,
                            const int32_t *idx, int T, int H, int k, float sm_scale,
