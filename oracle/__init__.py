@@ -45,6 +45,9 @@ def _L():
         lib.dsa_oracle_bf16.restype = f64
         lib.dsa_oracle_bf16.argtypes = [ctypes.c_uint16]
         lib.dsa_oracle_num_threads.restype = i32
+        lib.dsa_oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.dsa_oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.dsa_oracle_quantize_fp8.argtypes = [P, i64, i64, i32, P, P]
         lib.dsa_oracle_indexer.argtypes = [P, P, P, P, i32, i32, i32, P, P, i32, P, i64]
         lib.dsa_oracle_indexer_paged.argtypes = [P, P, P, P, i32, i32, i32, P, P, i32, i32, P, i32, P, i64]
         lib.dsa_oracle_topk.argtypes = [P, i64, i32, P, i32, P]
@@ -72,6 +75,28 @@ def e4m3(code: int) -> float:
 
 def bf16(bits: int) -> float:
     return float(_L().dsa_oracle_bf16(int(bits) & 0xFFFF))
+
+
+def e4m3_encode(v: float) -> int:
+    """E4M3 code of one fp32 value (nearest, ties to even, saturating at +-448)."""
+    return int(_L().dsa_oracle_e4m3_encode(float(v)))
+
+
+def quantize_fp8(x, mode: int = 0):
+    """Per-row FP8 quantisation of fp32 ``x`` [rows, cols] (leading dims flattened into rows).
+
+    mode 0: scale = fp32(amax / 448); mode 1: the smallest power of two not below it
+    (1 for an all-zero row).  Returns (codes uint8 shaped like x, scale float32 [rows]).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    shape = x.shape
+    rows = shape[0]
+    cols = int(np.prod(shape[1:])) if x.ndim > 1 else 1
+    xf = _c(x.reshape(rows, cols), np.float32)
+    codes = np.empty((rows, cols), dtype=np.uint8)
+    scale = np.empty(rows, dtype=np.float32)
+    _L().dsa_oracle_quantize_fp8(_p(xf), rows, cols, int(mode), _p(codes), _p(scale))
+    return codes.reshape(shape), scale
 
 
 def indexer(q8, q_scale, w, q_pos, k8, k_scale, ld: int | None = None, fill=np.nan) -> np.ndarray:

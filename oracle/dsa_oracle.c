@@ -93,6 +93,83 @@ int dsa_oracle_num_threads(void)
 #endif
 }
 
+/* ------------------------------------------------- per-token FP8 quantiser
+ * The indexer runs in FP8 ("AMD Instinct MI355X GPUs Power DeepSeek-V3.2-Exp",
+ * "DeepSeek Sparse Attention (DSA)", item 1; release summary, "Method"), with
+ * one scale per token; the gist page's indexer test script casts along chosen
+ * dimensions to E4M3 with an option for power-of-two ("UE8M0") scales.  The
+ * formulas are not printed; the readings taken here:
+ *   mode 0   scale = fp32(amax / 448), or 1 when the row is all zero;
+ *   mode 1   scale = the smallest power of two not below fp32(amax / 448),
+ *            or 1 when the row is all zero;
+ *   code     E4M3 nearest to fp32(x / scale), ties to the even code,
+ *            magnitudes above 448 saturate to 448.
+ * The divisions are single-precision on purpose: the code is an integer that a
+ * rounding decides, so both sides take that decision in the kernel's precision.
+ */
+
+/* E4M3 code of a finite value: binary search of |v| among the 127 ordered
+ * non-negative finite codes (the decoder above gives their values), nearest
+ * wins, a tie goes to the code with an even mantissa (even code). */
+uint8_t dsa_oracle_e4m3_encode(float v)
+{
+    if (isnan(v))
+        return 0x7F;
+    const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    const double a = fabs((double)v);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7E);
+    int lo = 0, hi = 126; /* dsa_oracle_e4m3(lo) <= a < dsa_oracle_e4m3(hi) */
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) / 2;
+        if (dsa_oracle_e4m3((uint8_t)mid) <= a)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    const double dlo = a - dsa_oracle_e4m3((uint8_t)lo);
+    const double dhi = dsa_oracle_e4m3((uint8_t)hi) - a;
+    int code;
+    if (dlo < dhi)
+        code = lo;
+    else if (dhi < dlo)
+        code = hi;
+    else
+        code = (lo % 2 == 0) ? lo : hi;
+    return (uint8_t)(sign | code);
+}
+
+/* Rows of cols fp32 values -> E4M3 codes [rows, cols] and one fp32 scale per row. */
+void dsa_oracle_quantize_fp8(const float *x, int64_t rows, int64_t cols, int mode, uint8_t *codes, float *scale)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *xr = x + r * cols;
+        float amax = 0.f;
+        for (int64_t c = 0; c < cols; ++c) {
+            const float m = fabsf(xr[c]);
+            if (m > amax)
+                amax = m;
+        }
+        float s = 1.f;
+        if (amax > 0.f) {
+            const float ratio = amax / 448.f;
+            if (mode == 0) {
+                s = ratio;
+            } else {
+                int e;
+                const double f = frexp((double)ratio, &e); /* ratio = f * 2^e, f in [0.5, 1) */
+                s = (float)(f == 0.5 ? (double)ratio : ldexp(1.0, e));
+            }
+        }
+        scale[r] = s;
+        for (int64_t c = 0; c < cols; ++c) {
+            const float q = xr[c] / s;
+            codes[r * cols + c] = dsa_oracle_e4m3_encode(q);
+        }
+    }
+}
+
 /* ----------------------------------------------------------- lightning index
  * I[t,s] = sum_j w[t,j] * ReLU( sum_d qdeq[t,j,d] * kdeq[s,d] )
  * with qdeq = e4m3(q8) * q_scale[t] and kdeq = e4m3(k8) * k_scale[s].

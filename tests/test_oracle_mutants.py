@@ -38,6 +38,12 @@ MUTANTS = {
     "paged_index_slot": ("int64_t slot = (int64_t)page * page_size + s % page_size;",
                          "int64_t slot = (int64_t)page * page_size;"),
     "prefill_bound": ("rows_sel[i] = (s >= 0 && s < S) ? (int64_t)s : -1;", "rows_sel[i] = (int64_t)s;"),
+    "e4m3_ties_up": ("code = (lo % 2 == 0) ? lo : hi;", "code = hi;"),
+    "e4m3_saturates_to_nan": ("return (uint8_t)(sign | 0x7E);", "return (uint8_t)(sign | 0x7F);"),
+    "quant_scale_constant": ("const float ratio = amax / 448.f;", "const float ratio = amax / 447.f;"),
+    "quant_amax_signed": ("const float m = fabsf(xr[c]);", "const float m = xr[c];"),
+    "quant_zero_row_scale": ("        float s = 1.f;\n", "        float s = 0.5f;\n"),
+    "ue8m0_rounds_down": ("ldexp(1.0, e)", "ldexp(1.0, e - 1)"),
 }
 
 PINS = [
@@ -57,6 +63,11 @@ PINS = [
     lambda: pins.test_mla_closed_forms(),
     lambda: pins.test_mla_split_and_combine(),
     lambda: pins.test_mla_paged_equals_contiguous(),
+    lambda: pins.test_quantize_hand_example(),
+    lambda: pins.test_e4m3_encoder_inverts_the_decoder(),
+    lambda: pins.test_e4m3_encoder_ties_to_even_and_saturates(),
+    lambda: pins.test_e4m3_encoder_matches_torch_cast(),
+    lambda: pins.test_quantize_matches_torch_per_row_and_scale_modes(),
 ]
 
 

@@ -354,3 +354,72 @@ def test_mla_paged_equals_contiguous():
         oc, lc = oracle.sparse_mla(q[b:b + 1], kvf, rows[None], 0.05)
         np.testing.assert_array_equal(out[b], oc[0])
         np.testing.assert_array_equal(lse[b], lc[0])
+
+
+# ------------------------------------------------------ FP8 quantiser (a0)
+
+def test_quantize_hand_example():
+    g = _load("quantize_fp8_hand_example.json")
+    for r in g["rows"]:
+        codes, scale = oracle.quantize_fp8(np.array([r["x"]], np.float32), r["mode"])
+        assert float(scale[0]) == r["scale"], r["why"]
+        assert codes[0].tolist() == r["codes"], r["why"]
+
+
+def test_e4m3_encoder_inverts_the_decoder():
+    for c in list(range(0, 127)) + list(range(128, 255)):
+        assert oracle.e4m3_encode(oracle.e4m3(c)) == c
+
+
+def test_e4m3_encoder_ties_to_even_and_saturates():
+    for c in range(0, 126):
+        lo, hi = oracle.e4m3(c), oracle.e4m3(c + 1)
+        mid = (lo + hi) / 2  # at most 5 significant bits: exact in fp32
+        even = c if c % 2 == 0 else c + 1
+        assert oracle.e4m3_encode(mid) == even
+        assert oracle.e4m3_encode(-mid) == 0x80 | even
+        assert oracle.e4m3_encode(np.nextafter(np.float32(mid), np.float32(np.inf))) == c + 1
+        assert oracle.e4m3_encode(np.nextafter(np.float32(mid), np.float32(0))) == c
+    for v in (448.0, 464.0, 1e6, 3.4e38):
+        assert oracle.e4m3_encode(v) == 0x7E and oracle.e4m3_encode(-v) == 0xFE
+
+
+def test_e4m3_encoder_matches_torch_cast():
+    g = np.random.default_rng(11)
+    v = (g.standard_normal(30000) * 10 ** g.uniform(-4.5, 2.7, 30000)).astype(np.float32)
+    v = np.clip(v, -448, 448)
+    mine = np.array([oracle.e4m3_encode(x) for x in v], np.uint8)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(mine, ref)
+
+
+def test_quantize_matches_torch_per_row_and_scale_modes():
+    g = np.random.default_rng(12)
+    x = (g.standard_normal((37, 96)) * 10 ** g.uniform(-3, 3, (37, 1))).astype(np.float32)
+    x[5] = 0.0
+    # mode 0: one fp32 division for the scale, one per element, torch's own E4M3 cast
+    codes, scale = oracle.quantize_fp8(x, 0)
+    xt = torch.from_numpy(x)
+    amax = xt.abs().amax(dim=1)
+    s_ref = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    assert np.array_equal(scale, s_ref.numpy())
+    c_ref = (xt / s_ref[:, None]).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes, c_ref)
+    # mode 1: a power of two, not below amax/448 and less than twice it; no code saturates
+    codes1, scale1 = oracle.quantize_fp8(x, 1)
+    for r in range(x.shape[0]):
+        s = float(scale1[r])
+        if float(amax[r]) == 0.0:
+            assert s == 1.0 and not codes1[r].any()
+            continue
+        m, e = math.frexp(s)
+        assert m == 0.5
+        ratio = float(np.float32(amax[r]) / np.float32(448.0))
+        assert ratio <= s < 2 * ratio
+        assert np.all(np.abs(np.array([oracle.e4m3(c) for c in codes1[r]])) <= 448.0)
+    c1_ref = (xt / torch.from_numpy(scale1)[:, None]).clamp(-448, 448).to(torch.float8_e4m3fn)
+    assert np.array_equal(codes1, c1_ref.view(torch.uint8).numpy())
+    # dequantised values stay within half an E4M3 step of x (relative 2^-4), away from subnormals
+    deq = np.array([[oracle.e4m3(c) for c in row] for row in codes]) * scale[:, None].astype(np.float64)
+    big = np.abs(x) > scale[:, None] * 2.0 ** -6
+    assert np.all(np.abs(deq - x)[big] <= np.abs(x)[big] * 2.0 ** -4 + 1e-30)
