@@ -268,6 +268,36 @@ def time_prefill(dsa, x, b, cfg, steps, warmup, flush):
     return st
 
 
+def quantize_bench(dsa, cfg, steps, warmup, flush, hbm, dev):
+    """Per-token FP8 quantisation of the indexer inputs (q^I [L, H_I, d_I], k^I [L, d_I] fp32), timed on
+    its own: the headline step starts from FP8 codes, as the workload defines it."""
+    L = cfg.L
+    xq = W.randn((L, cfg.HI, cfg.dI), dev, cfg.seed, 10)
+    xk = W.randn((L, cfg.dI), dev, cfg.seed, 12)
+    cq = torch.empty(xq.shape, dtype=torch.uint8, device=dev)
+    ck = torch.empty(xk.shape, dtype=torch.uint8, device=dev)
+    sq = torch.empty((L,), dtype=torch.float32, device=dev)
+    sk = torch.empty((L,), dtype=torch.float32, device=dev)
+    for _ in range(warmup):
+        dsa.dsa_quantize_fp8(xq, cq, sq)
+        dsa.dsa_quantize_fp8(xk, ck, sk)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for e in ev:
+        flush.zero_()
+        e[0].record()
+        dsa.dsa_quantize_fp8(xq, cq, sq)
+        dsa.dsa_quantize_fp8(xk, ck, sk)
+        e[1].record()
+    torch.cuda.synchronize()
+    ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    nbytes = 5.0 * (xq.numel() + xk.numel()) + 8.0 * L
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"ms": ms, "gbs": gbs, "bound": "hbm", "peak": hbm, "frac": gbs / hbm, "bytes": nbytes,
+            "in_step": False, "mode": "amax/448",
+            "what": f"q^I [{L},{cfg.HI},{cfg.dI}] and k^I [{L},{cfg.dI}] fp32 -> E4M3 codes + per-token scales"}
+
+
 def decode_bench(dsa, steps, warmup, flush, peaks, dev):
     cfg = W.CONFIGS["decode_paged"]
     d = W.decode_inputs(cfg, dev)
@@ -481,6 +511,8 @@ def main():
         line["cpu_baseline"] = cpu_baseline(cfg, x)
     if not args.no_decode:
         del b, x
+        torch.cuda.empty_cache()
+        line["stages"]["quantize"] = quantize_bench(dsa, cfg, args.steps, args.warmup, flush, hbm, dev)
         torch.cuda.empty_cache()
         line["decode"] = decode_bench(dsa, args.steps, args.warmup, flush, peaks, dev)
     if dist:

@@ -97,7 +97,9 @@ def quantize_fp8_per_token(x: torch.Tensor):
     n = x.shape[0]
     flat = x.reshape(n, -1).float()
     amax = flat.abs().amax(dim=1)
-    scale = torch.where(amax > 0, amax / FP8_MAX, torch.ones_like(amax))
+    # a tensor divisor: division by a Python scalar may run as a multiply by its
+    # rounded reciprocal on CUDA, which is not the fp32 quotient
+    scale = torch.where(amax > 0, amax / torch.full_like(amax, FP8_MAX), torch.ones_like(amax))
     codes = torch.empty(flat.shape, dtype=torch.uint8, device=x.device)
     step = max(1, _CHUNK_ELEMS // max(flat.shape[1], 1))
     for r0 in range(0, n, step):

@@ -115,6 +115,33 @@ int dsa_indexer_logits(const void *q8, const float *q_scale, const float *w,
                        float *logits, int64_t ld_logits, dsa_stream_t stream);
 
 /*
+ * dsa_quantize_fp8: per-token FP8 (E4M3) quantisation of the indexer inputs.
+ *
+ * The indexer runs in FP8 with one positive scale per token ("AMD Instinct
+ * MI355X GPUs Power DeepSeek-V3.2-Exp", section "DeepSeek Sparse Attention
+ * (DSA)", item 1; release summary "DeepSeek-V3.2-Exp: Boosting Long-Context
+ * Efficiency with DeepSeek Sparse Attention", section "Method"); the gist
+ * page's indexer test script casts to E4M3 with an option for power-of-two
+ * (UE8M0) scales.  For each row r of cols values x[r*cols + c]:
+ *   DSA_SCALE_AMAX  scale[r] = amax / 448 in fp32 (1 for an all-zero row)
+ *   DSA_SCALE_POW2  scale[r] = the smallest power of two >= that ratio
+ *                   (1 for an all-zero row)
+ *   codes[r*cols + c] = E4M3 nearest to x / scale[r] (fp32 division), ties to
+ *                   the even code, magnitudes above 448 saturated to 448.
+ * The indexer's q rows are tokens over all H_I * d_I entries, its k rows
+ * tokens over d_I; dequantised value = code * scale.
+ *
+ *   x      [rows, cols] fp32, contiguous;  codes [rows, cols] uint8 (E4M3);
+ *   scale  [rows] fp32.  rows = 0 is a no-op.  Inputs must be finite.
+ * Any alignment works; 16-byte aligned rows of x (and 4-byte aligned rows of
+ * codes) take the vector path.
+ */
+#define DSA_SCALE_AMAX 0
+#define DSA_SCALE_POW2 1
+int dsa_quantize_fp8(const float *x, int64_t rows, int64_t cols, int scale_mode,
+                     void *codes, float *scale, dsa_stream_t stream);
+
+/*
  * dsa_topk: fine-grained token selection (stage 2).
  *
  * For each row t with n = valid_len[t] candidates logits[t*ld + s], s in [0, n):

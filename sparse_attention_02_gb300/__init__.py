@@ -47,13 +47,14 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.dsa_last_error.restype = ctypes.c_char_p
     lib.dsa_version.restype = i32
     lib.dsa_get_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+    lib.dsa_quantize_fp8.argtypes = [P, i64, i64, i32, P, P, P]
     lib.dsa_indexer_logits.argtypes = [P, P, P, i32, i32, i32, P, P, i32, P, i32, i32, i32, P, P, i64, P]
     lib.dsa_topk.argtypes = [P, i64, i32, P, i32, P, P]
     lib.dsa_sparse_mla_prefill.argtypes = [P, P, i32, P, i32, i32, i32, f32, P, P, P]
     lib.dsa_sparse_mla_decode_paged.argtypes = [P, P, i32, i32, P, i32, P, P, i32, i32, i32, f32, P, P, P, sz, P]
     lib.dsa_sparse_mla_decode_workspace_size.restype = sz
     lib.dsa_sparse_mla_decode_workspace_size.argtypes = [i32, i32, i32]
-    for name in ("dsa_indexer_logits", "dsa_topk", "dsa_sparse_mla_prefill", "dsa_sparse_mla_decode_paged",
+    for name in ("dsa_quantize_fp8", "dsa_indexer_logits", "dsa_topk", "dsa_sparse_mla_prefill", "dsa_sparse_mla_decode_paged",
                  "dsa_get_device_status"):
         getattr(lib, name).restype = i32
     if path is None:
@@ -94,6 +95,27 @@ def _need_rows(t: torch.Tensor, dtype, name: str):
         raise TypeError(f"{name}: expected a 2-D CUDA {dtype} tensor")
     if t.stride(1) != 1 or t.stride(0) < t.shape[1]:
         raise ValueError(f"{name}: rows must be contiguous with a leading dimension >= width")
+
+
+DSA_SCALE_AMAX = 0
+DSA_SCALE_POW2 = 1
+
+
+def dsa_quantize_fp8(x, codes, scale, mode: int = DSA_SCALE_AMAX, stream=None):
+    """Per-row FP8 quantisation: x fp32 [rows, ...] -> codes uint8 (E4M3, same shape), scale fp32 [rows].
+
+    mode DSA_SCALE_AMAX: scale = amax / 448; DSA_SCALE_POW2: the smallest power of two >= that.
+    """
+    _need(x, torch.float32, "x")
+    _need(codes, torch.uint8, "codes")
+    _need(scale, torch.float32, "scale", 1)
+    if x.dim() < 1 or tuple(codes.shape) != tuple(x.shape) or scale.shape[0] != x.shape[0]:
+        raise ValueError("codes must match x's shape and scale must have one entry per row")
+    rows = x.shape[0]
+    cols = x.numel() // rows if rows > 0 else 1
+    _check(load_library().dsa_quantize_fp8(_ptr(x), rows, cols, int(mode), _ptr(codes), _ptr(scale),
+                                           _stream(stream)))
+    return codes, scale
 
 
 def dsa_indexer_logits(q8, q_scale, w, k8, k_scale, q_pos, logits, block_table=None, stream=None):

@@ -177,6 +177,24 @@ int dsa_indexer_logits(const void *q8, const float *q_scale, const float *w, int
     return rc == DSA_OK ? ok() : rc;
 }
 
+int dsa_quantize_fp8(const float *x, int64_t rows, int64_t cols, int scale_mode, void *codes, float *scale,
+                     dsa_stream_t stream)
+{
+    if (rows < 0 || cols < 1)
+        return fail(DSA_ERR_INVALID_ARG, "rows must be >= 0 and cols >= 1");
+    if (scale_mode != DSA_SCALE_AMAX && scale_mode != DSA_SCALE_POW2)
+        return fail(DSA_ERR_INVALID_ARG, "scale_mode must be DSA_SCALE_AMAX or DSA_SCALE_POW2");
+    if (rows == 0)
+        return ok();
+    if (!x || !codes || !scale)
+        return fail(DSA_ERR_INVALID_ARG, "null pointer argument");
+    if (rows > (int64_t(1) << 40) / cols)
+        return fail(DSA_ERR_UNSUPPORTED, "rows * cols too large");
+    QuantizeArgs a{x, rows, cols, scale_mode, static_cast<uint8_t *>(codes), scale};
+    int rc = launch_quantize(a, reinterpret_cast<cudaStream_t>(stream), t_err, sizeof t_err);
+    return rc == DSA_OK ? ok() : rc;
+}
+
 int dsa_topk(const float *logits, int64_t ld, int T, const int32_t *valid_len, int k, int32_t *idx,
              dsa_stream_t stream)
 {

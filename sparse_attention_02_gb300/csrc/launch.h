@@ -16,6 +16,15 @@ bool encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *bas
 int num_sms();
 unsigned *device_status_ptr(); // address of this device's status word, or null
 
+struct QuantizeArgs {
+    const float *x;  // [rows, cols] fp32
+    int64_t rows, cols;
+    int mode;        // 0: amax / 448, 1: power-of-two scale
+    uint8_t *codes;  // [rows, cols] E4M3
+    float *scale;    // [rows]
+};
+int launch_quantize(const QuantizeArgs &a, cudaStream_t stream, char *err, size_t errlen);
+
 struct IndexerArgs {
     const void *q8;
     const float *q_scale;

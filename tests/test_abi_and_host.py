@@ -53,6 +53,15 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.dsa_topk(fake, 16, -1, fake, 8, fake, None) == 1
     assert lib.dsa_topk(fake, 16, 0, fake, 8, fake, None) == 0
     assert lib.dsa_topk(fake, 1 << 29, 4, fake, 8, fake, None) == 2
+    # quantiser: bad mode, bad sizes, null pointers; rows == 0 is a no-op
+    i64 = ctypes.c_int64
+    assert lib.dsa_quantize_fp8(fake, i64(4), i64(128), 2, fake, fake, None) == 1
+    assert "scale_mode" in _err(lib)
+    assert lib.dsa_quantize_fp8(fake, i64(-1), i64(128), 0, fake, fake, None) == 1
+    assert lib.dsa_quantize_fp8(fake, i64(4), i64(0), 0, fake, fake, None) == 1
+    assert lib.dsa_quantize_fp8(None, i64(4), i64(128), 1, fake, fake, None) == 1
+    assert lib.dsa_quantize_fp8(fake, i64(0), i64(128), 0, None, None, None) == 0
+    assert lib.dsa_quantize_fp8(fake, i64(1 << 40), i64(1 << 20), 0, fake, fake, None) == 2
     # indexer: misaligned q8, bad page size, missing S
     assert lib.dsa_indexer_logits(P(4097), fake, fake, 4, 64, 128, fake, fake, 16, None, 0, 0, 0, fake, fake, 16,
                                   None) == 3
