@@ -201,3 +201,41 @@ def decode_inputs(cfg: Config, device, seed: int | None = None, B: int | None = 
     return dict(q8=q8, qs=qs, w=w, k8_pool=k8, ks_pool=ks, kv_pool=kv, q=q,
                 ctx=ctx.to(device), q_pos=(ctx - 1).to(device), block_table=bt.to(device),
                 num_pages=P)
+
+
+def varlen_inputs(cfg: Config, device, seq_lens, queries_per_seq=None, seed: int | None = None):
+    """Several sequences of different lengths over one shared, permuted page pool.
+
+    Sequence b holds ``seq_lens[b]`` tokens; its query rows are the last
+    ``queries_per_seq[b]`` positions (all of them when None: a ragged batched
+    prefill; a few: a multi-token decode).  Every query row carries its own
+    position, context length (position + 1) and copy of its sequence's block
+    table, which is how the paged entry points see a row.  Also returns the
+    same latent rows concatenated per sequence (``kv_concat`` with per-sequence
+    start offsets) for the contiguous entry point.
+    """
+    seed = cfg.seed if seed is None else seed
+    lens = torch.as_tensor(seq_lens, dtype=torch.int32)
+    d = decode_inputs(cfg, device, seed=seed, ctx=lens)
+    ps = cfg.page_size
+    bt = d["block_table"].cpu()
+    seq, pos = [], []
+    for b, n in enumerate(lens.tolist()):
+        m = n if queries_per_seq is None else int(queries_per_seq[b])
+        for p in range(n - m, n):
+            seq.append(b)
+            pos.append(p)
+    seq = torch.tensor(seq, dtype=torch.int64)
+    pos = torch.tensor(pos, dtype=torch.int32)
+    T = int(seq.numel())
+    q8, qs, w = indexer_queries(cfg, T, device, seed, tid0=40)
+    q = randn((T, cfg.H, cfg.D), device, seed, 42, dtype=torch.bfloat16)
+    starts = torch.zeros(len(lens), dtype=torch.int64)
+    starts[1:] = torch.cumsum(lens.to(torch.int64), 0)[:-1]
+    rows = torch.cat([(bt[b, torch.arange(n) // ps].to(torch.int64) * ps + torch.arange(n) % ps)
+                      for b, n in enumerate(lens.tolist())])
+    kv_concat = d["kv_pool"].view(-1, cfg.D)[rows.to(device)].contiguous()
+    return dict(q8=q8, qs=qs, w=w, q=q, k8_pool=d["k8_pool"], ks_pool=d["ks_pool"], kv_pool=d["kv_pool"],
+                num_pages=d["num_pages"], seq=seq, q_pos=pos.to(device), ctx=(pos + 1).to(device),
+                block_table=bt[seq].contiguous().to(device), seq_block_table=bt, seq_lens=lens,
+                seq_starts=starts, kv_concat=kv_concat)

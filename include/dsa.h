@@ -185,23 +185,25 @@ int dsa_sparse_mla_prefill(const void *q, const void *kv, int S,
                            void *out, float *lse, dsa_stream_t stream);
 
 /*
- * dsa_sparse_mla_decode_paged: the same attention for one new token per
- * sequence over a paged latent cache (decode form of stage 3).
+ * dsa_sparse_mla_decode_paged: the same attention over a paged latent cache
+ * (decode form of stage 3).
  *
- * Row b's query sits at position ctx_len[b]-1; idx[b*k + i] holds LOGICAL
- * positions, read from slot s % page_size of pool page
+ * Row b is one query: its token sits at position ctx_len[b]-1 of the sequence
+ * whose pages block_table row b lists.  Rows are independent, so a batch may
+ * hold one new token per sequence (decode), several positions of the same
+ * sequence (multi-token decode), or every token of sequences of different
+ * lengths (ragged batched prefill), all in one pool.  idx[b*k + i] holds
+ * LOGICAL positions, read from slot s % page_size of pool page
  * block_table[b*max_pages + s/page_size].  Entries outside [0, ctx_len[b]) are
  * skipped; a page id outside [0, num_pages) is skipped and flagged
- * DSA_DEV_BAD_PAGE.  The k selected rows are split across CTAs; partial
- * results go to `workspace` and are merged by their LSE in a second kernel.
+ * DSA_DEV_BAD_PAGE.  Each row runs on one two-CTA cluster, as in prefill.
  *
  *   q       [B, H, 576] bf16;  kv_pool [num_pages, page_size, 576] bf16
  *   block_table [B, max_pages] int32;  ctx_len [B] int32;  idx [B, k] int32
  *   out     [B, H, 512] bf16;  lse [B, H] fp32
- *   workspace: device buffer of at least
- *           dsa_sparse_mla_decode_workspace_size(B, H, k) bytes, 256-byte
- *           aligned, owned by the caller, contents need not be initialised;
- *           two calls in flight at once need two workspaces.
+ *   workspace: a device buffer of at least
+ *           dsa_sparse_mla_decode_workspace_size(B, H, k) bytes (0 in this
+ *           version: NULL is accepted), owned by the caller.
  */
 int dsa_sparse_mla_decode_paged(const void *q, const void *kv_pool, int num_pages, int page_size,
                                 const int32_t *block_table, int max_pages, const int32_t *ctx_len,
