@@ -11,29 +11,34 @@
 //
 // On-chip budget.  O for 128 heads x 512 columns in fp32 is 256 KB: all of one
 // SM's TMEM.  Each token therefore runs on a cluster of two CTAs (two SMs):
-//   CTA r keeps O[:, 256r : 256r+256) in TMEM and gathers latent columns
-//   [256r, 256r+320) of every selected row (five 64-column swizzle atoms);
-//   it computes the PARTIAL scores over latent columns [288r, 288r+288) (a
-//   K-split of QK^T, no duplicated MMA work), and the two CTAs swap their
+//   CTA r keeps O[:, 256r : 256r+256) in TMEM, gathers its V quarter (latent
+//   columns [256r, 256r+256), four 64-column swizzle atoms) and its half of the
+//   RoPE columns ([512+32r, 512+32r+32), one 32-column atom) of every selected
+//   row, and computes the PARTIAL scores over exactly those 288 columns (a
+//   K-split of QK^T, no duplicated MMA work); the two CTAs swap their
 //   partial-score tiles through distributed shared memory.  Both CTAs then
 //   add the same two halves in the same way, so they hold bit-identical
 //   scores, run the same softmax (identical P, m and l) and each applies P to
-//   its own V half.
-//
+//   its own V quarter.  Stages of 36 KB leave room for four in flight; the last
+//   96 of this CTA's Q columns live in TMEM (the score MMA reads them as a TMEM
+//   A operand), the first 192 in shared memory.
+
 // The swap carries the log2-scaled partial scores rounded to fp16 (saturating,
 // 16 KB per 64-key block instead of 32 KB in fp32); each CTA rounds its own
 // half the same way before adding.  At the scores' scale (|s| of a few units
 // in log2 terms) this perturbs each softmax weight by ~2^-11 relative, below
 // the bf16 rounding of P that the PV product applies anyway.
 //
-// Per 64-key block j (double-buffered S and swap buffers, three P buffers,
-// three KV stages):
-//   producer warps  four warps cp.async the 64 selected rows x 640 B into the
-//                   SW128 K-major layout (one 128-byte line per 8 lanes), zero-
-//                   fill invalid entries, and arrive on the stage's mbarrier as
-//                   their copies land (cp.async.mbarrier.arrive.noinc);
-//   MMA warps       S_j = Q_half . KV_j^T   (M=128 heads, N=64, K=288; A, B
-//                   K-major in smem), even and odd blocks from two warps, and
+// Per 64-key block j (double-buffered S, swap and P buffers, four KV stages):
+//   producer warps  four warps cp.async the 64 selected rows x 576 B into the
+//                   SW128 / SW64 K-major layouts (one 128-byte line per 8
+//                   lanes), zero-fill invalid entries, and arrive on the
+//                   stage's mbarrier as their copies land
+//                   (cp.async.mbarrier.arrive.noinc); at each token they also
+//                   write the TMEM part of Q (lane = head);
+//   MMA warps       S_j = Q_half . KV_j^T   (M=128 heads, N=64, K=288; A from
+//                   smem or TMEM, B K-major in smem), even and odd blocks from
+//                   two warps, and
 //                   O += P_j . V_j          (M=128, N=256, K=64; A = P from
 //                   TMEM, B = the same KV stage read MN-major) from a third.
 //                   One thread serialises its tcgen05.mma issue at ~100 cycles
@@ -69,12 +74,13 @@ namespace {
 constexpr int kD = 576;
 constexpr int kDv = 512;
 constexpr int kBN = 64;                  // keys per block
-constexpr int kAtoms = 5;                // 64-column atoms gathered per CTA
+constexpr int kVAtoms = 4;               // 64-column atoms of this CTA's V quarter per stage
 constexpr int kQAtom = 128 * 128;        // bytes of one full Q atom (128 rows x 128 B, SW128)
-constexpr int kQHalf = 128 * 64;         // bytes of the half atom (128 rows x 64 B, SW64)
-constexpr int kKVAtom = kBN * 128;       // bytes of one KV atom (64 rows)
-constexpr int kStage = kAtoms * kKVAtom; // 40 KB
-constexpr int kNStage = 3;
+constexpr int kQSmemAtoms = 3;           // Q atoms in shared memory; the 4th and the RoPE half sit in TMEM
+constexpr int kKVAtom = kBN * 128;       // bytes of one KV atom (64 rows x 128 B, SW128)
+constexpr int kKVHalf = kBN * 64;        // bytes of the RoPE half atom (64 rows x 64 B, SW64)
+constexpr int kStage = kVAtoms * kKVAtom + kKVHalf; // 36 KB
+constexpr int kNStage = 4;
 constexpr int kXBuf = 128 * kBN * 2;     // one swap buffer: 128 heads x 64 fp16
 constexpr int kProdWarps = 4;
 constexpr int kPvWarp = kProdWarps;      // all PV MMAs (fixed accumulation order) + TMEM owner
@@ -87,32 +93,33 @@ constexpr int kThreads = 32 * (kSoftWarp0 + kSoftWarps);
 constexpr int kSoftThread0 = 32 * kSoftWarp0;
 constexpr float kRescaleLog2 = 8.f;      // move the running max only when exceeded by this
 
-constexpr int OFF_Q = 0;                                  // 4 full atoms
-constexpr int OFF_QH = OFF_Q + 4 * kQAtom;               // half atom
-constexpr int OFF_KV = OFF_QH + kQHalf;                  // 72 KB
+constexpr int OFF_Q = 0;                                  // 3 full atoms
+constexpr int OFF_KV = OFF_Q + kQSmemAtoms * kQAtom;     // 48 KB
 constexpr int OFF_X = OFF_KV + kNStage * kStage;         // 192 KB
 constexpr int OFF_BAR = OFF_X + 2 * kXBuf;               // 224 KB
-constexpr int NBAR = 41;
+constexpr int NBAR = 40;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int kSmem = OFF_MISC + 64 + 1024;
 
 // barrier slots
 // [parity] for S and swap buffers, [J % kNP] for P buffers
-constexpr int kNP = 3; // P buffers in TMEM
-constexpr int B_KVF = 0, B_KVE = 3, B_SF = 6, B_SE = 8, B_XF = 10, B_XE = 12, B_PF = 14, B_PE = 17,
+constexpr int kNP = 2; // P buffers in TMEM
+constexpr int B_KVF = 0, B_KVE = 4, B_SF = 8, B_SE = 10, B_XF = 12, B_XE = 14, B_PF = 16, B_PE = 18,
               B_PK = 20,  // senders parked the block's own fp16 partial scores in its P buffer
-              B_QF = 23, B_QE = 24, B_QA = 25, B_OF = 26, B_OE = 27, B_DONE = 28,
-              B_RB = 29,  // [quad][parity]: sibling softmax warps swapped their block max
-              B_RL = 37;  // [quad]: sibling softmax warps swapped their row sums
+              B_QF = 22, B_QE = 23, B_QA = 24, B_OF = 25, B_OE = 26, B_DONE = 27,
+              B_RB = 28,  // [quad][parity]: sibling softmax warps swapped their block max
+              B_RL = 36;  // [quad]: sibling softmax warps swapped their row sums
 
 // TMEM columns
 constexpr uint32_t TM_O = 0;
 constexpr uint32_t TM_S = 256;  // two buffers of 64
 constexpr uint32_t TM_P = 384;  // kNP buffers of 32 (bf16 pairs)
-constexpr uint32_t TM_RED = 480; // per-head values swapped between the two softmax warps of a quadrant
+constexpr uint32_t TM_QT = 448; // Q: the 4th atom (32 columns of bf16 pairs) and the RoPE half (16)
+constexpr uint32_t TM_RED = 496; // per-head values swapped between the two softmax warps of a quadrant
 constexpr uint32_t kTmemCols = 512;
 
 struct Params {
+    const __nv_bfloat16 *q;    // [T, H, 576]
     const __nv_bfloat16 *kv;   // [S, 576] or pool [num_pages * page_size, 576]
     const int32_t *idx;        // [T, k]
     int S, T, H, k;
@@ -178,7 +185,7 @@ __device__ __forceinline__ float2 unpack_f16x2(uint32_t w)
 
 template <bool PAGED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qh, Params p)
+    sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_q, Params p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -213,7 +220,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(bar(B_PF + i), kSoftWarps);
             mbar_init(bar(B_PE + i), 1);
         }
-        mbar_init(bar(B_QF), 1);
+        mbar_init(bar(B_QF), 1 + kProdWarps); // the Q TMA (expect_tx) + each producer's TMEM part
         mbar_init(bar(B_QE), 2);
         mbar_init(bar(B_QA), kSoftWarps + kSendWarps + 1); // softmax, sender and PV warps read each token's nb slot
         mbar_init(bar(B_OF), 1);
@@ -229,13 +236,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // Q rows >= H stay zero (their scores are computed but never stored).
     if (p.H < 128) {
         const int nz = 128 - p.H;
-        for (int i = threadIdx.x; i < 4 * nz * 8; i += kThreads) {
+        for (int i = threadIdx.x; i < kQSmemAtoms * nz * 8; i += kThreads) {
             const int a = i / (nz * 8), rem = i % (nz * 8);
             *reinterpret_cast<uint4 *>(smem + OFF_Q + a * kQAtom + (p.H + rem / 8) * 128 + (rem % 8) * 16) =
                 make_uint4(0, 0, 0, 0);
         }
-        for (int i = threadIdx.x; i < nz * 4; i += kThreads)
-            *reinterpret_cast<uint4 *>(smem + OFF_QH + (p.H + i / 4) * 64 + (i % 4) * 16) = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
     }
     if (warp == kPvWarp)
@@ -250,10 +255,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------ producers
         // Warp pw fills rows [16 pw, 16 pw + 16) of each stage.  Lanes 0..15
         // hold those rows' latent-row indices; one cp.async instruction moves
-        // four rows x 128 B (lane = 8 x row-in-4 + 16-byte chunk).
+        // four rows x 128 B (lane = 8 x row-in-4 + 16-byte chunk).  At each
+        // token, warp pw also writes TMEM lane quadrant pw's part of Q.
         const int pw = warp;
         const int q_row0 = 16 * pw;
-        const __nv_bfloat16 *kv_cols = p.kv + 256 * rank;
+        const __nv_bfloat16 *kv_cols = p.kv + 256 * rank;          // this CTA's V quarter
+        const __nv_bfloat16 *rope_cols = p.kv + 512 + 32 * rank;   // this CTA's half of the RoPE columns
         uint32_t J = 0;
         int u = 0;
         bool ok = true;
@@ -271,35 +278,78 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 last = y > last ? y : last;
             }
             const int nb = last < 0 ? 0 : last / kBN + 1;
+            // Q (shared memory and TMEM parts) is reused: the score MMAs must be
+            // done reading the previous token's Q; warp 0 also reuses the nb slot,
+            // which the softmax, sender and PV warps must have taken
+            if (u >= 1 && !mbar_wait_warp(bar(B_QE), (u - 1) & 1, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
             if (pw == 0) {
-                // the Q buffer and the nb slot are reused: the MMA warp must be
-                // done reading Q and the softmax warps must have taken the
-                // previous token
-                if (u >= 1 && (!mbar_wait_warp(bar(B_QE), (u - 1) & 1, abort_flag, p.status) ||
-                               !mbar_wait_warp(bar(B_QA), (u - 1) & 1, abort_flag, p.status))) {
+                if (u >= 1 && !mbar_wait_warp(bar(B_QA), (u - 1) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 if (lane == 0) {
                     nb_s[u & 1] = nb;
-                    const int x_half = rank == 0 ? 256 : 288;
-                    const int x_full0 = rank == 0 ? 0 : 320;
+                    const int x0 = 256 * rank; // this CTA's Q columns: its V quarter ...
                     if (nb > 0) {
-                        mbar_arrive_expect_tx(bar(B_QF), 4 * p.H * 128 + p.H * 64);
-                        for (int a = 0; a < 4; ++a)
-                            tma_load_2d(sbase + OFF_Q + a * kQAtom, &tm_q, bar(B_QF), x_full0 + 64 * a, t * p.H);
-                        tma_load_2d(sbase + OFF_QH, &tm_qh, bar(B_QF), x_half, t * p.H);
+                        mbar_arrive_expect_tx(bar(B_QF), kQSmemAtoms * p.H * 128);
+                        for (int a = 0; a < kQSmemAtoms; ++a)
+                            tma_load_2d(sbase + OFF_Q + a * kQAtom, &tm_q, bar(B_QF), x0 + 64 * a, t * p.H);
                     } else {
                         mbar_arrive(bar(B_QF));
                     }
                     if (t + ncl < p.T) {
                         for (int a = 0; a < 4; ++a)
-                            tma_prefetch_l2_2d(&tm_q, x_full0 + 64 * a, (t + ncl) * p.H);
-                        tma_prefetch_l2_2d(&tm_qh, x_half, (t + ncl) * p.H);
+                            tma_prefetch_l2_2d(&tm_q, x0 + 64 * a, (t + ncl) * p.H);
+                        tma_prefetch_l2_2d(&tm_q, 512, (t + ncl) * p.H); // ... and its RoPE half
                     }
                 }
                 __syncwarp();
             }
+            if (nb > 0) {
+                // TMEM part of Q for heads 32 pw .. 32 pw + 31 (lane = head): the 4th
+                // atom of the V quarter (64 columns) and the RoPE half (32 columns),
+                // as bf16 pairs, the A-operand layout of a TMEM-sourced MMA
+                const int h = 32 * pw + lane;
+                uint32_t qa[32], qr[16];
+                if (h < p.H) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(p.q + ((int64_t)t * p.H + h) * kD + 256 * rank + 192);
+                    const uint4 *srr = reinterpret_cast<const uint4 *>(p.q + ((int64_t)t * p.H + h) * kD + 512 + 32 * rank);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 v = __ldg(src + c);
+                        qa[4 * c] = v.x;
+                        qa[4 * c + 1] = v.y;
+                        qa[4 * c + 2] = v.z;
+                        qa[4 * c + 3] = v.w;
+                    }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 v = __ldg(srr + c);
+                        qr[4 * c] = v.x;
+                        qr[4 * c + 1] = v.y;
+                        qr[4 * c + 2] = v.z;
+                        qr[4 * c + 3] = v.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        qa[c] = 0u;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        qr[c] = 0u;
+                }
+                const uint32_t tq = tmem + (static_cast<uint32_t>(32 * pw) << 16) + TM_QT;
+                tmem_st32(tq, qa);
+                tmem_st16(tq + 32, qr);
+                tmem_st_wait();
+                tc_fence_before();
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar(B_QF));
             auto resolve = [&](int j) -> int {
                 const int i = j * kBN + q_row0 + (lane & 15);
                 const int r = i < p.k ? latent_row<PAGED>(p, t, idx_row[i], ctx) : -1;
@@ -325,12 +375,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int il = 4 * m + (lane >> 3);
                     const int row = __shfl_sync(0xffffffffu, cur, il);
                     const int rl = q_row0 + il;
-                    const __nv_bfloat16 *src = kv_cols + (int64_t)(row >= 0 ? row : 0) * kD + cc * 8;
-                    const uint32_t dst = stage + rl * 128 + ((cc ^ (rl & 7)) << 4);
+                    const int64_t roff = (int64_t)(row >= 0 ? row : 0) * kD;
+                    const uint32_t dst = stage + rl * 128 + ((cc ^ (rl & 7)) << 4); // SW128 atoms
                     const uint32_t bytes = row >= 0 ? 16u : 0u;
 #pragma unroll
-                    for (int a = 0; a < kAtoms; ++a)
-                        cp_async_16_zfill(dst + a * kKVAtom, src + a * 64, bytes);
+                    for (int a = 0; a < kVAtoms; ++a)
+                        cp_async_16_zfill(dst + a * kKVAtom, kv_cols + roff + a * 64 + cc * 8, bytes);
+                    if (cc < 4) // RoPE half: 64-byte rows, SW64 (16-byte chunk ^ (row / 2) % 4)
+                        cp_async_16_zfill(stage + kVAtoms * kKVAtom + rl * 64 + ((cc ^ ((rl >> 1) & 3)) << 4),
+                                          rope_cols + roff + cc * 8, bytes);
                 }
                 cp_async_arrive_noinc(bar(B_KVF + st));
             }
@@ -397,26 +450,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t J = 0;
         int u = 0;
         bool ok = true;
-        // Descriptors are precomputed once: the issue loop below is one add and
-        // one tcgen05.mma per k-step (the issuing warp shares its SMSP with busy
-        // softmax and producer warps).  A operand of score k-step s (16 latent
-        // columns): the SW64 half atom holds this CTA's 32 columns that do not
-        // fill a whole 64-column atom.
-        uint64_t qd[18];
-        uint32_t bofs[18]; // B offset of k-step s within a KV stage, 16-byte units
+        // This CTA's 288 score columns: its V quarter [256 r, 256 r + 256) (16
+        // k-steps of 16 columns) and its half of the RoPE columns [512 + 32 r,
+        // +32) (2 k-steps).  A operand: k-steps 0..11 from the three Q atoms in
+        // shared memory, k-steps 12..17 from TMEM (the 4th atom, then the RoPE
+        // half).  B operand: the stage's four SW128 atoms, then its SW64 RoPE
+        // half atom.  Descriptors are precomputed: the issue loop is one add and
+        // one tcgen05.mma per k-step.
+        uint64_t qd[12];
+        uint32_t bofs[16]; // B offset of k-step s < 16 within a KV stage, 16-byte units
 #pragma unroll
-        for (int s = 0; s < 18; ++s) {
-            const int fs = rank == 0 ? s : s - 2; // k-step within the full atoms
-            if (fs < 0 || fs >= 16) {
-                const int hs = rank == 0 ? s - 16 : s;
-                qd[s] = sdesc(sbase + OFF_QH + hs * 32, 16, 512, 4);
-            } else {
-                qd[s] = sdesc(sbase + OFF_Q + (fs >> 2) * kQAtom + (fs & 3) * 32, 16, 1024, 2);
-            }
-            const int ks = s + 2 * (int)rank; // k-step within the gathered columns
-            bofs[s] = static_cast<uint32_t>(((ks >> 2) * kKVAtom + (ks & 3) * 32) >> 4);
+        for (int s = 0; s < 16; ++s) {
+            if (s < 12)
+                qd[s] = sdesc(sbase + OFF_Q + (s >> 2) * kQAtom + (s & 3) * 32, 16, 1024, 2);
+            bofs[s] = static_cast<uint32_t>(((s >> 2) * kKVAtom + (s & 3) * 32) >> 4);
         }
         const uint64_t kv_desc0 = sdesc(sbase + OFF_KV, 16, 1024, 2);
+        const uint64_t kvh_desc0 = sdesc(sbase + OFF_KV + kVAtoms * kKVAtom, 16, 512, 4);
         for (int t = cid; ok && t < p.T; t += ncl, ++u) {
             if (!mbar_wait_warp(bar(B_QF), u & 1, abort_flag, p.status)) {
                 ok = false;
@@ -436,12 +486,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem(); // the stage was written by cp.async (generic proxy)
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint64_t sd = kv_desc0 + static_cast<uint64_t>((st * kStage) >> 4);
+                    const uint64_t soff = static_cast<uint64_t>((st * kStage) >> 4);
+                    const uint64_t sd = kv_desc0 + soff, sdh = kvh_desc0 + soff;
                     const uint32_t d_tmem = tmem + TM_S + 64 * b;
                     umma_f16_ss(d_tmem, qd[0], sd + bofs[0], idesc_qk, 0u);
 #pragma unroll
-                    for (int s = 1; s < 18; ++s)
+                    for (int s = 1; s < 12; ++s)
                         umma_f16_ss(d_tmem, qd[s], sd + bofs[s], idesc_qk, 1u);
+#pragma unroll
+                    for (int s = 12; s < 16; ++s)
+                        umma_f16_ts(d_tmem, tmem + TM_QT + 8 * (s - 12), sd + bofs[s], idesc_qk, 1u);
+#pragma unroll
+                    for (int s = 16; s < 18; ++s)
+                        umma_f16_ts(d_tmem, tmem + TM_QT + 8 * (s - 12), sdh + static_cast<uint64_t>(2 * (s - 16)),
+                                    idesc_qk, 1u);
                     umma_commit(bar(B_SF + b));
                 }
                 __syncwarp();
@@ -757,15 +815,13 @@ int launch(const MlaArgs &a, cudaStream_t stream, char *err, size_t errlen)
         }
         attr_set[dev] = true;
     }
-    // Q as [T*H rows, 576 cols]: 64-column boxes (SW128) and one 32-column box (SW64)
-    CUtensorMap tq, tqh;
+    // Q as [T*H rows, 576 cols]: 64-column boxes (SW128)
+    CUtensorMap tq;
     if (!encode_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, kD, (uint64_t)a.T * a.H, kD * 2, 64, a.H,
                         CU_TENSOR_MAP_SWIZZLE_128B, err, errlen))
         return DSA_ERR_CUDA;
-    if (!encode_tmap_2d(&tqh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, kD, (uint64_t)a.T * a.H, kD * 2, 32, a.H,
-                        CU_TENSOR_MAP_SWIZZLE_64B, err, errlen))
-        return DSA_ERR_CUDA;
     Params p;
+    p.q = static_cast<const __nv_bfloat16 *>(a.q);
     p.kv = static_cast<const __nv_bfloat16 *>(a.kv);
     p.idx = a.idx;
     p.S = a.S;
@@ -791,7 +847,7 @@ int launch(const MlaArgs &a, cudaStream_t stream, char *err, size_t errlen)
         clusters = a.T;
     if (clusters < 1)
         clusters = 1;
-    sparse_mla_kernel<PAGED><<<dim3(2 * clusters), kThreads, kSmem, stream>>>(tq, tqh, p);
+    sparse_mla_kernel<PAGED><<<dim3(2 * clusters), kThreads, kSmem, stream>>>(tq, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(err, errlen, "sparse_mla launch: %s", cudaGetErrorString(e));
