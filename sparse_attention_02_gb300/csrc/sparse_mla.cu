@@ -47,15 +47,16 @@
 //   sender warps    thread = head, one warp per TMEM lane quadrant: the
 //                   block's partial S from TMEM, log2-scaled and rounded to
 //                   fp16 pairs, st.async to the peer (completion counted in
-//                   bytes on the peer's mbarrier) and parked in the block's P
-//                   columns.  They run ahead of the softmax, so the swap of one
+//                   bytes on the peer's mbarrier) and parked in place over the
+//                   block's S buffer.  They run ahead of the softmax, so the swap of one
 //                   block overlaps the softmax of the previous one and the
 //                   softmax warps never stall on the slow DSMEM stores;
 //   softmax warps   thread = head, two warps per TMEM lane quadrant, each with
-//                   32 of the block's keys: own half from the P columns, peer
-//                   half from the swap buffer, mask, max (agreed with the
-//                   sibling warp through a spare TMEM column), exp2, running
-//                   sum; P (bf16) back into TMEM over the parked half.  The
+//                   32 of the block's keys: own half from the S buffer (then
+//                   free for the next score MMAs), peer half from the swap
+//                   buffer, mask, max (agreed with the sibling warp through a
+//                   spare TMEM column), exp2, running sum; P (bf16) into the
+//                   block's P buffer once its previous PV is done.  The
 //                   running max only moves when a block exceeds it by more
 //                   than 2^8 (then O is rescaled in TMEM), so P <= 256.
 // The kernel is persistent: each cluster walks tokens t = c, c + C, ... with
@@ -211,7 +212,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_SF + i), 1);
-            mbar_init(bar(B_SE + i), kSendWarps);
+            mbar_init(bar(B_SE + i), kSoftWarps);
             mbar_init(bar(B_XF + i), 1);
             mbar_init(bar(B_XE + i), kSoftWarps);
         }
@@ -519,8 +520,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // Thread = head (TMEM lane), all 64 keys of each block: this CTA's
         // partial scores, log2-scaled and rounded to fp16 pairs, go to the peer
         // by st.async (completion counted in bytes on the peer's mbarrier) and
-        // into this CTA's P buffer of the block, where the softmax warps read
-        // them back; P buffer J % kNP is free once PV of block J - kNP is done.
+        // back over the first half of the block's S buffer, where the softmax
+        // warps read them.
         const int quad = warp & 3;
         const int h = quad * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
@@ -557,10 +558,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         own[16 * hh + c] = pack_f16x2_sat(__uint_as_float(r[2 * c]) * p.scale_log2,
                                                           __uint_as_float(r[2 * c + 1]) * p.scale_log2);
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(bar(B_SE + b));
                 // the peer's buffer b must be free (its softmax warps read block J-2)
                 if (J >= 2 && !mbar_wait_warp<true>(bar(B_XE + b), ((J >> 1) - 1) & 1, abort_flag, p.status)) {
                     ok = false;
@@ -571,18 +568,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int cc = 0; cc < 8; ++cc)
                     st_async_v4_b32(xr + ((static_cast<uint32_t>(cc) ^ hsw) << 4), own[4 * cc], own[4 * cc + 1],
                                     own[4 * cc + 2], own[4 * cc + 3], xfr);
-                const int pb = J % kNP;
-                if (J >= kNP && !mbar_wait_warp(bar(B_PE + pb), ((J / kNP) - 1) & 1, abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                tmem_st32(tmem + lane_off + TM_P + 32 * pb, own);
+                // park the own half in place, over the first 32 columns of S buffer b
+                // (this warp's lanes were read whole above); the softmax warps read
+                // it back and then free the buffer for the score MMAs of block J + 2
+                tmem_st32(tmem + lane_off + TM_S + 64 * b, own);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(bar(B_PK + pb));
+                    mbar_arrive(bar(B_PK + b));
             }
         }
     } else {
@@ -625,14 +619,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 // 1. this CTA's partial scores (fp16 pairs parked by the senders) and the peer's half
                 const int pb = J % kNP;
-                if (!mbar_wait_warp(bar(B_PK + pb), (J / kNP) & 1, abort_flag, p.status)) {
+                if (!mbar_wait_warp(bar(B_PK + b), (J >> 1) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 uint32_t own[16];
-                tmem_ld16(tmem + lane_off + TM_P + 32 * pb + 16 * hf, own);
+                tmem_ld16(tmem + lane_off + TM_S + 64 * b + 16 * hf, own);
                 tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(bar(B_SE + b)); // S buffer b is free for the score MMAs of block J + 2
                 // arm buffer b for the peer's half of block J (its bytes may already be landing);
                 // this thread has seen the phase of block J-2 complete
                 if (threadIdx.x == kSoftThread0)
@@ -725,7 +723,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     pk[c >> 1] = pack_bf16x2(p0, p1);
                 }
                 l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-                // P over this warp's parked half (the P buffer was freed before the senders parked)
+                // P buffer pb is free once the PV MMAs of block J - kNP are done
+                if (J >= kNP && !mbar_wait_warp(bar(B_PE + pb), ((J / kNP) - 1) & 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
                 tmem_st16(tmem + lane_off + TM_P + 32 * pb + 16 * hf, pk);
                 tmem_st_wait();
                 tc_fence_before();
