@@ -55,10 +55,16 @@ def test_topk_from_gpu_logits_bit_exact():
         assert np.array_equal(idx.cpu().numpy(), ref), f"k={k}"
 
 
+# A grid of at most two rows per SM takes the candidate fast path, a larger one the
+# four-pass kernel; tiling the same rows REPS times sends them through the latter.
+REPS_MANY_ROWS = 20
+
+
+@pytest.mark.parametrize("reps", [1, REPS_MANY_ROWS])
 @pytest.mark.parametrize("ld", [4099, 4096])
-def test_topk_edge_rows_and_ties(ld):
+def test_topk_edge_rows_and_ties(ld, reps):
     """Valid lengths 0, 1, k-1, k, k+1, ld; tie-heavy integer scores with -0/+0;
-    ld both aligned and unaligned (vector and scalar paths)."""
+    ld both aligned and unaligned (vector and scalar paths); few rows and many."""
     dsa = lib()
     g = torch.Generator(device=DEV).manual_seed(3)
     T = 24
@@ -70,30 +76,33 @@ def test_topk_edge_rows_and_ties(ld):
     # poison past the valid length: any read of it would change the result
     for r in range(T):
         vals[r, int(n[r]):] = float("nan")
-    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
-    dsa.dsa_topk(vals, n.to(DEV), k, idx)
+    idx = torch.empty((T * reps, k), dtype=torch.int32, device=DEV)
+    dsa.dsa_topk(vals.repeat(reps, 1), n.repeat(reps).to(DEV), k, idx)
     torch.cuda.synchronize()
     v = vals.cpu().double().numpy()
     ref = oracle.topk(np.nan_to_num(v, nan=-np.inf), n.numpy(), k)
-    assert np.array_equal(idx.cpu().numpy(), ref)
+    assert np.array_equal(idx.cpu().numpy(), np.tile(ref, (reps, 1)))
     assert dsa.dsa_get_device_status() == 0
 
 
-def test_topk_deterministic_large_row():
+@pytest.mark.parametrize("reps", [1, REPS_MANY_ROWS])
+def test_topk_deterministic_large_row(reps):
     dsa = lib()
     T, ld = 8, 131072
     g = torch.Generator(device=DEV).manual_seed(4)
     vals = torch.randn((T, ld), generator=g, device=DEV)
     vals[:, ::7] = 0.25  # a large tie block straddling the threshold
+    vals[7] = 1.0        # one tie over the whole row: every key passes the sampled threshold
     n = torch.tensor([ld, ld - 5, 70000, 2049, 65536, 131071, 4096, 100000], dtype=torch.int32, device=DEV)
-    a = torch.empty((T, 2048), dtype=torch.int32, device=DEV)
+    a = torch.empty((T * reps, 2048), dtype=torch.int32, device=DEV)
     b = torch.empty_like(a)
-    dsa.dsa_topk(vals, n, 2048, a)
-    dsa.dsa_topk(vals, n, 2048, b)
+    vals_r, n_r = vals.repeat(reps, 1), n.repeat(reps)
+    dsa.dsa_topk(vals_r, n_r, 2048, a)
+    dsa.dsa_topk(vals_r, n_r, 2048, b)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
     ref = oracle.topk(vals.cpu().double().numpy(), n.cpu().numpy(), 2048)
-    assert np.array_equal(a.cpu().numpy(), ref)
+    assert np.array_equal(a.cpu().numpy(), np.tile(ref, (reps, 1)))
 
 
 def _mla_case(T, S, H, k, seed, invalid_frac=0.0, rows=None):
