@@ -196,14 +196,26 @@ int dsa_sparse_mla_prefill(const void *q, const void *kv, int S,
  * LOGICAL positions, read from slot s % page_size of pool page
  * block_table[b*max_pages + s/page_size].  Entries outside [0, ctx_len[b]) are
  * skipped; a page id outside [0, num_pages) is skipped and flagged
- * DSA_DEV_BAD_PAGE.  Each row runs on one two-CTA cluster, as in prefill.
+ * DSA_DEV_BAD_PAGE.
+ *
+ * Work split.  Attention runs on two-CTA clusters, one per pair of SMs.  With
+ * more rows than two thirds of the clusters, each cluster takes whole rows, as
+ * in prefill.  With fewer, the flattened (row, 64-entry block of idx) space is
+ * cut into one contiguous share per cluster, so every SM works; a share that
+ * holds only part of a row writes that part's softmax-normalised output and
+ * LSE (fp32) to the workspace, and a second kernel merges the parts of each
+ * row by their LSEs (LSE = ln sum exp LSE_p, O = sum exp(LSE_p - LSE) O_p)
+ * into out and lse.  The split changes only the fp32 summation order.
  *
  *   q       [B, H, 576] bf16;  kv_pool [num_pages, page_size, 576] bf16
  *   block_table [B, max_pages] int32;  ctx_len [B] int32;  idx [B, k] int32
  *   out     [B, H, 512] bf16;  lse [B, H] fp32
  *   workspace: a device buffer of at least
- *           dsa_sparse_mla_decode_workspace_size(B, H, k) bytes (0 in this
- *           version: NULL is accepted), owned by the caller.
+ *           dsa_sparse_mla_decode_workspace_size(B, H, k) bytes, 256-byte
+ *           aligned, owned by the caller, used only while the call's kernels
+ *           run on `stream`; NULL is accepted when that size is 0.  Calls that
+ *           share one workspace must be ordered on the GPU (same stream).
+ *           A missing or short workspace returns DSA_ERR_WORKSPACE.
  */
 int dsa_sparse_mla_decode_paged(const void *q, const void *kv_pool, int num_pages, int page_size,
                                 const int32_t *block_table, int max_pages, const int32_t *ctx_len,
@@ -211,7 +223,10 @@ int dsa_sparse_mla_decode_paged(const void *q, const void *kv_pool, int num_page
                                 void *out, float *lse, void *workspace, size_t workspace_bytes,
                                 dsa_stream_t stream);
 
-/* Bytes of workspace dsa_sparse_mla_decode_paged needs for (B, H, k); 0 on bad input. */
+/* Bytes of workspace dsa_sparse_mla_decode_paged needs for (B, H, k) on the
+ * current device: 0 when the rows stay whole (3 B > 2 clusters), else
+ * 2 * clusters * H * 513 * 4, with clusters = min(SM pairs, B * ceil(k / 64)).
+ * 0 on bad input. */
 size_t dsa_sparse_mla_decode_workspace_size(int B, int H, int k);
 
 #ifdef __cplusplus

@@ -195,7 +195,9 @@ def dsa_sparse_mla_decode_workspace_size(B: int, H: int, k: int) -> int:
 def dsa_sparse_mla_decode_paged(q, kv_pool, block_table, ctx_len, idx, sm_scale: float, out, lse,
                                 workspace=None, stream=None):
     """Paged decode attention: q bf16 [B, H, 576], kv_pool bf16 [P, page, 576],
-    block_table int32 [B, max_pages], ctx_len int32 [B], idx int32 [B, k] (logical positions)."""
+    block_table int32 [B, max_pages], ctx_len int32 [B], idx int32 [B, k] (logical positions).
+    ``workspace``: a uint8 CUDA tensor of at least dsa_sparse_mla_decode_workspace_size(B, H, k)
+    bytes; when None and the call needs one, it is taken from PyTorch's allocator."""
     _need(q, torch.bfloat16, "q", 3)
     _need(kv_pool, torch.bfloat16, "kv_pool", 3)
     _need(block_table, torch.int32, "block_table", 2)
@@ -210,6 +212,10 @@ def dsa_sparse_mla_decode_paged(q, kv_pool, block_table, ctx_len, idx, sm_scale:
             or tuple(out.shape) != (B, H, 512) or tuple(lse.shape) != (B, H):
         raise ValueError("inconsistent shapes")
     ws_bytes = 0
+    if workspace is None:
+        need = dsa_sparse_mla_decode_workspace_size(B, H, k)
+        if need:  # device memory from PyTorch's caching allocator (256-byte aligned)
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     if workspace is not None:
         if not workspace.is_cuda or not workspace.is_contiguous():
             raise ValueError("workspace must be a contiguous CUDA tensor")

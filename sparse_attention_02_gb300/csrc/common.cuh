@@ -183,6 +183,12 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32
                  : "memory");
 }
 
+// Prefetch the cache line holding `src` into L2 (an ordinary load-unit instruction).
+__device__ __forceinline__ void prefetch_l2_line(const void *src)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
+}
+
 // --------------------------------------------------------------- cp.async 16B
 
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src)
@@ -428,6 +434,25 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank)
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
     return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void cluster_sync_all()

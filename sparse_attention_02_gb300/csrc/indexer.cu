@@ -201,28 +201,42 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI, PAGED>::THREADS, 1)
                 tma_load_2d(sbase + C::OFF_Q + g * C::QTILE, &tm_q, q_bar, 0, (r0 + g * C::G) * HI);
         }
         int issued = 0;
+        // paged: lane j holds the pool page of logical page bt_base + j; the warp
+        // refills all 32 with one load each when a tile runs past them
+        int bt_base = INT_MIN / 2, bt_page = -1;
         for (int it = 0; it < ntiles; ++it) {
             const int s = it % C::NSTAGE;
+            const int kt = kt0 + it;
+            if (PAGED) {
+                const int lp0 = (kt * kTileKeys) / p.page_size;
+                if (lp0 < bt_base || lp0 + kTileKeys / p.page_size > bt_base + 32) {
+                    bt_base = lp0;
+                    const int lp = lp0 + lane;
+                    bt_page = lp < p.max_pages ? __ldg(p.block_table + (int64_t)r0 * p.max_pages + lp) : -1;
+                }
+            }
             if (it >= C::NSTAGE &&
                 !mbar_wait_warp(empty_bar(s), ((it / C::NSTAGE) - 1) & 1, abort_flag, p.status))
                 break;
-            if (lane == 0) {
-                const int kt = kt0 + it;
-                const uint32_t dst = sbase + C::OFF_K + s * C::KSTAGE;
-                mbar_arrive_expect_tx(full_bar(s), C::KSTAGE);
-                if (!PAGED) {
+            const uint32_t dst = sbase + C::OFF_K + s * C::KSTAGE;
+            if (!PAGED) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(full_bar(s), C::KSTAGE);
                     tma_load_2d(dst, &tm_k, full_bar(s), 0, kt * kTileKeys);
-                } else {
-                    const int per_tile = kTileKeys / p.page_size;
-                    for (int j = 0; j < per_tile; ++j) {
-                        const int lp = (kt * kTileKeys) / p.page_size + j;
-                        int page = lp < p.max_pages ? p.block_table[(int64_t)r0 * p.max_pages + lp] : -1;
-                        // An invalid page loads out-of-range rows: TMA fills zeros and
-                        // the epilogue skips those keys.
-                        const int row = (page >= 0 && page < p.num_pages) ? page * p.page_size
-                                                                          : p.num_pages * p.page_size;
+                }
+            } else {
+                if (lane == 0)
+                    mbar_arrive_expect_tx(full_bar(s), C::KSTAGE);
+                const int per_tile = kTileKeys / p.page_size;
+                const int lp0 = (kt * kTileKeys) / p.page_size;
+                for (int j = 0; j < per_tile; ++j) {
+                    const int page = __shfl_sync(0xffffffffu, bt_page, lp0 + j - bt_base);
+                    // An invalid page loads out-of-range rows: TMA fills zeros and
+                    // the epilogue skips those keys.
+                    const int row = (page >= 0 && page < p.num_pages) ? page * p.page_size
+                                                                      : p.num_pages * p.page_size;
+                    if (lane == 0)
                         tma_load_2d(dst + j * p.page_size * DI, &tm_k, full_bar(s), 0, row);
-                    }
                 }
             }
             ++issued;
@@ -458,6 +472,26 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI, PAGED>::THREADS, 1)
         const int half = (warp - 2) >> 2;
         const int key_in_tile = quad * 32 + lane;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        // paged: this thread's key's pool page and scale run two and one tiles
+        // ahead (page of tile it + 2 and scale of tile it + 1 loaded during tile
+        // it), so no tile waits on the block table
+        auto page_of = [&](int it) -> int {
+            const int64_t sk = (int64_t)(kt0 + it) * kTileKeys + key_in_tile;
+            const int lp = (int)(sk / p.page_size);
+            return (it < ntiles && lp < p.max_pages) ? __ldg(p.block_table + (int64_t)r0 * p.max_pages + lp) : -1;
+        };
+        auto scale_of = [&](int it, int page) -> float {
+            const int64_t sk = (int64_t)(kt0 + it) * kTileKeys + key_in_tile;
+            return (page >= 0 && page < p.num_pages) ? __ldg(p.k_scale + (int64_t)page * p.page_size + sk % p.page_size)
+                                                     : 0.f;
+        };
+        int pg0 = 0, pg1 = 0;
+        float ks0 = 0.f;
+        if (PAGED) {
+            pg0 = page_of(0);
+            pg1 = page_of(1);
+            ks0 = scale_of(0, pg0);
+        }
         for (int it = 0; it < ntiles; ++it) {
             const int kt = kt0 + it;
             const int64_t s = (int64_t)kt * kTileKeys + key_in_tile;
@@ -467,12 +501,13 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI, PAGED>::THREADS, 1)
                 key_ok = s < p.S;
                 ks = key_ok ? p.k_scale[s] : 0.f;
             } else {
-                const int lp = (int)(s / p.page_size);
-                const int page = lp < p.max_pages ? p.block_table[(int64_t)r0 * p.max_pages + lp] : -1;
-                key_ok = page >= 0 && page < p.num_pages;
+                key_ok = pg0 >= 0 && pg0 < p.num_pages;
                 if (!key_ok && s <= pos_s[0] && lane == 0)
                     atomicOr(p.status, DSA_DEV_BAD_PAGE);
-                ks = key_ok ? p.k_scale[(int64_t)page * p.page_size + s % p.page_size] : 0.f;
+                ks = ks0;
+                ks0 = scale_of(it + 1, pg1);
+                pg0 = pg1;
+                pg1 = page_of(it + 2);
             }
             bool ok = true;
             for (int g = 0; g < C::NGROUP; ++g) {
@@ -535,6 +570,343 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI, PAGED>::THREADS, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Paged form for batches of at most kFlatRows rows (decode): a persistent grid
+// of two CTAs per SM.  Row r needs key tiles [0, q_pos[r] / 128 + 1); the rows'
+// tiles laid end to end form one list, and CTA c takes the contiguous share
+// [c * total / C, (c + 1) * total / C), so every CTA scores the same number of
+// tiles whatever the context lengths and pays its setup once.  A share crosses
+// row boundaries: the query tile (TMA) and the folded head weights of each row
+// it touches go through two buffers, so the next row's query loads while the
+// current row is scored.  Roles as above: warp 0 loads, warp 1 issues the
+// MMAs, warps 2..5 (one per TMEM lane quadrant, one key per thread) reduce
+// over the heads.
+constexpr int kFlatRows = 1024;
+
+template <int HI, int DI>
+struct FlatCfg {
+    static constexpr int N = HI;
+    static constexpr int NEPI = 4;
+    static constexpr int THREADS = 64 + 32 * NEPI;
+    static constexpr int NSTAGE = 5;
+    static constexpr int QTILE = N * DI;
+    static constexpr int KSTAGE = kTileKeys * DI;
+    static constexpr int TMEM_COLS = 2 * N <= 64 ? 64 : (2 * N <= 128 ? 128 : 256);
+    static constexpr uint32_t SWZ = 2u; // d_I = 128: 128-byte rows, 128-byte swizzle
+    static constexpr uint32_t SBO = 8 * DI;
+    static constexpr int OFF_Q = 0;                                 // two query tiles
+    static constexpr int OFF_K = ((2 * QTILE + 1023) / 1024) * 1024; // key ring
+    static constexpr int OFF_W = OFF_K + NSTAGE * KSTAGE;           // [2][HI] folded weights
+    static constexpr int OFF_PRE = OFF_W + 2 * HI * 4;              // [kFlatRows + 1] tile prefix
+    static constexpr int OFF_BAR = ((OFF_PRE + (kFlatRows + 1) * 4 + 7) / 8) * 8;
+    static constexpr int NBAR = 2 * NSTAGE + 2 + 2 + 2 + 2 + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM = OFF_MISC + 64 + 1024;
+    static_assert(DI == 128 && N % 32 == 0 && N >= 32 && N <= 128, "flat indexer shape");
+};
+
+// Units of a share: (row r, its tiles [a, b)) in order.
+struct FlatUnits {
+    int g, g1;
+    __device__ FlatUnits(int g0_, int g1_) : g(g0_), g1(g1_) {}
+    __device__ bool next(const int *pre, int T, int &r, int &a, int &b)
+    {
+        if (g >= g1)
+            return false;
+        int lo = 0, hi = T - 1; // last row with pre[row] <= g: the non-empty row holding tile g
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (pre[mid] <= g)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        r = lo;
+        const int e = pre[r + 1] < g1 ? pre[r + 1] : g1;
+        a = g - pre[r];
+        b = e - pre[r];
+        g = e;
+        return true;
+    }
+};
+
+template <int HI, int DI>
+__global__ void __launch_bounds__(FlatCfg<HI, DI>::THREADS, 2)
+    indexer_paged_flat_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                              Params p)
+{
+    using C = FlatCfg<HI, DI>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    float *wq_s = reinterpret_cast<float *>(smem + C::OFF_W);
+    int *pre_s = reinterpret_cast<int *>(smem + C::OFF_PRE);
+    const uint32_t bar0 = sbase + C::OFF_BAR;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (C::NSTAGE + s); };
+    auto accf_bar = [&](int a) { return bar0 + 8u * (2 * C::NSTAGE + a); };
+    auto acce_bar = [&](int a) { return bar0 + 8u * (2 * C::NSTAGE + 2 + a); };
+    auto qfull_bar = [&](int b) { return bar0 + 8u * (2 * C::NSTAGE + 4 + b); };
+    auto qempty_bar = [&](int b) { return bar0 + 8u * (2 * C::NSTAGE + 6 + b); };
+    const uint32_t done_bar = bar0 + 8u * (2 * C::NSTAGE + 8);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+    int *pos_s = reinterpret_cast<int *>(smem + C::OFF_MISC + 8); // [2]: position of the row in each buffer
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t key_limit = (int64_t)p.max_pages * p.page_size;
+    const int64_t lim = (key_limit < p.ld ? key_limit : p.ld) - 1;
+    auto clamp_pos = [&](int r) -> int {
+        int64_t qp = p.q_pos[r];
+        if (qp > lim)
+            qp = lim;
+        return qp < 0 ? -1 : static_cast<int>(qp);
+    };
+
+    // ---- tile prefix over the rows (warp 0; lane l sums rows [l * per, l * per + per))
+    if (warp == 0) {
+        const int per = (p.T + 31) / 32;
+        int cnt = 0;
+        for (int i = 0; i < per; ++i) {
+            const int r = lane * per + i;
+            if (r < p.T) {
+                if (blockIdx.x == 0 && p.q_pos[r] > lim)
+                    atomicOr(p.status, DSA_DEV_BAD_POSITION);
+                const int pos = clamp_pos(r);
+                cnt += pos < 0 ? 0 : pos / kTileKeys + 1;
+            }
+        }
+        int x = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o)
+                x += y;
+        }
+        int run = x - cnt;
+        for (int i = 0; i < per; ++i) {
+            const int r = lane * per + i;
+            if (r < p.T) {
+                pre_s[r] = run;
+                const int pos = clamp_pos(r);
+                run += pos < 0 ? 0 : pos / kTileKeys + 1;
+            }
+        }
+        if (lane == 31)
+            pre_s[p.T] = x;
+    }
+    if (threadIdx.x == 32) {
+        for (int s = 0; s < C::NSTAGE; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(accf_bar(a), 1);
+            mbar_init(acce_bar(a), C::NEPI);
+            mbar_init(qfull_bar(a), 1);
+            mbar_init(qempty_bar(a), 1 + C::NEPI); // the MMAs of the row, then each epilogue warp
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const int total = pre_s[p.T];
+    const int g0 = static_cast<int>((int64_t)blockIdx.x * total / gridDim.x);
+    const int g1 = static_cast<int>((int64_t)(blockIdx.x + 1) * total / gridDim.x);
+    if (g1 <= g0)
+        return; // uniform: an empty share
+
+    if (warp == 1)
+        tmem_alloc(sbase + C::OFF_MISC, C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    FlatUnits units(g0, g1);
+    int r = 0, ta = 0, tb = 0;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+        }
+        int it = 0, u = 0;
+        bool ok = true;
+        while (ok && units.next(pre_s, p.T, r, ta, tb)) {
+            const int qb = u & 1;
+            if (u >= 2 && !mbar_wait_warp(qempty_bar(qb), ((u >> 1) - 1) & 1, abort_flag, p.status))
+                break;
+            const float qs = p.q_scale[r];
+            for (int h = lane; h < HI; h += 32)
+                wq_s[qb * HI + h] = p.w[(int64_t)r * HI + h] * qs;
+            if (lane == 0)
+                pos_s[qb] = clamp_pos(r);
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive_expect_tx(qfull_bar(qb), C::QTILE);
+                tma_load_2d(sbase + C::OFF_Q + qb * C::QTILE, &tm_q, qfull_bar(qb), 0, r * HI);
+            }
+            ++u;
+            // lane j holds the pool page of logical page bt_base + j
+            int bt_base = INT_MIN / 2, bt_page = -1;
+            const int per_tile = kTileKeys / p.page_size;
+            for (int kt = ta; kt < tb; ++kt, ++it) {
+                const int s = it % C::NSTAGE;
+                const int lp0 = (kt * kTileKeys) / p.page_size;
+                if (lp0 < bt_base || lp0 + per_tile > bt_base + 32) {
+                    bt_base = lp0;
+                    const int lp = lp0 + lane;
+                    bt_page = lp < p.max_pages ? __ldg(p.block_table + (int64_t)r * p.max_pages + lp) : -1;
+                }
+                if (it >= C::NSTAGE &&
+                    !mbar_wait_warp(empty_bar(s), ((it / C::NSTAGE) - 1) & 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t dst = sbase + C::OFF_K + s * C::KSTAGE;
+                if (lane == 0)
+                    mbar_arrive_expect_tx(full_bar(s), C::KSTAGE);
+                for (int j = 0; j < per_tile; ++j) {
+                    const int page = __shfl_sync(0xffffffffu, bt_page, lp0 + j - bt_base);
+                    // an invalid page loads rows past the pool: TMA fills zeros and the
+                    // epilogue skips those keys
+                    const int row = (page >= 0 && page < p.num_pages) ? page * p.page_size : p.num_pages * p.page_size;
+                    if (lane == 0)
+                        tma_load_2d(dst + j * p.page_size * DI, &tm_k, full_bar(s), 0, row);
+                }
+                __syncwarp();
+            }
+        }
+        // drain: every load issued has landed before the CTA exits
+        if (lane == 0) {
+            for (int v = u - 2 > 0 ? u - 2 : 0; v < u; ++v)
+                mbar_drain(qfull_bar(v & 1), (v >> 1) & 1);
+            for (int i = it - C::NSTAGE > 0 ? it - C::NSTAGE : 0; i < it; ++i)
+                mbar_drain(full_bar(i % C::NSTAGE), (i / C::NSTAGE) & 1);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        constexpr uint32_t idesc = idesc_f32acc(128, C::N, 0u, false, false);
+        int it = 0, u = 0;
+        bool ok = true;
+        while (ok && units.next(pre_s, p.T, r, ta, tb)) {
+            const int qb = u & 1;
+            if (!mbar_wait_warp(qfull_bar(qb), (u >> 1) & 1, abort_flag, p.status))
+                break;
+            for (int kt = ta; kt < tb; ++kt, ++it) {
+                const int s = it % C::NSTAGE;
+                const int acc = it & 1, use = it >> 1;
+                if (!mbar_wait_warp(full_bar(s), (it / C::NSTAGE) & 1, abort_flag, p.status) ||
+                    (use >= 1 && !mbar_wait_warp(acce_bar(acc), (use - 1) & 1, abort_flag, p.status))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t abase = sbase + C::OFF_K + s * C::KSTAGE;
+                    const uint32_t bbase = sbase + C::OFF_Q + qb * C::QTILE;
+#pragma unroll
+                    for (int kk = 0; kk < DI / 32; ++kk) {
+                        const uint64_t ad = sdesc(abase + kk * 32, 16, C::SBO, C::SWZ);
+                        const uint64_t bd = sdesc(bbase + kk * 32, 16, C::SBO, C::SWZ);
+                        umma_f8f6f4(tmem + acc * C::N, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(accf_bar(acc));
+                    umma_commit(empty_bar(s));
+                }
+                __syncwarp();
+            }
+            if (lane == 0)
+                umma_commit(qempty_bar(qb)); // the query tile is free once these MMAs complete
+            __syncwarp();
+            ++u;
+        }
+        if (lane == 0) {
+            umma_commit(done_bar);
+            mbar_drain(done_bar, 0);
+        }
+        __syncwarp();
+    } else {
+        // --------------------------------------------------------- epilogue
+        const int quad = warp & 3;
+        const int key_in_tile = quad * 32 + lane;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        int it = 0, u = 0;
+        bool ok = true;
+        while (ok && units.next(pre_s, p.T, r, ta, tb)) {
+            const int qb = u & 1;
+            if (!mbar_wait_warp(qfull_bar(qb), (u >> 1) & 1, abort_flag, p.status))
+                break;
+            const int pos = pos_s[qb];
+            const float4 *w4 = reinterpret_cast<const float4 *>(wq_s + qb * HI);
+            // this thread's key's pool page and scale, two and one tiles ahead
+            auto page_of = [&](int kt) -> int {
+                const int lp = (int)(((int64_t)kt * kTileKeys + key_in_tile) / p.page_size);
+                return (kt < tb && lp < p.max_pages) ? __ldg(p.block_table + (int64_t)r * p.max_pages + lp) : -1;
+            };
+            auto scale_of = [&](int kt, int page) -> float {
+                const int64_t sk = (int64_t)kt * kTileKeys + key_in_tile;
+                return (page >= 0 && page < p.num_pages)
+                           ? __ldg(p.k_scale + (int64_t)page * p.page_size + sk % p.page_size)
+                           : 0.f;
+            };
+            int pg0 = page_of(ta), pg1 = page_of(ta + 1);
+            float ks0 = scale_of(ta, pg0);
+            for (int kt = ta; kt < tb; ++kt, ++it) {
+                const int64_t s = (int64_t)kt * kTileKeys + key_in_tile;
+                const bool key_ok = pg0 >= 0 && pg0 < p.num_pages;
+                if (!key_ok && s <= pos && lane == 0)
+                    atomicOr(p.status, DSA_DEV_BAD_PAGE);
+                const float ks = ks0;
+                ks0 = scale_of(kt + 1, pg1);
+                pg0 = pg1;
+                pg1 = page_of(kt + 2);
+                const int acc = it & 1, use = it >> 1;
+                if (!mbar_wait_warp(accf_bar(acc), use & 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t v[HI];
+#pragma unroll
+                for (int c0 = 0; c0 < HI; c0 += 32)
+                    tmem_ld32(lane_base + acc * C::N + c0, *reinterpret_cast<uint32_t(*)[32]>(v + c0));
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(acce_bar(acc));
+                float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                for (int h4 = 0; h4 < HI / 4; ++h4) {
+                    const float4 wv = w4[h4];
+                    a0 = fmaf(fmaxf(__uint_as_float(v[4 * h4]), 0.f), wv.x, a0);
+                    a1 = fmaf(fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f), wv.y, a1);
+                    a0 = fmaf(fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f), wv.z, a0);
+                    a1 = fmaf(fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f), wv.w, a1);
+                }
+                if (key_ok && s <= pos)
+                    p.logits[(int64_t)r * p.ld + s] = (a0 + a1) * ks;
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(qempty_bar(qb)); // done with this buffer's weights and position
+            ++u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
 template <int HI, int DI, bool PAGED>
 int launch_cfg(const IndexerArgs &a, cudaStream_t stream, char *err, size_t errlen)
 {
@@ -583,6 +955,31 @@ int launch_cfg(const IndexerArgs &a, cudaStream_t stream, char *err, size_t errl
     if (!p.status) {
         snprintf(err, errlen, "device status word unavailable");
         return DSA_ERR_CUDA;
+    }
+    if constexpr (PAGED && DI == 128 && (HI == 64 || HI == 32)) {
+        // decode-sized batches: the persistent flat schedule (tile counts fit int)
+        const int64_t keys = (int64_t)a.max_pages * a.page_size < a.ld ? (int64_t)a.max_pages * a.page_size : a.ld;
+        if (a.T <= kFlatRows && (int64_t)a.T * ((keys + kTileKeys - 1) / kTileKeys) < INT_MAX) {
+            using F = FlatCfg<HI, DI>;
+            static bool flat_attr[64] = {};
+            if (dev < 64 && !flat_attr[dev]) {
+                cudaError_t e = cudaFuncSetAttribute(indexer_paged_flat_kernel<HI, DI>,
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, F::SMEM);
+                if (e != cudaSuccess) {
+                    snprintf(err, errlen, "cudaFuncSetAttribute(indexer flat): %s", cudaGetErrorString(e));
+                    return DSA_ERR_CUDA;
+                }
+                flat_attr[dev] = true;
+            }
+            p.splits = 1;
+            indexer_paged_flat_kernel<HI, DI><<<2 * num_sms(), F::THREADS, F::SMEM, stream>>>(tq, tk, p);
+            cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) {
+                snprintf(err, errlen, "indexer launch: %s", cudaGetErrorString(e));
+                return DSA_ERR_CUDA;
+            }
+            return DSA_OK;
+        }
     }
     const int groups = (a.T + C::R - 1) / C::R;
     int splits = 1;

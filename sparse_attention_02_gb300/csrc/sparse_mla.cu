@@ -82,6 +82,7 @@ constexpr int kKVAtom = kBN * 128;       // bytes of one KV atom (64 rows x 128 
 constexpr int kKVHalf = kBN * 64;        // bytes of the RoPE half atom (64 rows x 64 B, SW64)
 constexpr int kStage = kVAtoms * kKVAtom + kKVHalf; // 36 KB
 constexpr int kNStage = 4;
+constexpr int kPf = 3;                   // blocks ahead whose rows the producers prefetch into L2
 constexpr int kXBuf = 128 * kBN * 2;     // one swap buffer: 128 heads x 64 fp16
 constexpr int kProdWarps = 4;
 constexpr int kPvWarp = kProdWarps;      // all PV MMAs (fixed accumulation order) + TMEM owner
@@ -131,6 +132,71 @@ struct Params {
     int max_pages, num_pages, page_size;
     const int32_t *ctx_len;
     unsigned *status;
+    // work split (decode with fewer rows than clusters): see Units
+    int split, nbk, ncl;       // split flag, 64-key blocks per row (ceil(k / 64)), clusters in the grid
+    float *ws_o;               // [2 * ncl, H, 512] fp32 partial outputs (normalised by their own sum)
+    float *ws_lse;             // [2 * ncl, H] fp32 partial LSEs
+};
+
+// Work units of cluster c.  Unsplit: whole rows t = c, c + ncl, ...  Split:
+// the cluster's share [start(c), start(c + 1)) of the flattened (row, 64-key
+// block) space, start(c) = floor(c * T * nbk / ncl), cut at row boundaries.
+// With T < ncl a share is shorter than a row, so it touches at most two rows;
+// a piece that is not a whole row goes to workspace slot 2c + (its row - the
+// share's first row), and combine_kernel merges the pieces of each row.
+struct Unit {
+    int t, jb, je; // row, blocks [jb, je)
+    int slot;      // -1: the whole row, written to out/lse directly
+};
+
+__device__ __forceinline__ int64_t share_start(const Params &p, int c)
+{
+    return (int64_t)c * p.T * p.nbk / p.ncl;
+}
+
+struct Units {
+    int64_t g, g1;
+    int t_first, cid;
+    __device__ Units(const Params &p, int c) : cid(c)
+    {
+        if (p.split) {
+            g = share_start(p, c);
+            g1 = share_start(p, c + 1);
+            t_first = static_cast<int>(g / p.nbk);
+        } else {
+            g = c;
+            g1 = p.T;
+            t_first = 0;
+        }
+    }
+    __device__ bool next(const Params &p, Unit &u)
+    {
+        if (g >= g1)
+            return false;
+        if (!p.split) {
+            u.t = static_cast<int>(g);
+            u.jb = 0;
+            u.je = p.nbk;
+            u.slot = -1;
+            g += p.ncl;
+            return true;
+        }
+        u.t = static_cast<int>(g / p.nbk);
+        u.jb = static_cast<int>(g - (int64_t)u.t * p.nbk);
+        const int64_t row_end = (int64_t)(u.t + 1) * p.nbk;
+        const int64_t end = row_end < g1 ? row_end : g1;
+        u.je = static_cast<int>(end - (int64_t)u.t * p.nbk);
+        u.slot = (u.jb == 0 && u.je == p.nbk) ? -1 : 2 * cid + (u.t - t_first);
+        g = end;
+        return true;
+    }
+    // row of the unit after the current one, or -1
+    __device__ int peek_row(const Params &p) const
+    {
+        if (g >= g1)
+            return -1;
+        return p.split ? static_cast<int>(g / p.nbk) : static_cast<int>(g);
+    }
 };
 
 // Latent row of a selected entry: >= 0 valid, -1 skipped, -2 bad page (skipped, flagged).
@@ -202,7 +268,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t rank = cluster_ctarank();
     const uint32_t peer = rank ^ 1u;
     const int cid = blockIdx.x >> 1;
-    const int ncl = gridDim.x >> 1;
 
     // ---- one-time setup
     if (threadIdx.x == 0) {
@@ -265,20 +330,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t J = 0;
         int u = 0;
         bool ok = true;
-        for (int t = cid; ok && t < p.T; t += ncl, ++u) {
+        Units it(p, cid);
+        Unit un;
+        for (; ok && it.next(p, un); ++u) {
+            const int t = un.t;
             const int32_t *idx_row = p.idx + (int64_t)t * p.k;
             const int ctx = PAGED ? p.ctx_len[t] : 0;
-            // blocks up to the last in-range entry
+            // the unit's blocks up to its last in-range entry.  Paged (decode: the
+            // scan sits before the unit's first gather, nothing hides it): 16-byte
+            // loads, a unit holds at most 64 blocks = 4096 entries = 32 loads per
+            // lane; prefill overlaps the scan with the previous token's blocks
             int last = -1;
+            const int i_beg = un.jb * kBN;
+            const int i_end = un.je * kBN < p.k ? un.je * kBN : p.k;
+            if (PAGED && (p.k & 3) == 0 && (reinterpret_cast<uintptr_t>(p.idx) & 15u) == 0) {
+                const int4 *q4 = reinterpret_cast<const int4 *>(idx_row);
+#pragma unroll 16
+                for (int m = 0; m < 32; ++m) {
+                    const int i = i_beg + 4 * (lane + 32 * m);
+                    if (i < i_end) {
+                        const int4 v = __ldg(q4 + (i >> 2));
+                        const int vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (i + e < i_end && in_range<PAGED>(p, vv[e], ctx))
+                                last = i + e;
+                    }
+                }
+            } else {
 #pragma unroll 8
-            for (int i = lane; i < p.k; i += 32)
-                if (in_range<PAGED>(p, idx_row[i], ctx))
-                    last = i;
+                for (int i = i_beg + lane; i < i_end; i += 32)
+                    if (in_range<PAGED>(p, idx_row[i], ctx))
+                        last = i;
+            }
             for (int o = 16; o > 0; o >>= 1) {
                 const int y = __shfl_xor_sync(0xffffffffu, last, o);
                 last = y > last ? y : last;
             }
-            const int nb = last < 0 ? 0 : last / kBN + 1;
+            const int nb = last < 0 ? 0 : last / kBN + 1 - un.jb;
             // Q (shared memory and TMEM parts) is reused: the score MMAs must be
             // done reading the previous token's Q; warp 0 also reuses the nb slot,
             // which the softmax, sender and PV warps must have taken
@@ -301,10 +390,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     } else {
                         mbar_arrive(bar(B_QF));
                     }
-                    if (t + ncl < p.T) {
+                    const int tn = it.peek_row(p);
+                    if (tn >= 0 && tn != t) {
                         for (int a = 0; a < 4; ++a)
-                            tma_prefetch_l2_2d(&tm_q, x0 + 64 * a, (t + ncl) * p.H);
-                        tma_prefetch_l2_2d(&tm_q, 512, (t + ncl) * p.H); // ... and its RoPE half
+                            tma_prefetch_l2_2d(&tm_q, x0 + 64 * a, tn * p.H);
+                        tma_prefetch_l2_2d(&tm_q, 512, tn * p.H); // ... and its RoPE half
                     }
                 }
                 __syncwarp();
@@ -358,12 +448,91 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     atomicOr(p.status, DSA_DEV_BAD_PAGE);
                 return r;
             };
-            int my_row = nb > 0 ? resolve(0) : -1;
+            // Paged (decode): L2 prefetch of this CTA's columns of the rows kPf
+            // blocks ahead, so the stages fill from L2 although the rows come from
+            // HBM.  Five 128-byte lines per row: lanes 0..15 take lines 0..2 of the
+            // V quarter of row q_row0 + (lane & 15), lanes 16..31 line 3 and the
+            // line holding the RoPE half.  (Prefill's latent rows sit in L2.)
+            // The two dependent loads that locate a row (selected position, then
+            // block-table entry) run as a software pipeline one block apart, so
+            // no load result is waited for in the iteration that issued it.
+            auto pf_raw_of = [&](int jj) -> int { // selected position of block jb + jj for this lane's row
+                const int i = (un.jb + jj) * kBN + q_row0 + (lane & 15);
+                return (jj < nb && i < p.k) ? __ldg(idx_row + i) : -1;
+            };
+            auto pf_page_of = [&](int sp) -> int { // its pool page, or -1 (no load when out of range)
+                if (sp < 0 || sp >= ctx || sp / p.page_size >= p.max_pages)
+                    return -1;
+                return __ldg(p.block_table + (int64_t)t * p.max_pages + sp / p.page_size);
+            };
+            auto pf_row_of = [&](int sp, int page) -> int { // latent row, -1 skipped, -2 bad page
+                if (sp < 0 || sp >= ctx || sp / p.page_size >= p.max_pages)
+                    return -1;
+                if (page < 0 || page >= p.num_pages) {
+                    if (lane < 16)
+                        atomicOr(p.status, DSA_DEV_BAD_PAGE);
+                    return -2;
+                }
+                return page * p.page_size + sp % p.page_size;
+            };
+            auto prefetch = [&](int row) {
+                if (row >= 0) {
+                    const __nv_bfloat16 *v = kv_cols + (int64_t)row * kD;
+                    if (lane < 16) {
+                        prefetch_l2_line(v);
+                        prefetch_l2_line(v + 64);
+                        prefetch_l2_line(v + 128);
+                    } else {
+                        prefetch_l2_line(v + 192);
+                        prefetch_l2_line(rope_cols + (int64_t)row * kD);
+                    }
+                }
+            };
+            // Paged: rw[q] is this lane's latent row of block j + q; the rows of
+            // block j + kPf come out of a pipeline whose loads are a block apart
+            // (position of block j + kPf + 2, page of block j + kPf + 1 issued
+            // now), get prefetched into L2 and join the ring.
+            int rw[kPf];
+            int pf_s = -1, pf_page = -1, pf_raw = -1;
+            int my_row = -1;
+            if (PAGED) {
+                int sp[kPf + 2], pg[kPf + 1];
+#pragma unroll
+                for (int jj = 0; jj < kPf + 2; ++jj)
+                    sp[jj] = pf_raw_of(jj);
+#pragma unroll
+                for (int jj = 0; jj < kPf + 1; ++jj)
+                    pg[jj] = pf_page_of(sp[jj]);
+#pragma unroll
+                for (int jj = 0; jj < kPf; ++jj) {
+                    rw[jj] = pf_row_of(sp[jj], pg[jj]);
+                    if (jj > 0)
+                        prefetch(rw[jj]);
+                }
+                pf_s = sp[kPf];
+                pf_page = pg[kPf];
+                pf_raw = sp[kPf + 1];
+            } else {
+                my_row = nb > 0 ? resolve(un.jb) : -1;
+            }
             for (int j = 0; j < nb; ++j, ++J) {
                 const int st = J % kNStage;
-                const int cur = my_row;
-                if (j + 1 < nb)
-                    my_row = resolve(j + 1); // next block's rows, ahead of the stage wait
+                int cur;
+                if (PAGED) {
+                    cur = rw[0];
+#pragma unroll
+                    for (int q = 0; q + 1 < kPf; ++q)
+                        rw[q] = rw[q + 1];
+                    rw[kPf - 1] = pf_row_of(pf_s, pf_page); // block j + kPf
+                    prefetch(rw[kPf - 1]);
+                    pf_s = pf_raw;                          // block j + kPf + 1: its page
+                    pf_page = pf_page_of(pf_raw);
+                    pf_raw = pf_raw_of(j + kPf + 2);        // block j + kPf + 2: its position
+                } else {
+                    cur = my_row;
+                    if (j + 1 < nb)
+                        my_row = resolve(un.jb + j + 1); // next block's rows, ahead of the stage wait
+                }
                 if (J >= kNStage &&
                     !mbar_wait_warp(bar(B_KVE + st), ((J / kNStage) - 1) & 1, abort_flag, p.status)) {
                     ok = false;
@@ -401,7 +570,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t J = 0;
         int u = 0, v = 0;
         bool ok = true;
-        for (int t = cid; ok && t < p.T; t += ncl, ++u) {
+        Units it(p, cid);
+        Unit un;
+        for (; ok && it.next(p, un); ++u) {
             if (!mbar_wait_warp(bar(B_QF), u & 1, abort_flag, p.status)) {
                 ok = false;
                 break;
@@ -468,7 +639,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         const uint64_t kv_desc0 = sdesc(sbase + OFF_KV, 16, 1024, 2);
         const uint64_t kvh_desc0 = sdesc(sbase + OFF_KV + kVAtoms * kKVAtom, 16, 512, 4);
-        for (int t = cid; ok && t < p.T; t += ncl, ++u) {
+        Units it(p, cid);
+        Unit un;
+        for (; ok && it.next(p, un); ++u) {
             if (!mbar_wait_warp(bar(B_QF), u & 1, abort_flag, p.status)) {
                 ok = false;
                 break;
@@ -531,7 +704,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t J = 0;
         int u = 0;
         bool ok = true;
-        for (int t = cid; ok && t < p.T; t += ncl, ++u) {
+        Units it(p, cid);
+        Unit un;
+        for (; ok && it.next(p, un); ++u) {
             if (!mbar_wait_warp(bar(B_QF), u & 1, abort_flag, p.status)) {
                 ok = false;
                 break;
@@ -595,7 +770,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t J = 0;
         int u = 0, v = 0;
         bool ok = true;
-        for (int t = cid; ok && t < p.T; t += ncl, ++u) {
+        Units it(p, cid);
+        Unit un;
+        for (; ok && it.next(p, un); ++u) {
+            const int t = un.t;
             const int32_t *idx_row = p.idx + (int64_t)t * p.k;
             const int ctx = PAGED ? p.ctx_len[t] : 0;
             if (!mbar_wait_warp(bar(B_QF), u & 1, abort_flag, p.status)) {
@@ -608,13 +786,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 mbar_arrive(bar(B_QA)); // this token's nb slot has been read
             float m_run = -INFINITY; // running max, log2 domain (same in both sibling warps)
             float l_run = 0.f;       // this warp's partial row sum
-            int32_t raw = 32 * hf + lane < p.k ? idx_row[32 * hf + lane] : -1;
+            const int i0 = un.jb * kBN + 32 * hf + lane;
+            int32_t raw = i0 < p.k ? idx_row[i0] : -1;
+            // Paged: an entry is valid when its position is in the context and its
+            // block-table entry names a pool page.  The block-table entry of block
+            // j + 1 and the position of block j + 2 are loaded during block j, so
+            // the mask never waits for a load.
+            auto page_of = [&](int32_t sp) -> int {
+                if (sp < 0 || sp >= ctx || sp / p.page_size >= p.max_pages)
+                    return -1;
+                return __ldg(p.block_table + (int64_t)t * p.max_pages + sp / p.page_size);
+            };
+            int pg = 0, raw_n = -1;
+            if (PAGED) {
+                pg = page_of(raw);
+                const int n1 = i0 + kBN;
+                raw_n = n1 < p.k ? idx_row[n1] : -1;
+            }
             for (int j = 0; j < nb; ++j, ++J) {
                 const int b = J & 1;
-                // validity of this warp's 32 entries; prefetch the next block's index
-                const uint32_t vmask = __ballot_sync(0xffffffffu, latent_row<PAGED>(p, t, raw, ctx) >= 0);
-                {
-                    const int n0 = (j + 1) * kBN + 32 * hf + lane;
+                // validity of this warp's 32 entries; the next block's index ahead
+                uint32_t vmask;
+                if (PAGED) {
+                    vmask = __ballot_sync(0xffffffffu, raw >= 0 && raw < ctx && pg >= 0 && pg < p.num_pages);
+                    raw = raw_n;
+                    pg = page_of(raw);
+                    const int n2 = i0 + (j + 2) * kBN;
+                    raw_n = n2 < p.k ? idx_row[n2] : -1;
+                } else {
+                    vmask = __ballot_sync(0xffffffffu, latent_row<PAGED>(p, t, raw, ctx) >= 0);
+                    const int n0 = (un.jb + j + 1) * kBN + 32 * hf + lane;
                     raw = n0 < p.k ? idx_row[n0] : -1;
                 }
                 // 1. this CTA's partial scores (fp16 pairs parked by the senders) and the peer's half
@@ -754,7 +955,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tmem_ld_wait();
             const float l_tot = hf == 0 ? l_run + l_other : l_other + l_run;
             const bool store = h < p.H;
+            const bool part = un.slot >= 0; // a piece of a split row: fp32 O / l and LSE into the workspace
             __nv_bfloat16 *orow = p.out + ((int64_t)t * p.H + h) * kDv + 256 * rank + 128 * hf;
+            float *prow = part ? p.ws_o + ((int64_t)un.slot * p.H + h) * kDv + 256 * rank + 128 * hf : nullptr;
             if (nb > 0) {
                 if (!mbar_wait_warp(bar(B_OF), v & 1, abort_flag, p.status)) {
                     ok = false;
@@ -768,6 +971,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     uint32_t r[32];
                     tmem_ld32(tmem + lane_off + TM_O + 128 * hf + c0, r);
                     tmem_ld_wait();
+                    if (part) {
+                        if (store) {
+                            float4 *dst = reinterpret_cast<float4 *>(prow + c0);
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                dst[c] = make_float4(__uint_as_float(r[4 * c]) * inv_l, __uint_as_float(r[4 * c + 1]) * inv_l,
+                                                     __uint_as_float(r[4 * c + 2]) * inv_l,
+                                                     __uint_as_float(r[4 * c + 3]) * inv_l);
+                        }
+                        continue;
+                    }
                     uint32_t o[16];
 #pragma unroll
                     for (int c = 0; c < 16; ++c)
@@ -783,14 +997,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(bar(B_OE));
+            } else if (store && part) {
+                float4 *dst = reinterpret_cast<float4 *>(prow);
+                for (int c = 0; c < 128 / 4; ++c)
+                    dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
             } else if (store) {
                 uint4 *dst = reinterpret_cast<uint4 *>(orow);
                 for (int c = 0; c < 128 / 8; ++c)
                     dst[c] = make_uint4(0, 0, 0, 0);
             }
-            if (store && rank == 0 && hf == 0)
-                p.lse[(int64_t)t * p.H + h] =
-                    l_tot > 0.f ? (m_run + __log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
+            if (store && rank == 0 && hf == 0) {
+                const float lv = l_tot > 0.f ? (m_run + __log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
+                if (part)
+                    p.ws_lse[(int64_t)un.slot * p.H + h] = lv;
+                else
+                    p.lse[(int64_t)t * p.H + h] = lv;
+            }
         }
     }
 
@@ -801,6 +1023,102 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+}
+
+// Merges the pieces of each split row: for a row covered by clusters
+// c_lo < ... < c_hi with piece LSEs L_c and outputs O_c (each normalised by
+// its own sum), LSE = ln sum_c exp(L_c) and O = sum_c exp(L_c - LSE) O_c,
+// rounded to bf16 (the split-and-merge identity of a softmax).  Rows that one
+// cluster held whole were written directly and are skipped.  Block (t, y):
+// heads [8y, 8y + 8), one warp per head, 16 columns per lane.
+__global__ void __launch_bounds__(256) combine_kernel(Params p)
+{
+    const int t = blockIdx.x;
+    const int lane = threadIdx.x & 31;
+    const int64_t total = (int64_t)p.T * p.nbk;
+    auto cluster_of = [&](int64_t g) { return static_cast<int>(((g + 1) * p.ncl + total - 1) / total - 1); };
+    const int c_lo = cluster_of((int64_t)t * p.nbk), c_hi = cluster_of((int64_t)(t + 1) * p.nbk - 1);
+    const int h = 8 * blockIdx.y + (threadIdx.x >> 5);
+    if (c_lo == c_hi || h >= p.H)
+        return;
+    const int np = c_hi - c_lo + 1;
+    const int col = lane * 16;
+    auto slot_of = [&](int c) { return 2 * c + (t - static_cast<int>(share_start(p, c) / p.nbk)); };
+    // lane q holds the LSE of piece q0 + q of each group of 32
+    float lmax = -INFINITY;
+    for (int q0 = 0; q0 < np; q0 += 32) {
+        const int q = q0 + lane;
+        if (q < np)
+            lmax = fmaxf(lmax, p.ws_lse[(int64_t)slot_of(c_lo + q) * p.H + h]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+    float acc[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+        acc[e] = 0.f;
+    float wsum = 0.f;
+    if (lmax != -INFINITY) {
+        for (int q0 = 0; q0 < np; q0 += 32) {
+            const int q = q0 + lane;
+            const float wl = q < np ? expf(p.ws_lse[(int64_t)slot_of(c_lo + q) * p.H + h] - lmax) : 0.f;
+            const int nq = np - q0 < 32 ? np - q0 : 32;
+#pragma unroll 4
+            for (int e = 0; e < nq; ++e) {
+                const float wgt = __shfl_sync(0xffffffffu, wl, e);
+                wsum += wgt;
+                const float4 *src =
+                    reinterpret_cast<const float4 *>(p.ws_o + ((int64_t)slot_of(c_lo + q0 + e) * p.H + h) * kDv + col);
+                const float4 x0 = src[0], x1 = src[1], x2 = src[2], x3 = src[3];
+                const float xs[16] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
+                                      x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
+#pragma unroll
+                for (int c = 0; c < 16; ++c)
+                    acc[c] += wgt * xs[c];
+            }
+        }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    uint32_t o[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        o[e] = pack_bf16x2(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+    uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((int64_t)t * p.H + h) * kDv + col);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    if (lane == 0)
+        p.lse[(int64_t)t * p.H + h] = lmax == -INFINITY ? -INFINITY : lmax + logf(wsum);
+}
+
+// Clusters and split decision of a launch.  Decode cuts rows into pieces only
+// when at most two thirds of the clusters would otherwise have a row: a piece
+// costs its own Q load, pipeline fill and fp32 partial store plus the merge,
+// which measured a loss at 64 rows on 76 clusters, break-even at 48 and a gain
+// below (1.3x at 32 rows, 1.7x at 8).  Prefill never splits.
+struct Plan {
+    int clusters, split, nbk;
+};
+
+Plan plan(bool paged, int T, int k)
+{
+    Plan pl;
+    pl.nbk = (k + kBN - 1) / kBN;
+    int clusters = num_sms() / 2;
+    if (clusters < 1)
+        clusters = 1;
+    pl.split = 0;
+    if (paged) {
+        const int64_t tot = (int64_t)T * pl.nbk;
+        const int ncl = tot < clusters ? static_cast<int>(tot) : clusters;
+        if (3 * (int64_t)T <= 2 * (int64_t)ncl) {
+            pl.split = 1;
+            pl.clusters = ncl;
+            return pl;
+        }
+    }
+    pl.clusters = T < clusters ? (T > 0 ? T : 1) : clusters;
+    return pl;
 }
 
 template <bool PAGED>
@@ -844,17 +1162,35 @@ int launch(const MlaArgs &a, cudaStream_t stream, char *err, size_t errlen)
         snprintf(err, errlen, "device status word unavailable");
         return DSA_ERR_CUDA;
     }
-    // persistent: one cluster per pair of SMs, each walking tokens c, c + C, ...
-    int clusters = num_sms() / 2;
-    if (clusters > a.T)
-        clusters = a.T;
-    if (clusters < 1)
-        clusters = 1;
-    sparse_mla_kernel<PAGED><<<dim3(2 * clusters), kThreads, kSmem, stream>>>(tq, p);
+    // persistent: one cluster per pair of SMs, each walking its work units
+    const Plan pl = plan(PAGED, a.T, a.k);
+    p.split = pl.split;
+    p.nbk = pl.nbk;
+    p.ncl = pl.clusters;
+    p.ws_o = nullptr;
+    p.ws_lse = nullptr;
+    if (pl.split) {
+        const size_t o_bytes = (size_t)2 * pl.clusters * a.H * kDv * sizeof(float);
+        if (!a.workspace || a.workspace_bytes < o_bytes + (size_t)2 * pl.clusters * a.H * sizeof(float)) {
+            snprintf(err, errlen, "workspace too small for the split decode");
+            return DSA_ERR_WORKSPACE;
+        }
+        p.ws_o = static_cast<float *>(a.workspace);
+        p.ws_lse = reinterpret_cast<float *>(static_cast<char *>(a.workspace) + o_bytes);
+    }
+    sparse_mla_kernel<PAGED><<<dim3(2 * pl.clusters), kThreads, kSmem, stream>>>(tq, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(err, errlen, "sparse_mla launch: %s", cudaGetErrorString(e));
         return DSA_ERR_CUDA;
+    }
+    if (pl.split) {
+        combine_kernel<<<dim3(a.T, (a.H + 7) / 8), 256, 0, stream>>>(p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) {
+            snprintf(err, errlen, "sparse_mla combine launch: %s", cudaGetErrorString(e));
+            return DSA_ERR_CUDA;
+        }
     }
     return DSA_OK;
 }
@@ -871,6 +1207,11 @@ int launch_mla_decode(const MlaArgs &a, cudaStream_t stream, char *err, size_t e
     return launch<true>(a, stream, err, errlen);
 }
 
-size_t mla_decode_workspace_bytes(int, int, int) { return 0; }
+// Split decode: [2 * clusters, H, 512] fp32 partial outputs, then [2 * clusters, H] fp32 LSEs.
+size_t mla_decode_workspace_bytes(int B, int H, int k)
+{
+    const Plan pl = plan(true, B, k);
+    return pl.split ? (size_t)2 * pl.clusters * H * (kDv + 1) * sizeof(float) : 0;
+}
 
 } // namespace dsa

@@ -14,22 +14,24 @@
 // a block-wide prefix count gives each kept index its output slot directly,
 // so the output comes out sorted without a sort.
 //
-// Fast path (every row it can take; the passes above are its fallback).  Four
-// passes over a long row cost more than they need to: (1) rows longer than
-// kCand draw kSamples keys at a fixed stride, and a radix select over those
-// samples gives the key at sample rank ~ (1.5 k + 512) / n from the top, the
-// threshold (shorter rows use none); (2) one streaming pass keeps every key at
-// or above it: warp w scans its own contiguous segment of the row and appends
-// (key, index) to its own region of shared memory with warp-level prefix
-// counts, so the regions taken in warp order list the candidates in index
-// order; (3) the exact radix select runs on those few thousand candidates;
-// (4) one block-wide prefix count over the ordered candidates writes the kept
-// indices in ascending order, as the compaction above does.  A row whose
-// candidates miss [k, capacity] (tie-heavy or adversarial rows) takes the four
-// passes instead; either way the output is the same.  The fast path runs only
-// when the grid is at most one resident wave (decode batches): with many rows
-// in flight the four-pass kernel, whose footprint is 16 KB of shared memory
-// rather than 80 KB, keeps more rows per SM and finishes the batch sooner.
+// Candidate path (batches of at most two rows per SM, i.e. decode; the passes
+// above are its fallback and the whole path for prefill-sized batches).  Each
+// row runs on a cluster of cs CTAs (cs = 1, 2, 4 or 8, as many as the SMs
+// allow): (1) rows longer than kGather draw kSamples keys at a fixed stride,
+// and a radix select over those samples gives a key near sample rank
+// (1.5 k + 512) / n from the top, the threshold (every CTA of the cluster
+// draws the same samples and gets the same value; shorter rows use none);
+// (2) CTA c streams its own 1/cs of the row once, kUnroll 16-byte loads per
+// lane in flight, and keeps every key at or above the threshold: warp w scans
+// a contiguous segment and appends (key, index) to its own region of shared
+// memory with ballot prefix counts, so the regions taken in warp order list
+// the CTA's candidates in index order; (3) each CTA pushes its candidates,
+// in order, into CTA 0's list through distributed shared memory; (4) CTA 0
+// runs the exact radix select on those few thousand candidates and one
+// block-wide prefix count over the ordered list writes the kept indices in
+// ascending order, as the compaction above does.  A row whose candidates miss
+// [k, kGather] (tie-heavy or adversarial rows) takes the four passes in CTA 0
+// instead; either way the output is the same.
 #include "common.cuh"
 #include "launch.h"
 
@@ -41,9 +43,12 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kSeg = 512;               // candidates one warp's segment may keep
-constexpr int kCand = kWarps * kSeg;    // 8192
+constexpr int kCand = kWarps * kSeg;    // 8192: a CTA's own candidates
+constexpr int kGather = 8192;           // a cluster's candidates, gathered in CTA 0
 constexpr int kSamples = 4 * kThreads;  // 2048 threshold samples
-constexpr int kSmemTopk = (2 * kCand + 4096) * 4; // candidate keys, indices, histogram
+constexpr int kUnroll = 8;              // 16-byte loads per lane in flight in the filter
+// candidate keys and indices (own, then gathered), histogram
+constexpr int kSmemTopk = (2 * kCand + 2 * kGather + 4096) * 4;
 
 __device__ __forceinline__ uint32_t order_key(float x)
 {
@@ -109,27 +114,56 @@ __device__ __forceinline__ void for_each_key(const float *row, int n, F &&f)
     }
 }
 
-// Given a histogram of `nbins` bins, finds the bin b holding the k_rem-th
-// largest element: count(bins > b) < k_rem <= count(bins >= b).  Writes b and
-// count(bins > b) to out[0], out[1].
+// Given a histogram of `nbins` bins (a power of two, 16-byte aligned), finds
+// the bin b holding the k_rem-th largest element: count(bins > b) < k_rem <=
+// count(bins >= b).  Writes b and count(bins > b) to out[0], out[1].  Thread t
+// owns the contiguous bins [nbins - (t + 1) per, nbins - t per), read with
+// 16-byte loads when per >= 4 so the warp's reads do not collide on banks.
 __device__ __forceinline__ void select_bin(const int *hist, int nbins, int k_rem, int *scratch, int *out)
 {
     const int per = nbins / kThreads > 0 ? nbins / kThreads : 1;
     const int hi = nbins - threadIdx.x * per; // this thread owns bins [hi - per, hi), highest first
+    int c[8];                                 // c[j]: count of bin hi - 1 - j
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        c[j] = 0;
+    if (hi > 0) {
+        if (per >= 4) {
+            const int4 b = *reinterpret_cast<const int4 *>(hist + hi - 4);
+            c[0] = b.w;
+            c[1] = b.z;
+            c[2] = b.y;
+            c[3] = b.x;
+            if (per == 8) {
+                const int4 a = *reinterpret_cast<const int4 *>(hist + hi - 8);
+                c[4] = a.w;
+                c[5] = a.z;
+                c[6] = a.y;
+                c[7] = a.x;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                if (j < per)
+                    c[j] = hist[hi - 1 - j];
+        }
+    }
     int sum = 0;
-    if (hi > 0)
-        for (int b = hi - 1; b >= hi - per && b >= 0; --b)
-            sum += hist[b];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        sum += c[j];
     int total;
     int above = block_exclusive_scan(sum, scratch, &total);
     if (hi > 0) {
-        for (int b = hi - 1; b >= hi - per && b >= 0; --b) {
-            const int c = hist[b];
-            if (above < k_rem && above + c >= k_rem) {
-                out[0] = b;
-                out[1] = above;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j < per) {
+                if (above < k_rem && above + c[j] >= k_rem) {
+                    out[0] = hi - 1 - j;
+                    out[1] = above;
+                }
+                above += c[j];
             }
-            above += c;
         }
     }
     __syncthreads();
@@ -237,125 +271,120 @@ __device__ void topk_row(const float *row, int n, int k, int32_t *out, int *hist
             break; // block-uniform: every kept index has been written
     }
 }
+// Threshold of the candidate path: the 24-bit prefix (low 8 bits cleared) of
+// the key at rank ~ (1.5 k + 512) / n among kSamples keys drawn at a fixed
+// stride, so every sample at or above that rank passes it.  Deterministic: a
+// function of the row alone.
+__device__ uint32_t sample_threshold(const float *row, int n, int k, int *hist, int *scratch, int *sel)
+{
+    constexpr int kPer = kSamples / kThreads;
+    uint32_t sk[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e)
+        sk[e] = order_key(__ldg(row + (int64_t)(threadIdx.x + e * kThreads) * n / kSamples));
+    int r = (int)((int64_t)(3 * k / 2 + 512) * kSamples / n);
+    r = r < 1 ? 1 : (r > kSamples ? kSamples : r);
+    for (int b = threadIdx.x; b < 4096; b += kThreads)
+        hist[b] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < kPer; ++e)
+        atomicAdd(&hist[sk[e] >> 20], 1);
+    __syncthreads();
+    select_bin(hist, 4096, r, scratch, sel);
+    const uint32_t d0 = sel[0];
+    r -= sel[1];
+    __syncthreads();
+    for (int b = threadIdx.x; b < 4096; b += kThreads)
+        hist[b] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < kPer; ++e)
+        if ((sk[e] >> 20) == d0)
+            atomicAdd(&hist[(sk[e] >> 8) & 0xFFFu], 1);
+    __syncthreads();
+    select_bin(hist, 4096, r, scratch, sel);
+    const uint32_t thr = ((d0 << 12) | static_cast<uint32_t>(sel[0])) << 8;
+    __syncthreads();
+    return thr;
+}
 
-// Fast path for one row with k < n; returns false (writing nothing) when the
-// row must take the four passes.  wc: kWarps + 1 ints of shared memory.
-template <bool kVec>
-__device__ bool topk_row_fast(const float *row, int n, int k, int32_t *out, uint32_t *ckey, int32_t *cidx,
-                              int *hist, int *scratch, int *sel, int *wc)
+// Keeps the keys >= thr of row[c0, c1) in index order.  The first `head`
+// keys (row + c0 + head is 16-byte aligned) go through warp 0 one per lane;
+// then warp w scans its own contiguous segment of the rest, kUnroll 16-byte
+// loads per lane in flight.  Keys are appended with (key, index) to the warp's
+// region ck/ci[w * kSeg, +kSeg) with ballot prefix counts.  Leaves in wc[w]
+// the offset of warp w's region in the CTA's flat candidate list and in
+// wc[kWarps] the CTA's count, or -1 if a region overflowed.
+__device__ void filter_segment(const float *row, int c0, int c1, int head, uint32_t thr, uint32_t *ck, int32_t *ci,
+                               int *wc)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // 1. threshold: the r-th largest of kSamples keys drawn at a fixed stride
-    uint32_t thr = 0u;
-    if (n > kCand) {
-        uint32_t sk[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            sk[e] = order_key(__ldg(row + (int64_t)(threadIdx.x + e * kThreads) * n / kSamples));
-        int r = (int)((int64_t)(3 * k / 2 + 512) * kSamples / n);
-        r = r < 1 ? 1 : (r > kSamples ? kSamples : r);
-        for (int b = threadIdx.x; b < 4096; b += kThreads)
-            hist[b] = 0;
-        __syncthreads();
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            atomicAdd(&hist[sk[e] >> 20], 1);
-        __syncthreads();
-        select_bin(hist, 4096, r, scratch, sel);
-        const uint32_t d0 = sel[0];
-        r -= sel[1];
-        __syncthreads();
-        for (int b = threadIdx.x; b < 4096; b += kThreads)
-            hist[b] = 0;
-        __syncthreads();
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            if ((sk[e] >> 20) == d0)
-                atomicAdd(&hist[(sk[e] >> 8) & 0xFFFu], 1);
-        __syncthreads();
-        select_bin(hist, 4096, r, scratch, sel);
-        const uint32_t p1 = (d0 << 12) | static_cast<uint32_t>(sel[0]);
-        r -= sel[1];
-        __syncthreads();
-        for (int b = threadIdx.x; b < 256; b += kThreads)
-            hist[b] = 0;
-        __syncthreads();
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            if ((sk[e] >> 8) == p1)
-                atomicAdd(&hist[sk[e] & 0xFFu], 1);
-        __syncthreads();
-        select_bin(hist, 256, r, scratch, sel);
-        thr = (p1 << 8) | static_cast<uint32_t>(sel[0]);
-        __syncthreads();
-    }
-    // 2. warp w keeps the keys >= thr of its segment [s0, s1), in order
-    const int seg = (((n + kWarps - 1) / kWarps) + 3) & ~3;
-    const int s0 = warp * seg;
-    const int s1 = s0 + seg < n ? s0 + seg : n;
-    uint32_t *wk = ckey + warp * kSeg;
-    int32_t *wi = cidx + warp * kSeg;
+    const uint32_t lt = (1u << lane) - 1u;
+    const int v0 = c0 + head;
+    const int seg = (((c1 - v0 + kWarps - 1) / kWarps) + 3) & ~3;
+    const int s0 = v0 + warp * seg < c1 ? v0 + warp * seg : c1;
+    const int s1 = s0 + seg < c1 ? s0 + seg : c1;
+    uint32_t *wk = ck + warp * kSeg;
+    int32_t *wi = ci + warp * kSeg;
     int cnt = 0; // warp-uniform
-    if (kVec) {
-        for (int base = s0; base < s1; base += 128) {
-            const int i = base + 4 * lane;
-            uint32_t kk[4];
-            bool f[4];
+    if (warp == 0 && head > 0) {
+        const int i = c0 + lane;
+        const uint32_t key = lane < head ? order_key(__ldg(row + i)) : 0u;
+        const bool f = lane < head && key >= thr;
+        const unsigned m = __ballot_sync(0xffffffffu, f);
+        if (f) {
+            wk[__popc(m & lt)] = key;
+            wi[__popc(m & lt)] = i;
+        }
+        cnt = __popc(m);
+    }
+    for (int base = s0; base < s1; base += 128 * kUnroll) {
+        uint32_t kk[kUnroll][4];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int i = base + 128 * u + 4 * lane;
             if (i + 3 < s1) {
                 const float4 v = __ldg(reinterpret_cast<const float4 *>(row + i));
-                kk[0] = order_key(v.x);
-                kk[1] = order_key(v.y);
-                kk[2] = order_key(v.z);
-                kk[3] = order_key(v.w);
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    f[e] = kk[e] >= thr;
+                kk[u][0] = order_key(v.x);
+                kk[u][1] = order_key(v.y);
+                kk[u][2] = order_key(v.z);
+                kk[u][3] = order_key(v.w);
             } else {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    kk[e] = i + e < s1 ? order_key(__ldg(row + i + e)) : 0u;
-                    f[e] = i + e < s1 && kk[e] >= thr;
-                }
+                for (int e = 0; e < 4; ++e)
+                    kk[u][e] = i + e < s1 ? order_key(__ldg(row + i + e)) : 0u;
             }
-            const int c = (int)f[0] + (int)f[1] + (int)f[2] + (int)f[3];
-            int x = c;
+        }
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o)
-                    x += y;
+        for (int u = 0; u < kUnroll; ++u) {
+            const int i = base + 128 * u + 4 * lane;
+            bool f[4];
+            int pre = 0, tot = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                f[e] = i + e < s1 && kk[u][e] >= thr;
+                const unsigned m = __ballot_sync(0xffffffffu, f[e]);
+                pre += __popc(m & lt);
+                tot += __popc(m);
             }
-            int slot = cnt + x - c;
+            int slot = cnt + pre; // keys of lower lanes come first, then this lane's in order
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 if (f[e]) {
                     if (slot < kSeg) {
-                        wk[slot] = kk[e];
+                        wk[slot] = kk[u][e];
                         wi[slot] = i + e;
                     }
                     ++slot;
                 }
             }
-            cnt += __shfl_sync(0xffffffffu, x, 31);
-        }
-    } else {
-        for (int base = s0; base < s1; base += 32) {
-            const int i = base + lane;
-            const uint32_t key = i < s1 ? order_key(__ldg(row + i)) : 0u;
-            const bool f = i < s1 && key >= thr;
-            const unsigned m = __ballot_sync(0xffffffffu, f);
-            const int slot = cnt + __popc(m & ((1u << lane) - 1u));
-            if (f && slot < kSeg) {
-                wk[slot] = key;
-                wi[slot] = i;
-            }
-            cnt += __popc(m);
+            cnt += tot;
         }
     }
     if (lane == 0)
         wc[warp] = cnt;
     __syncthreads();
-    // candidate count, overflow, and the exclusive prefix of the regions (in place)
     if (threadIdx.x == 0) {
         int tot = 0, over = 0;
         for (int w = 0; w < kWarps; ++w) {
@@ -367,23 +396,30 @@ __device__ bool topk_row_fast(const float *row, int n, int k, int32_t *out, uint
         wc[kWarps] = over ? -1 : tot;
     }
     __syncthreads();
-    const int nc = wc[kWarps];
-    if (nc < k) // overflow (-1) or too few
-        return false;
-    // flat candidate f lives in region w (wc[w] <= f < wc[w + 1]) at offset f - wc[w]
-    auto at = [&](int f) -> int {
-        int w = 0;
+}
+
+// Slot of flat candidate f: region w (wc[w] <= f < wc[w + 1]) at offset f - wc[w].
+__device__ __forceinline__ int cand_slot(const int *wc, int f)
+{
+    int w = 0;
 #pragma unroll
-        for (int q = 1; q < kWarps; ++q)
-            w = wc[q] <= f ? q : w;
-        return w * kSeg + (f - wc[w]);
-    };
-    // 3. exact radix select among the candidates on (key - kmin): the range of
-    //    candidate keys spans at most 4096 bins per pass, so close scores spread
-    //    out instead of piling into a few bins of the raw top digit
+    for (int q = 1; q < kWarps; ++q)
+        w = wc[q] <= f ? q : w;
+    return w * kSeg + (f - wc[w]);
+}
+
+// Exact top-k of nc >= k candidates ck/ci listed in ascending index order;
+// writes the kept indices to out in that order.
+__device__ void select_candidates(const uint32_t *ck, const int32_t *ci, int nc, int k, int32_t *out, int *hist,
+                                  int *scratch, int *sel)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Radix select on d = key - kmin: the candidates span a narrow key range,
+    // so passes of at most 12 bits over d spread close scores over the bins
+    // instead of piling them into a few bins of the raw top digit.
     uint32_t lo = 0xFFFFFFFFu, hi = 0u;
     for (int f = threadIdx.x; f < nc; f += kThreads) {
-        const uint32_t key = ckey[at(f)];
+        const uint32_t key = ck[f];
         lo = key < lo ? key : lo;
         hi = key > hi ? key : hi;
     }
@@ -406,7 +442,7 @@ __device__ bool topk_row_fast(const float *row, int n, int k, int32_t *out, uint
     }
     __syncthreads();
     const uint32_t range = kmax - kmin;
-    const int bits = range == 0u ? 0 : 32 - __clz(range); // d = key - kmin has `bits` significant bits
+    const int bits = range == 0u ? 0 : 32 - __clz(range); // d has `bits` significant bits
     int shift = bits > 12 ? bits - 12 : 0;  // this pass sorts d into bins of d >> shift ...
     int nbins = 1 << (bits - shift);        // ... of which there are nbins (at most 4096)
     int prev = 32;                          // bits of d at and above `prev` are fixed to `prefix`
@@ -417,7 +453,7 @@ __device__ bool topk_row_fast(const float *row, int n, int k, int32_t *out, uint
             hist[q] = 0;
         __syncthreads();
         for (int f = threadIdx.x; f < nc; f += kThreads) {
-            const uint32_t d = ckey[at(f)] - kmin;
+            const uint32_t d = ck[f] - kmin;
             if (prev == 32 || (d >> prev) == prefix)
                 atomicAdd(&hist[(d >> shift) & static_cast<uint32_t>(nbins - 1)], 1);
         }
@@ -435,14 +471,13 @@ __device__ bool topk_row_fast(const float *row, int n, int k, int32_t *out, uint
     }
     const uint32_t tau = kmin + prefix; // every bit of d fixed: the k-th largest candidate key
     const int need_eq = k_rem;          // keys equal to tau to keep (the smallest indices)
-    __syncthreads();
-    // 4. ordered output: thread t walks flat candidates [t*per, t*per + per)
+    // ordered output: thread t walks candidates [t * per, t * per + per)
     const int per = (nc + kThreads - 1) / kThreads;
-    const int f0 = threadIdx.x * per;
+    const int f0 = threadIdx.x * per < nc ? threadIdx.x * per : nc;
     const int f1 = f0 + per < nc ? f0 + per : nc;
     int gt = 0, eq = 0;
     for (int f = f0; f < f1; ++f) {
-        const uint32_t key = ckey[at(f)];
+        const uint32_t key = ck[f];
         gt += key > tau;
         eq += key == tau;
     }
@@ -450,25 +485,23 @@ __device__ bool topk_row_fast(const float *row, int n, int k, int32_t *out, uint
     const int pre = block_exclusive_scan((gt << 16) | eq, scratch, &total);
     int g_before = pre >> 16, e_before = pre & 0xFFFF;
     for (int f = f0; f < f1; ++f) {
-        const int a = at(f);
-        const uint32_t key = ckey[a];
+        const uint32_t key = ck[f];
         if (key > tau) {
-            out[g_before + (e_before < need_eq ? e_before : need_eq)] = cidx[a];
+            out[g_before + (e_before < need_eq ? e_before : need_eq)] = ci[f];
             ++g_before;
         } else if (key == tau) {
             if (e_before < need_eq)
-                out[g_before + e_before] = cidx[a];
+                out[g_before + e_before] = ci[f];
             ++e_before;
         }
     }
-    return true;
 }
 
 __global__ void __launch_bounds__(kThreads, 2)
     topk_kernel(const float *__restrict__ logits, int64_t ld, int T, const int32_t *__restrict__ valid_len, int k,
                 int32_t *__restrict__ idx, unsigned *status)
 {
-    __shared__ int hist[4096];
+    __shared__ __align__(16) int hist[4096];
     __shared__ int scratch[kWarps + 1];
     __shared__ int sel[2];
     for (int row = blockIdx.x; row < T; row += gridDim.x) {
@@ -495,39 +528,81 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
-    topk_fast_kernel(const float *__restrict__ logits, int64_t ld, int T, const int32_t *__restrict__ valid_len, int k,
-                int32_t *__restrict__ idx, unsigned *status)
+// Candidate path: one cluster of cs CTAs per row (cs from the launch).
+__global__ void __launch_bounds__(kThreads, 1)
+    topk_cluster_kernel(const float *__restrict__ logits, int64_t ld, int T, const int32_t *__restrict__ valid_len,
+                        int k, int32_t *__restrict__ idx, unsigned *status)
 {
     extern __shared__ __align__(16) uint32_t dsm[];
-    uint32_t *ckey = dsm;
-    int32_t *cidx = reinterpret_cast<int32_t *>(dsm + kCand);
-    int *hist = reinterpret_cast<int *>(dsm + 2 * kCand);
+    uint32_t *lkey = dsm;
+    int32_t *lidx = reinterpret_cast<int32_t *>(dsm + kCand);
+    uint32_t *gkey = dsm + 2 * kCand;
+    int32_t *gidx = reinterpret_cast<int32_t *>(dsm + 2 * kCand + kGather);
+    int *hist = reinterpret_cast<int *>(dsm + 2 * kCand + 2 * kGather);
     __shared__ int scratch[kWarps + 1];
     __shared__ int sel[2];
     __shared__ int wc[kWarps + 1];
-    for (int row = blockIdx.x; row < T; row += gridDim.x) {
+    __shared__ int cinfo[2]; // this CTA's offset in CTA 0's list; the cluster's count, or -1
+    const int cs = static_cast<int>(cluster_nctarank());
+    const int cr = static_cast<int>(cluster_ctarank());
+    const int ncl = gridDim.x / cs;
+    const uint32_t gk0 = mapa_shared(smem_u32(gkey), 0), gi0 = mapa_shared(smem_u32(gidx), 0);
+    const uint32_t cnt_local = smem_u32(&wc[kWarps]);
+    for (int row = blockIdx.x / cs; row < T; row += ncl) { // the same rows in every CTA of the cluster
         int n = valid_len[row];
         if (n < 0)
             n = 0;
         if (n > ld) {
-            if (threadIdx.x == 0)
+            if (cr == 0 && threadIdx.x == 0)
                 atomicOr(status, DSA_DEV_BAD_POSITION);
             n = static_cast<int>(ld);
         }
         int32_t *out = idx + static_cast<int64_t>(row) * k;
         if (n <= k) {
-            for (int j = threadIdx.x; j < k; j += kThreads)
-                out[j] = j < n ? j : -1;
+            if (cr == 0)
+                for (int j = threadIdx.x; j < k; j += kThreads)
+                    out[j] = j < n ? j : -1;
             continue;
         }
         const float *r = logits + static_cast<int64_t>(row) * ld;
         const bool vec = (reinterpret_cast<uintptr_t>(r) & 15u) == 0;
-        const bool done = vec ? topk_row_fast<true>(r, n, k, out, ckey, cidx, hist, scratch, sel, wc)
-                              : topk_row_fast<false>(r, n, k, out, ckey, cidx, hist, scratch, sel, wc);
+        const uint32_t thr = n > kGather ? sample_threshold(r, n, k, hist, scratch, sel) : 0u;
+        // keys before the row's first 16-byte boundary, then chunks of a multiple
+        // of 4 keys from there (fp32 rows are 4-byte aligned)
+        int h = static_cast<int>((4u - ((reinterpret_cast<uintptr_t>(r) >> 2) & 3u)) & 3u);
+        h = h < n ? h : n;
+        const int chunk = ((n - h + cs - 1) / cs + 3) & ~3;
+        const int c0 = cr == 0 ? 0 : (h + cr * chunk < n ? h + cr * chunk : n);
+        const int c1 = h + (cr + 1) * chunk < n ? h + (cr + 1) * chunk : n;
+        filter_segment(r, c0, c1, cr == 0 ? h : 0, thr, lkey, lidx, wc);
+        cluster_sync_all(); // every CTA's count is in its wc[kWarps]
+        if (threadIdx.x == 0) {
+            int off = 0, tot = 0;
+            bool bad = false;
+            for (int q = 0; q < cs; ++q) {
+                const int c = static_cast<int>(ld_cluster_u32(mapa_shared(cnt_local, q)));
+                bad |= c < 0;
+                off += q < cr ? c : 0;
+                tot += c;
+            }
+            cinfo[0] = off;
+            cinfo[1] = (bad || tot < k || tot > kGather) ? -1 : tot;
+        }
         __syncthreads();
-        if (!done) {
-            if (vec)
+        const int nc = cinfo[1];
+        if (nc >= 0) {
+            const int off = cinfo[0], mine = wc[kWarps];
+            for (int f = threadIdx.x; f < mine; f += kThreads) {
+                const int a = cand_slot(wc, f);
+                st_cluster_u32(gk0 + 4u * (off + f), lkey[a]);
+                st_cluster_u32(gi0 + 4u * (off + f), static_cast<uint32_t>(lidx[a]));
+            }
+        }
+        cluster_sync_all(); // CTA 0's list is complete; nothing of a peer is touched after this
+        if (cr == 0) {
+            if (nc >= 0)
+                select_candidates(gkey, gidx, nc, k, out, hist, scratch, sel);
+            else if (vec)
                 topk_row<true>(r, n, k, out, hist, scratch, sel);
             else
                 topk_row<false>(r, n, k, out, hist, scratch, sel);
@@ -545,30 +620,45 @@ int launch_topk(const TopkArgs &a, cudaStream_t stream, char *err, size_t errlen
         snprintf(err, errlen, "device status word unavailable");
         return DSA_ERR_CUDA;
     }
-    // Few rows (decode, one resident wave at most): each row's latency is the
-    // cost, so the candidate fast path takes them.  Many rows (prefill): the
-    // four-pass kernel's small footprint keeps more rows in flight per SM and
-    // wins on throughput.
-    if (a.T <= 2 * num_sms()) {
+    const int sms = num_sms();
+    cudaError_t e;
+    if (a.T <= 2 * sms) {
+        // Few rows (decode): each row's latency is the cost, so a row gets as
+        // many CTAs as the SMs allow and is read once.  Many rows (prefill): the
+        // four-pass kernel's 16 KB footprint keeps two rows in flight per SM.
         static bool attr_set[64] = {};
         int dev = 0;
         cudaGetDevice(&dev);
         if (dev < 64 && !attr_set[dev]) {
-            cudaError_t e = cudaFuncSetAttribute(topk_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 kSmemTopk);
+            e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTopk);
             if (e != cudaSuccess) {
                 snprintf(err, errlen, "cudaFuncSetAttribute(topk): %s", cudaGetErrorString(e));
                 return DSA_ERR_CUDA;
             }
             attr_set[dev] = true;
         }
-        topk_fast_kernel<<<a.T, kThreads, kSmemTopk, stream>>>(a.logits, a.ld, a.T, a.valid_len, a.k, a.idx,
-                                                                status);
+        int cs = 1;
+        while (cs < 8 && a.T * cs * 2 <= sms)
+            cs *= 2;
+        const int clusters = a.T < sms / cs ? a.T : sms / cs;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(clusters * cs));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmemTopk;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, a.logits, a.ld, a.T, a.valid_len, a.k, a.idx, status);
     } else {
         const int grid = a.T < 65535 * 4 ? a.T : 65535 * 4;
         topk_kernel<<<grid, kThreads, 0, stream>>>(a.logits, a.ld, a.T, a.valid_len, a.k, a.idx, status);
+        e = cudaGetLastError();
     }
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(err, errlen, "topk launch: %s", cudaGetErrorString(e));
         return DSA_ERR_CUDA;

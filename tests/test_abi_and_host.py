@@ -35,7 +35,13 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_version_and_workspace_query(lib):
     assert lib.dsa_version() >= 100
-    assert lib.dsa_sparse_mla_decode_workspace_size(64, 128, 2048) == 0
+    # at most two thirds as many rows as SM pairs: rows are split, 2 slots per
+    # cluster of H x (512 + 1) fp32
+    n = lib.dsa_sparse_mla_decode_workspace_size(32, 128, 2048)
+    assert n > 0 and n % (2 * 128 * 513 * 4) == 0
+    assert lib.dsa_sparse_mla_decode_workspace_size(32, 16, 2048) == n // 8
+    assert lib.dsa_sparse_mla_decode_workspace_size(1024, 128, 2048) == 0  # whole rows: none
+    assert lib.dsa_sparse_mla_decode_workspace_size(1, 128, 64) == 0       # one block: nothing to split
     assert lib.dsa_sparse_mla_decode_workspace_size(64, 129, 2048) == 0  # unsupported H: 0
 
 

@@ -200,3 +200,35 @@ def test_decode_paged_pipeline():
     o_ref, l_ref = oracle.sparse_mla_paged(bits16(d["q"]), bits16(d["kv_pool"]), h["block_table"].numpy(),
                                            h["ctx"].numpy(), ref_idx, cfg.sm_scale)
     check_attention(out.cpu().double().numpy(), lse.cpu().double().numpy(), o_ref, l_ref)
+
+
+@pytest.mark.parametrize("B,k", [(1, 2048), (3, 100), (5, 64), (17, 2048), (64, 2048), (75, 256), (100, 300)])
+def test_decode_split_pieces(B, k):
+    """Decode batches with fewer rows than SM pairs cut each row into pieces over
+    the clusters (partial output and LSE per piece in the workspace, then a merge
+    by LSE); larger batches keep whole rows.  Selections are unsorted and hold
+    -1 and out-of-context entries; some contexts are shorter than k, so whole
+    pieces see nothing valid."""
+    cfg = W.CONFIGS["decode_paged"]
+    dsa = lib()
+    g = np.random.default_rng(1000 * B + k)
+    ctx = g.integers(1, 3 * k, size=B)
+    ctx[0] = 1
+    d = W.decode_inputs(cfg, DEV, ctx=ctx.tolist(), seed=B + k)
+    idx_np = np.full((B, k), -1, np.int32)
+    for b in range(B):
+        c = int(ctx[b])
+        m = min(k, c + 2)
+        idx_np[b, :m] = g.choice(np.arange(-1, c + 1), size=m, replace=False)
+    idx = torch.from_numpy(idx_np).to(DEV)
+    out = torch.empty((B, cfg.H, 512), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((B, cfg.H), dtype=torch.float32, device=DEV)
+    ws_n = dsa.dsa_sparse_mla_decode_workspace_size(B, cfg.H, k)
+    ws = torch.full((max(ws_n, 1),), 0xFF, dtype=torch.uint8, device=DEV)  # NaN-filled: stale data shows
+    dsa.dsa_sparse_mla_decode_paged(d["q"], d["kv_pool"], d["block_table"], d["ctx"], idx, cfg.sm_scale,
+                                    out, lse, workspace=ws)
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_device_status() == 0
+    o_ref, l_ref = oracle.sparse_mla_paged(bits16(d["q"]), bits16(d["kv_pool"]), d["block_table"].cpu().numpy(),
+                                           ctx.astype(np.int32), idx_np, cfg.sm_scale)
+    check_attention(out.cpu().double().numpy(), lse.cpu().double().numpy(), o_ref, l_ref)

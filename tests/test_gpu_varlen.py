@@ -4,7 +4,9 @@ multi-token decode (the last few positions of each sequence), all rows sharing o
 permuted page pool.  Each query row carries its own position, context length and
 block-table row.  Checked against the oracle (indexer rows, top-k on every row
 from the GPU's logits, attention rows) and against the contiguous entry point on
-the same latent rows concatenated per sequence (bit-identical output)."""
+the same latent rows concatenated per sequence: bit-identical output when the
+decode keeps whole rows (at least as many rows as SM pairs), equal up to fp32
+summation order when it cuts fewer rows into pieces over the SMs."""
 import dataclasses
 
 import numpy as np
@@ -64,8 +66,13 @@ def check_contiguous_equivalence(dsa, v, idx, out, lse, sm_scale):
     dsa.dsa_sparse_mla_prefill(v["q"], v["kv_concat"], gidx, sm_scale, out2, lse2)
     torch.cuda.synchronize()
     assert S == int(v["seq_lens"].sum())
-    assert torch.equal(out2.view(torch.int16), out.view(torch.int16))
-    assert torch.equal(lse2, lse)
+    T, H = lse.shape
+    if dsa.dsa_sparse_mla_decode_workspace_size(T, H, idx.shape[1]) == 0:  # whole rows: same kernel path
+        assert torch.equal(out2.view(torch.int16), out.view(torch.int16))
+        assert torch.equal(lse2, lse)
+    else:  # rows merged from pieces: fp32 rounding, then one bf16 rounding of O
+        assert (out2.float() - out.float()).abs().max().item() <= 2e-3
+        assert (lse2 - lse).abs().max().item() <= 1e-4
 
 
 def boundary_rows(v, extra=()):
