@@ -223,6 +223,35 @@ int dsa_sparse_mla_decode_paged(const void *q, const void *kv_pool, int num_page
                                 void *out, float *lse, void *workspace, size_t workspace_bytes,
                                 dsa_stream_t stream);
 
+/*
+ * dsa_sparse_mla_decode_paged_noalloc: dsa_sparse_mla_decode_paged without a
+ * caller-provided workspace.  The pages have no counterpart to this entry
+ * point: it is for callers that cannot allocate device memory while they
+ * run, such as a plugin inside a host program that owns every device
+ * allocation, or a service held to a fixed device-memory budget that must not
+ * grow or wait on an allocator mid-request.  It allocates nothing (no
+ * cudaMalloc, no cudaFree, no allocating library call): its workspace is a
+ * static device buffer of DSA_DECODE_STATIC_WS_BYTES (40 MiB) built into the
+ * library, which every GPU that loads libdsa.so holds until the process exits.
+ *
+ * Arguments, results and errors are those of dsa_sparse_mla_decode_paged.  A
+ * call whose workspace need (dsa_sparse_mla_decode_workspace_size) exceeds the
+ * buffer returns DSA_ERR_WORKSPACE with a message naming both sizes; with
+ * H <= 128 that takes a device of 160 SMs or more.  The first call on each
+ * device looks up the buffer's device address (cudaGetSymbolAddress, with
+ * that device current) and keeps it; make that first call before any stream
+ * capture.  All calls share the one buffer, which keeps the contents of the
+ * last call (nothing in it needs to start at zero: each call writes every
+ * part it reads), so calls whose kernels may overlap on the GPU (different
+ * streams, or different host threads, on one device) race on it and must be
+ * ordered by the caller.
+ */
+#define DSA_DECODE_STATIC_WS_BYTES (40u << 20)
+int dsa_sparse_mla_decode_paged_noalloc(const void *q, const void *kv_pool, int num_pages, int page_size,
+                                        const int32_t *block_table, int max_pages, const int32_t *ctx_len,
+                                        const int32_t *idx, int B, int H, int k, float sm_scale,
+                                        void *out, float *lse, dsa_stream_t stream);
+
 /* Bytes of workspace dsa_sparse_mla_decode_paged needs for (B, H, k) on the
  * current device: 0 when the rows stay whole (3 B > 2 clusters), else
  * 2 * clusters * H * 513 * 4, with clusters = min(SM pairs, B * ceil(k / 64)).

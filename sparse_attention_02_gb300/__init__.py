@@ -52,10 +52,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.dsa_topk.argtypes = [P, i64, i32, P, i32, P, P]
     lib.dsa_sparse_mla_prefill.argtypes = [P, P, i32, P, i32, i32, i32, f32, P, P, P]
     lib.dsa_sparse_mla_decode_paged.argtypes = [P, P, i32, i32, P, i32, P, P, i32, i32, i32, f32, P, P, P, sz, P]
+    lib.dsa_sparse_mla_decode_paged_noalloc.argtypes = [P, P, i32, i32, P, i32, P, P, i32, i32, i32, f32, P, P, P]
     lib.dsa_sparse_mla_decode_workspace_size.restype = sz
     lib.dsa_sparse_mla_decode_workspace_size.argtypes = [i32, i32, i32]
     for name in ("dsa_quantize_fp8", "dsa_indexer_logits", "dsa_topk", "dsa_sparse_mla_prefill", "dsa_sparse_mla_decode_paged",
-                 "dsa_get_device_status"):
+                 "dsa_sparse_mla_decode_paged_noalloc", "dsa_get_device_status"):
         getattr(lib, name).restype = i32
     if path is None:
         _lib = lib
@@ -224,6 +225,31 @@ def dsa_sparse_mla_decode_paged(q, kv_pool, block_table, ctx_len, idx, sm_scale:
                                                       block_table.shape[1], _ptr(ctx_len), _ptr(idx), B, H, k,
                                                       float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
                                                       ws_bytes, _stream(stream)))
+    return out, lse
+
+
+def dsa_sparse_mla_decode_paged_noalloc(q, kv_pool, block_table, ctx_len, idx, sm_scale: float, out, lse,
+                                        stream=None):
+    """dsa_sparse_mla_decode_paged for callers that cannot allocate device memory:
+    the library's static device buffer serves as the workspace, and this wrapper
+    allocates nothing either.  Same arguments, minus the workspace."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(kv_pool, torch.bfloat16, "kv_pool", 3)
+    _need(block_table, torch.int32, "block_table", 2)
+    _need(ctx_len, torch.int32, "ctx_len", 1)
+    _need(idx, torch.int32, "idx", 2)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(lse, torch.float32, "lse", 2)
+    B, H, D = q.shape
+    P, ps, D2 = kv_pool.shape
+    k = idx.shape[1]
+    if D != 576 or D2 != 576 or block_table.shape[0] != B or ctx_len.shape[0] != B or idx.shape[0] != B \
+            or tuple(out.shape) != (B, H, 512) or tuple(lse.shape) != (B, H):
+        raise ValueError("inconsistent shapes")
+    _check(load_library().dsa_sparse_mla_decode_paged_noalloc(_ptr(q), _ptr(kv_pool), P, ps, _ptr(block_table),
+                                                              block_table.shape[1], _ptr(ctx_len), _ptr(idx), B, H,
+                                                              k, float(sm_scale), _ptr(out), _ptr(lse),
+                                                              _stream(stream)))
     return out, lse
 
 

@@ -303,3 +303,57 @@ int dsa_sparse_mla_decode_paged(const void *q, const void *kv_pool, int num_page
 }
 
 } // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode attention.  The workspace lives in this file-scope
+// device array, which every device that loads the library holds until the
+// process exits.  In host code the array's name only stands for it: the
+// device address comes from cudaGetSymbolAddress, looked up once per device
+// (with that device current) on the first call and kept.
+namespace dsa {
+namespace {
+
+static __device__ __align__(256) unsigned char g_decode_static_ws[DSA_DECODE_STATIC_WS_BYTES];
+void *g_decode_static_ws_ptr[kMaxDevices] = {};
+
+// Device address of this device's static decode workspace, or null (message in *why).
+void *decode_static_workspace(cudaError_t *why)
+{
+    *why = cudaSuccess;
+    const int d = current_device();
+    if (d < 0 || d >= kMaxDevices)
+        return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_decode_static_ws_ptr[d]) {
+        void *p = nullptr;
+        *why = cudaGetSymbolAddress(&p, g_decode_static_ws);
+        if (*why != cudaSuccess || !p)
+            return nullptr;
+        g_decode_static_ws_ptr[d] = p;
+    }
+    return g_decode_static_ws_ptr[d];
+}
+
+} // namespace
+} // namespace dsa
+
+extern "C" int dsa_sparse_mla_decode_paged_noalloc(const void *q, const void *kv_pool, int num_pages, int page_size,
+                                                   const int32_t *block_table, int max_pages, const int32_t *ctx_len,
+                                                   const int32_t *idx, int B, int H, int k, float sm_scale, void *out,
+                                                   float *lse, dsa_stream_t stream)
+{
+    // 0 for bad arguments too: those are then reported by the call below
+    const size_t need = dsa_sparse_mla_decode_workspace_size(B, H, k);
+    if (need > (size_t)DSA_DECODE_STATIC_WS_BYTES)
+        return fail(DSA_ERR_WORKSPACE,
+                    "decode with B=%d, H=%d, k=%d needs %zu bytes of workspace on this device, more than the "
+                    "%zu-byte static buffer of the allocation-free entry point",
+                    B, H, k, need, (size_t)DSA_DECODE_STATIC_WS_BYTES);
+    cudaError_t why;
+    void *ws = decode_static_workspace(&why);
+    if (!ws)
+        return fail(DSA_ERR_CUDA, "address of the static decode workspace: %s",
+                    why == cudaSuccess ? "no current device" : cudaGetErrorString(why));
+    return dsa_sparse_mla_decode_paged(q, kv_pool, num_pages, page_size, block_table, max_pages, ctx_len, idx, B, H, k,
+                                       sm_scale, out, lse, ws, (size_t)DSA_DECODE_STATIC_WS_BYTES, stream);
+}
