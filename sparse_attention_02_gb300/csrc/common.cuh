@@ -36,6 +36,17 @@ __device__ __forceinline__ uint64_t global_timer_ns()
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31; }
 
+// ----------------------------------------------- programmatic dependent launch
+// Every kernel here is launched with programmatic dependent launch, so its
+// CTAs may be dispatched while the previous kernel on the stream is still
+// finishing.  A kernel touches no global memory (reads or writes) before
+// grid_dep_wait() returns, which happens once every earlier kernel of the
+// stream has completed and its writes are visible; setup that needs only
+// shared memory, TMEM or kernel parameters may run before it.
+// grid_dep_launch() lets the next kernel be dispatched early.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)

@@ -131,6 +131,8 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI, PAGED>::THREADS, 1)
     const int cg = PAGED ? blockIdx.x : (gridDim.x - 1 - blockIdx.x); // heavy groups first
     const int r0 = cg * C::R;
 
+    grid_dep_wait();
+    grid_dep_launch();
     // ---- setup: row positions, folded weights, tile range
     const int64_t key_limit = PAGED ? (int64_t)p.max_pages * p.page_size : (int64_t)p.S;
     const int64_t lim = (key_limit < p.ld ? key_limit : p.ld) - 1;
@@ -664,6 +666,8 @@ __global__ void __launch_bounds__(FlatCfg<HI, DI>::THREADS, 2)
         return qp < 0 ? -1 : static_cast<int>(qp);
     };
 
+    grid_dep_wait();
+    grid_dep_launch();
     // ---- tile prefix over the rows (warp 0; lane l sums rows [l * per, l * per + per))
     if (warp == 0) {
         const int per = (p.T + 31) / 32;
@@ -972,8 +976,8 @@ int launch_cfg(const IndexerArgs &a, cudaStream_t stream, char *err, size_t errl
                 flat_attr[dev] = true;
             }
             p.splits = 1;
-            indexer_paged_flat_kernel<HI, DI><<<2 * num_sms(), F::THREADS, F::SMEM, stream>>>(tq, tk, p);
-            cudaError_t e = cudaGetLastError();
+            cudaError_t e = launch_pdl(indexer_paged_flat_kernel<HI, DI>, dim3(2 * num_sms()), dim3(F::THREADS),
+                                       F::SMEM, stream, 1, tq, tk, p);
             if (e != cudaSuccess) {
                 snprintf(err, errlen, "indexer launch: %s", cudaGetErrorString(e));
                 return DSA_ERR_CUDA;
@@ -992,8 +996,7 @@ int launch_cfg(const IndexerArgs &a, cudaStream_t stream, char *err, size_t errl
     }
     p.splits = splits;
     dim3 grid(groups, splits);
-    indexer_kernel<HI, DI, PAGED><<<grid, C::THREADS, C::SMEM, stream>>>(tq, tk, p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(indexer_kernel<HI, DI, PAGED>, grid, dim3(C::THREADS), C::SMEM, stream, 1, tq, tk, p);
     if (e != cudaSuccess) {
         snprintf(err, errlen, "indexer launch: %s", cudaGetErrorString(e));
         return DSA_ERR_CUDA;

@@ -14,6 +14,35 @@ bool encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *bas
                     CUtensorMapSwizzle swizzle, char *err, size_t errlen);
 
 int num_sms();
+
+// Launches `kernel` on `stream` with programmatic dependent launch allowed
+// (the kernel must call grid_dep_wait() before touching global memory) and,
+// when cluster_x > 1, thread-block clusters of cluster_x CTAs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       unsigned cluster_x, Args &&...args)
+{
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
 unsigned *device_status_ptr(); // address of this device's status word, or null
 
 struct QuantizeArgs {

@@ -53,6 +53,8 @@ __global__ void __launch_bounds__(kQThreads)
 {
     constexpr int kRowsPerCta = kQThreads / GROUP;
     __shared__ float red[kQThreads / 32];
+    grid_dep_wait();
+    grid_dep_launch();
     const int g = threadIdx.x % GROUP;
     const int64_t stride = (int64_t)gridDim.x * kRowsPerCta;
     // GROUP == kQThreads: the whole CTA walks the same rows, so the loop and the
@@ -112,15 +114,15 @@ int launch_quantize(const QuantizeArgs &a, cudaStream_t stream, char *err, size_
         int64_t grid = (a.rows + kRows - 1) / kRows;
         if (grid > 64LL * sms)
             grid = 64LL * sms;
-        quantize_kernel<32><<<(unsigned)grid, kQThreads, 0, stream>>>(a.x, a.rows, a.cols, a.mode, a.codes, a.scale);
+        e = launch_pdl(quantize_kernel<32>, dim3((unsigned)grid), dim3(kQThreads), 0, stream, 1, a.x, a.rows, a.cols,
+                       a.mode, a.codes, a.scale);
     } else {
         int64_t grid = a.rows;
         if (grid > 64LL * sms)
             grid = 64LL * sms;
-        quantize_kernel<kQThreads><<<(unsigned)grid, kQThreads, 0, stream>>>(a.x, a.rows, a.cols, a.mode, a.codes,
-                                                                             a.scale);
+        e = launch_pdl(quantize_kernel<kQThreads>, dim3((unsigned)grid), dim3(kQThreads), 0, stream, 1, a.x, a.rows,
+                       a.cols, a.mode, a.codes, a.scale);
     }
-    e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(err, errlen, "quantize launch: %s", cudaGetErrorString(e));
         return DSA_ERR_CUDA;

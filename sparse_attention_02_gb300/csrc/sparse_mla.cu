@@ -316,6 +316,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_sync_all(); // both CTAs' barriers exist before any remote operation
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    grid_dep_wait(); // no global memory before this: the previous kernel may still be running
+    grid_dep_launch();
 
     if (warp < kProdWarps) {
         // ------------------------------------------------------ producers
@@ -1033,6 +1035,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // heads [8y, 8y + 8), one warp per head, 16 columns per lane.
 __global__ void __launch_bounds__(256) combine_kernel(Params p)
 {
+    grid_dep_wait();
+    grid_dep_launch();
     const int t = blockIdx.x;
     const int lane = threadIdx.x & 31;
     const int64_t total = (int64_t)p.T * p.nbk;
@@ -1178,15 +1182,13 @@ int launch(const MlaArgs &a, cudaStream_t stream, char *err, size_t errlen)
         p.ws_o = static_cast<float *>(a.workspace);
         p.ws_lse = reinterpret_cast<float *>(static_cast<char *>(a.workspace) + o_bytes);
     }
-    sparse_mla_kernel<PAGED><<<dim3(2 * pl.clusters), kThreads, kSmem, stream>>>(tq, p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(sparse_mla_kernel<PAGED>, dim3(2 * pl.clusters), dim3(kThreads), kSmem, stream, 1, tq, p);
     if (e != cudaSuccess) {
         snprintf(err, errlen, "sparse_mla launch: %s", cudaGetErrorString(e));
         return DSA_ERR_CUDA;
     }
     if (pl.split) {
-        combine_kernel<<<dim3(a.T, (a.H + 7) / 8), 256, 0, stream>>>(p);
-        e = cudaGetLastError();
+        e = launch_pdl(combine_kernel, dim3(a.T, (a.H + 7) / 8), dim3(256), 0, stream, 1, p);
         if (e != cudaSuccess) {
             snprintf(err, errlen, "sparse_mla combine launch: %s", cudaGetErrorString(e));
             return DSA_ERR_CUDA;

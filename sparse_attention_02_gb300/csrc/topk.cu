@@ -504,6 +504,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     __shared__ __align__(16) int hist[4096];
     __shared__ int scratch[kWarps + 1];
     __shared__ int sel[2];
+    grid_dep_wait();
+    grid_dep_launch();
     for (int row = blockIdx.x; row < T; row += gridDim.x) {
         int n = valid_len[row];
         if (n < 0)
@@ -548,6 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ncl = gridDim.x / cs;
     const uint32_t gk0 = mapa_shared(smem_u32(gkey), 0), gi0 = mapa_shared(smem_u32(gidx), 0);
     const uint32_t cnt_local = smem_u32(&wc[kWarps]);
+    grid_dep_wait();
+    grid_dep_launch();
     for (int row = blockIdx.x / cs; row < T; row += ncl) { // the same rows in every CTA of the cluster
         int n = valid_len[row];
         if (n < 0)
@@ -641,23 +645,12 @@ int launch_topk(const TopkArgs &a, cudaStream_t stream, char *err, size_t errlen
         while (cs < 8 && a.T * cs * 2 <= sms)
             cs *= 2;
         const int clusters = a.T < sms / cs ? a.T : sms / cs;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(clusters * cs));
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = kSmemTopk;
-        cfg.stream = stream;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, a.logits, a.ld, a.T, a.valid_len, a.k, a.idx, status);
+        e = launch_pdl(topk_cluster_kernel, dim3(static_cast<unsigned>(clusters * cs)), dim3(kThreads), kSmemTopk,
+                       stream, static_cast<unsigned>(cs), a.logits, a.ld, a.T, a.valid_len, a.k, a.idx, status);
     } else {
         const int grid = a.T < 65535 * 4 ? a.T : 65535 * 4;
-        topk_kernel<<<grid, kThreads, 0, stream>>>(a.logits, a.ld, a.T, a.valid_len, a.k, a.idx, status);
-        e = cudaGetLastError();
+        e = launch_pdl(topk_kernel, dim3(grid), dim3(kThreads), 0, stream, 1, a.logits, a.ld, a.T, a.valid_len, a.k,
+                       a.idx, status);
     }
     if (e != cudaSuccess) {
         snprintf(err, errlen, "topk launch: %s", cudaGetErrorString(e));
