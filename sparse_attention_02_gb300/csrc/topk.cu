@@ -14,11 +14,13 @@
 // a block-wide prefix count gives each kept index its output slot directly,
 // so the output comes out sorted without a sort.
 //
-// Candidate path (batches of at most two rows per SM, i.e. decode; the passes
-// above are its fallback and the whole path for prefill-sized batches).  Each
-// row runs on a cluster of cs CTAs (cs = 1, 2, 4 or 8, as many as the SMs
-// allow): (1) rows longer than kGather draw kSamples keys at a fixed stride,
-// and a radix select over those samples gives a key near sample rank
+// The four passes are the fallback of two candidate kernels, which read a row
+// once or twice and select among a few thousand of its keys.
+//
+// Decode-sized batches (at most two rows per SM): each row runs on a cluster
+// of cs CTAs (cs = 1, 2, 4 or 8, as many as the SMs allow): (1) rows longer
+// than kGather draw kSamples keys at a fixed stride, and a radix select over
+// those samples gives a key near sample rank
 // (1.5 k + 512) / n from the top, the threshold (every CTA of the cluster
 // draws the same samples and gets the same value; shorter rows use none);
 // (2) CTA c streams its own 1/cs of the row once, kUnroll 16-byte loads per
@@ -31,7 +33,8 @@
 // block-wide prefix count over the ordered list writes the kept indices in
 // ascending order, as the compaction above does.  A row whose candidates miss
 // [k, kGather] (tie-heavy or adversarial rows) takes the four passes in CTA 0
-// instead; either way the output is the same.
+// instead; either way the output is the same.  Prefill-sized batches use the
+// one-CTA-per-row kernel described before topk_rows_kernel.
 #include "common.cuh"
 #include "launch.h"
 
@@ -60,6 +63,7 @@ __device__ __forceinline__ uint32_t order_key(float x)
 
 // Exclusive prefix sum over the block in thread order; returns the prefix and
 // writes the block total to *total.  `scratch` holds kWarps + 1 ints.
+template <int NT>
 __device__ __forceinline__ int block_exclusive_scan(int v, int *scratch, int *total)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -74,42 +78,42 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *scratch, int *to
         scratch[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        int w = lane < kWarps ? scratch[lane] : 0;
+        int w = lane < (NT / 32) ? scratch[lane] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, w, o);
             if (lane >= o)
                 w += y;
         }
-        if (lane < kWarps)
+        if (lane < (NT / 32))
             scratch[lane] = w; // inclusive over warps
-        if (lane == kWarps - 1)
-            scratch[kWarps] = w;
+        if (lane == (NT / 32) - 1)
+            scratch[(NT / 32)] = w;
     }
     __syncthreads();
     const int prefix = (warp > 0 ? scratch[warp - 1] : 0) + x - v;
-    *total = scratch[kWarps];
+    *total = scratch[(NT / 32)];
     __syncthreads(); // scratch reusable afterwards
     return prefix;
 }
 
-template <bool kVec, typename F>
+template <int NT, bool kVec, typename F>
 __device__ __forceinline__ void for_each_key(const float *row, int n, F &&f)
 {
     if (kVec) {
         const float4 *r4 = reinterpret_cast<const float4 *>(row);
         const int n4 = n >> 2;
-        for (int i = threadIdx.x; i < n4; i += kThreads) {
+        for (int i = threadIdx.x; i < n4; i += NT) {
             const float4 v = __ldg(r4 + i);
             f(4 * i + 0, order_key(v.x));
             f(4 * i + 1, order_key(v.y));
             f(4 * i + 2, order_key(v.z));
             f(4 * i + 3, order_key(v.w));
         }
-        for (int i = 4 * n4 + threadIdx.x; i < n; i += kThreads)
+        for (int i = 4 * n4 + threadIdx.x; i < n; i += NT)
             f(i, order_key(__ldg(row + i)));
     } else {
-        for (int i = threadIdx.x; i < n; i += kThreads)
+        for (int i = threadIdx.x; i < n; i += NT)
             f(i, order_key(__ldg(row + i)));
     }
 }
@@ -119,27 +123,27 @@ __device__ __forceinline__ void for_each_key(const float *row, int n, F &&f)
 // count(bins >= b).  Writes b and count(bins > b) to out[0], out[1].  Thread t
 // owns the contiguous bins [nbins - (t + 1) per, nbins - t per), read with
 // 16-byte loads when per >= 4 so the warp's reads do not collide on banks.
+template <int NT>
 __device__ __forceinline__ void select_bin(const int *hist, int nbins, int k_rem, int *scratch, int *out)
 {
-    const int per = nbins / kThreads > 0 ? nbins / kThreads : 1;
+    constexpr int kMaxPer = 4096 / NT; // histograms hold at most 4096 bins
+    const int per = nbins / NT > 0 ? nbins / NT : 1;
     const int hi = nbins - threadIdx.x * per; // this thread owns bins [hi - per, hi), highest first
-    int c[8];                                 // c[j]: count of bin hi - 1 - j
+    int c[kMaxPer];                           // c[j]: count of bin hi - 1 - j
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+    for (int j = 0; j < kMaxPer; ++j)
         c[j] = 0;
     if (hi > 0) {
         if (per >= 4) {
-            const int4 b = *reinterpret_cast<const int4 *>(hist + hi - 4);
-            c[0] = b.w;
-            c[1] = b.z;
-            c[2] = b.y;
-            c[3] = b.x;
-            if (per == 8) {
-                const int4 a = *reinterpret_cast<const int4 *>(hist + hi - 8);
-                c[4] = a.w;
-                c[5] = a.z;
-                c[6] = a.y;
-                c[7] = a.x;
+#pragma unroll
+            for (int q = 0; q < kMaxPer / 4; ++q) {
+                if (4 * q < per) {
+                    const int4 b = *reinterpret_cast<const int4 *>(hist + hi - 4 * (q + 1));
+                    c[4 * q] = b.w;
+                    c[4 * q + 1] = b.z;
+                    c[4 * q + 2] = b.y;
+                    c[4 * q + 3] = b.x;
+                }
             }
         } else {
 #pragma unroll
@@ -150,13 +154,13 @@ __device__ __forceinline__ void select_bin(const int *hist, int nbins, int k_rem
     }
     int sum = 0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+    for (int j = 0; j < kMaxPer; ++j)
         sum += c[j];
     int total;
-    int above = block_exclusive_scan(sum, scratch, &total);
+    int above = block_exclusive_scan<NT>(sum, scratch, &total);
     if (hi > 0) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < kMaxPer; ++j) {
             if (j < per) {
                 if (above < k_rem && above + c[j] >= k_rem) {
                     out[0] = hi - 1 - j;
@@ -169,44 +173,44 @@ __device__ __forceinline__ void select_bin(const int *hist, int nbins, int k_rem
     __syncthreads();
 }
 
-template <bool kVec>
+template <int NT, bool kVec>
 __device__ void topk_row(const float *row, int n, int k, int32_t *out, int *hist, int *scratch, int *sel)
 {
     // pass 1: top 12 bits
-    for (int b = threadIdx.x; b < 4096; b += kThreads)
+    for (int b = threadIdx.x; b < 4096; b += NT)
         hist[b] = 0;
     __syncthreads();
-    for_each_key<kVec>(row, n, [&](int, uint32_t key) { atomicAdd(&hist[key >> 20], 1); });
+    for_each_key<NT, kVec>(row, n, [&](int, uint32_t key) { atomicAdd(&hist[key >> 20], 1); });
     __syncthreads();
-    select_bin(hist, 4096, k, scratch, sel);
+    select_bin<NT>(hist, 4096, k, scratch, sel);
     const uint32_t d0 = sel[0];
     int k_rem = k - sel[1];
     __syncthreads();
 
     // pass 2: next 12 bits among keys with the chosen top digit
-    for (int b = threadIdx.x; b < 4096; b += kThreads)
+    for (int b = threadIdx.x; b < 4096; b += NT)
         hist[b] = 0;
     __syncthreads();
-    for_each_key<kVec>(row, n, [&](int, uint32_t key) {
+    for_each_key<NT, kVec>(row, n, [&](int, uint32_t key) {
         if ((key >> 20) == d0)
             atomicAdd(&hist[(key >> 8) & 0xFFFu], 1);
     });
     __syncthreads();
-    select_bin(hist, 4096, k_rem, scratch, sel);
+    select_bin<NT>(hist, 4096, k_rem, scratch, sel);
     const uint32_t p1 = (d0 << 12) | static_cast<uint32_t>(sel[0]);
     k_rem -= sel[1];
     __syncthreads();
 
     // pass 3: last 8 bits
-    for (int b = threadIdx.x; b < 256; b += kThreads)
+    for (int b = threadIdx.x; b < 256; b += NT)
         hist[b] = 0;
     __syncthreads();
-    for_each_key<kVec>(row, n, [&](int, uint32_t key) {
+    for_each_key<NT, kVec>(row, n, [&](int, uint32_t key) {
         if ((key >> 8) == p1)
             atomicAdd(&hist[key & 0xFFu], 1);
     });
     __syncthreads();
-    select_bin(hist, 256, k_rem, scratch, sel);
+    select_bin<NT>(hist, 256, k_rem, scratch, sel);
     const uint32_t tau = (p1 << 8) | static_cast<uint32_t>(sel[0]);
     k_rem -= sel[1];
     // k_rem = how many keys equal to tau are kept (the first ones in index order)
@@ -214,9 +218,9 @@ __device__ void topk_row(const float *row, int n, int k, int32_t *out, int *hist
     __syncthreads();
 
     // pass 4: ordered compaction.  Thread i handles elements [4i, 4i+4) of
-    // each 4*kThreads chunk; gt/eq counts are packed (gt << 16 | eq).
+    // each 4*NT chunk; gt/eq counts are packed (gt << 16 | eq).
     int gt_base = 0, eq_base = 0;
-    for (int c0 = 0; c0 < n; c0 += 4 * kThreads) {
+    for (int c0 = 0; c0 < n; c0 += 4 * NT) {
         const int i0 = c0 + 4 * threadIdx.x;
         uint32_t keys[4];
         int valid = 0;
@@ -247,7 +251,7 @@ __device__ void topk_row(const float *row, int n, int k, int32_t *out, int *hist
             }
         }
         int total;
-        const int pre = block_exclusive_scan((gt << 16) | eq, scratch, &total);
+        const int pre = block_exclusive_scan<NT>((gt << 16) | eq, scratch, &total);
         int g_before = gt_base + (pre >> 16);
         int e_before = eq_base + (pre & 0xFFFF);
 #pragma unroll
@@ -275,27 +279,28 @@ __device__ void topk_row(const float *row, int n, int k, int32_t *out, int *hist
 // the key at rank ~ (1.5 k + 512) / n among kSamples keys drawn at a fixed
 // stride, so every sample at or above that rank passes it.  Deterministic: a
 // function of the row alone.
+template <int NT>
 __device__ uint32_t sample_threshold(const float *row, int n, int k, int *hist, int *scratch, int *sel)
 {
-    constexpr int kPer = kSamples / kThreads;
+    constexpr int kPer = kSamples / NT;
     uint32_t sk[kPer];
 #pragma unroll
     for (int e = 0; e < kPer; ++e)
-        sk[e] = order_key(__ldg(row + (int64_t)(threadIdx.x + e * kThreads) * n / kSamples));
+        sk[e] = order_key(__ldg(row + (int64_t)(threadIdx.x + e * NT) * n / kSamples));
     int r = (int)((int64_t)(3 * k / 2 + 512) * kSamples / n);
     r = r < 1 ? 1 : (r > kSamples ? kSamples : r);
-    for (int b = threadIdx.x; b < 4096; b += kThreads)
+    for (int b = threadIdx.x; b < 4096; b += NT)
         hist[b] = 0;
     __syncthreads();
 #pragma unroll
     for (int e = 0; e < kPer; ++e)
         atomicAdd(&hist[sk[e] >> 20], 1);
     __syncthreads();
-    select_bin(hist, 4096, r, scratch, sel);
+    select_bin<NT>(hist, 4096, r, scratch, sel);
     const uint32_t d0 = sel[0];
     r -= sel[1];
     __syncthreads();
-    for (int b = threadIdx.x; b < 4096; b += kThreads)
+    for (int b = threadIdx.x; b < 4096; b += NT)
         hist[b] = 0;
     __syncthreads();
 #pragma unroll
@@ -303,7 +308,7 @@ __device__ uint32_t sample_threshold(const float *row, int n, int k, int *hist, 
         if ((sk[e] >> 20) == d0)
             atomicAdd(&hist[(sk[e] >> 8) & 0xFFFu], 1);
     __syncthreads();
-    select_bin(hist, 4096, r, scratch, sel);
+    select_bin<NT>(hist, 4096, r, scratch, sel);
     const uint32_t thr = ((d0 << 12) | static_cast<uint32_t>(sel[0])) << 8;
     __syncthreads();
     return thr;
@@ -316,13 +321,14 @@ __device__ uint32_t sample_threshold(const float *row, int n, int k, int *hist, 
 // region ck/ci[w * kSeg, +kSeg) with ballot prefix counts.  Leaves in wc[w]
 // the offset of warp w's region in the CTA's flat candidate list and in
 // wc[kWarps] the CTA's count, or -1 if a region overflowed.
+template <int NT>
 __device__ void filter_segment(const float *row, int c0, int c1, int head, uint32_t thr, uint32_t *ck, int32_t *ci,
                                int *wc)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t lt = (1u << lane) - 1u;
     const int v0 = c0 + head;
-    const int seg = (((c1 - v0 + kWarps - 1) / kWarps) + 3) & ~3;
+    const int seg = (((c1 - v0 + (NT / 32) - 1) / (NT / 32)) + 3) & ~3;
     const int s0 = v0 + warp * seg < c1 ? v0 + warp * seg : c1;
     const int s1 = s0 + seg < c1 ? s0 + seg : c1;
     uint32_t *wk = ck + warp * kSeg;
@@ -387,13 +393,13 @@ __device__ void filter_segment(const float *row, int c0, int c1, int head, uint3
     __syncthreads();
     if (threadIdx.x == 0) {
         int tot = 0, over = 0;
-        for (int w = 0; w < kWarps; ++w) {
+        for (int w = 0; w < (NT / 32); ++w) {
             const int c = wc[w];
             over |= c > kSeg;
             wc[w] = tot;
             tot += c;
         }
-        wc[kWarps] = over ? -1 : tot;
+        wc[(NT / 32)] = over ? -1 : tot;
     }
     __syncthreads();
 }
@@ -410,6 +416,7 @@ __device__ __forceinline__ int cand_slot(const int *wc, int f)
 
 // Exact top-k of nc >= k candidates ck/ci listed in ascending index order;
 // writes the kept indices to out in that order.
+template <int NT>
 __device__ void select_candidates(const uint32_t *ck, const int32_t *ci, int nc, int k, int32_t *out, int *hist,
                                   int *scratch, int *sel)
 {
@@ -418,7 +425,7 @@ __device__ void select_candidates(const uint32_t *ck, const int32_t *ci, int nc,
     // so passes of at most 12 bits over d spread close scores over the bins
     // instead of piling them into a few bins of the raw top digit.
     uint32_t lo = 0xFFFFFFFFu, hi = 0u;
-    for (int f = threadIdx.x; f < nc; f += kThreads) {
+    for (int f = threadIdx.x; f < nc; f += NT) {
         const uint32_t key = ck[f];
         lo = key < lo ? key : lo;
         hi = key > hi ? key : hi;
@@ -435,7 +442,7 @@ __device__ void select_candidates(const uint32_t *ck, const int32_t *ci, int nc,
     }
     __syncthreads();
     uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-    for (int w = 0; w < kWarps; ++w) {
+    for (int w = 0; w < (NT / 32); ++w) {
         const uint32_t l2 = static_cast<uint32_t>(hist[2 * w]), h2 = static_cast<uint32_t>(hist[2 * w + 1]);
         kmin = l2 < kmin ? l2 : kmin;
         kmax = h2 > kmax ? h2 : kmax;
@@ -449,16 +456,16 @@ __device__ void select_candidates(const uint32_t *ck, const int32_t *ci, int nc,
     uint32_t prefix = 0u;
     int k_rem = k;
     for (;;) {
-        for (int q = threadIdx.x; q < nbins; q += kThreads)
+        for (int q = threadIdx.x; q < nbins; q += NT)
             hist[q] = 0;
         __syncthreads();
-        for (int f = threadIdx.x; f < nc; f += kThreads) {
+        for (int f = threadIdx.x; f < nc; f += NT) {
             const uint32_t d = ck[f] - kmin;
             if (prev == 32 || (d >> prev) == prefix)
                 atomicAdd(&hist[(d >> shift) & static_cast<uint32_t>(nbins - 1)], 1);
         }
         __syncthreads();
-        select_bin(hist, nbins, k_rem, scratch, sel);
+        select_bin<NT>(hist, nbins, k_rem, scratch, sel);
         const uint32_t bsel = static_cast<uint32_t>(sel[0]);
         k_rem -= sel[1];
         __syncthreads();
@@ -472,7 +479,7 @@ __device__ void select_candidates(const uint32_t *ck, const int32_t *ci, int nc,
     const uint32_t tau = kmin + prefix; // every bit of d fixed: the k-th largest candidate key
     const int need_eq = k_rem;          // keys equal to tau to keep (the smallest indices)
     // ordered output: thread t walks candidates [t * per, t * per + per)
-    const int per = (nc + kThreads - 1) / kThreads;
+    const int per = (nc + NT - 1) / NT;
     const int f0 = threadIdx.x * per < nc ? threadIdx.x * per : nc;
     const int f1 = f0 + per < nc ? f0 + per : nc;
     int gt = 0, eq = 0;
@@ -482,7 +489,7 @@ __device__ void select_candidates(const uint32_t *ck, const int32_t *ci, int nc,
         eq += key == tau;
     }
     int total;
-    const int pre = block_exclusive_scan((gt << 16) | eq, scratch, &total);
+    const int pre = block_exclusive_scan<NT>((gt << 16) | eq, scratch, &total);
     int g_before = pre >> 16, e_before = pre & 0xFFFF;
     for (int f = f0; f < f1; ++f) {
         const uint32_t key = ck[f];
@@ -497,13 +504,189 @@ __device__ void select_candidates(const uint32_t *ck, const int32_t *ci, int nc,
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
-    topk_kernel(const float *__restrict__ logits, int64_t ld, int T, const int32_t *__restrict__ valid_len, int k,
-                int32_t *__restrict__ idx, unsigned *status)
+// ---------------------------------------------------------------------------
+// Prefill-sized batches: one 256-thread CTA per row, four rows in flight per
+// SM (the phases below are short and end in barriers, so rows in flight, not
+// bytes, set the rate); the row is read twice.
+// (1) Rows longer than kRowCap draw kSamples keys at a fixed stride; one
+//     11-bit histogram of (sample key - smallest sample key), scaled to the
+//     samples' range, gives a threshold at or below the sample of rank
+//     ~ (1.25 k + 256) / n from the top.  (2) A counting pass over the row
+//     (warp w scans its own contiguous segment, ballot counts) and a block
+//     scan place every warp's keys at or above the threshold; a second pass
+//     (L1/L2 hits) writes (key, index) there, so the list is in index order.
+//     (3) The exact radix select over those candidates and the ordered
+//     compaction of select_candidates.  A row whose count misses [k, kRowCap]
+//     takes the four passes instead; the result is the same.
+constexpr int kRowThreads = 256;                       // four rows in flight per SM
+constexpr int kRowCap = 4096;                          // candidates of one row
+constexpr int kRowSmem = (2 * kRowCap + 4096) * 4;     // keys, indices, histogram
+
+template <int NT>
+__device__ uint32_t row_threshold(const float *row, int n, int k, int *hist, int *scratch, int *sel)
 {
-    __shared__ __align__(16) int hist[4096];
-    __shared__ int scratch[kWarps + 1];
+    constexpr int kPer = kSamples / NT;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint32_t sk[kPer];
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+        sk[e] = order_key(__ldg(row + (int64_t)(threadIdx.x + e * NT) * n / kSamples));
+        lo = sk[e] < lo ? sk[e] : lo;
+        hi = sk[e] > hi ? sk[e] : hi;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const uint32_t l2 = __shfl_xor_sync(0xffffffffu, lo, o), h2 = __shfl_xor_sync(0xffffffffu, hi, o);
+        lo = l2 < lo ? l2 : lo;
+        hi = h2 > hi ? h2 : hi;
+    }
+    if (lane == 0) {
+        hist[2 * warp] = static_cast<int>(lo);
+        hist[2 * warp + 1] = static_cast<int>(hi);
+    }
+    __syncthreads();
+    uint32_t smin = 0xFFFFFFFFu, smax = 0u;
+    for (int w = 0; w < (NT / 32); ++w) {
+        const uint32_t l2 = static_cast<uint32_t>(hist[2 * w]), h2 = static_cast<uint32_t>(hist[2 * w + 1]);
+        smin = l2 < smin ? l2 : smin;
+        smax = h2 > smax ? h2 : smax;
+    }
+    __syncthreads();
+    const uint32_t range = smax - smin;
+    const int bits = range == 0u ? 0 : 32 - __clz(range);
+    const int shift = bits > 11 ? bits - 11 : 0;
+    for (int b = threadIdx.x; b < 2048; b += NT)
+        hist[b] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < kPer; ++e)
+        atomicAdd(&hist[(sk[e] - smin) >> shift], 1);
+    __syncthreads();
+    int r = (int)((int64_t)(5 * k / 4 + 256) * kSamples / n);
+    r = r < 1 ? 1 : (r > kSamples ? kSamples : r);
+    select_bin<NT>(hist, 2048, r, scratch, sel);
+    const uint32_t thr = smin + (static_cast<uint32_t>(sel[0]) << shift);
+    __syncthreads();
+    return thr;
+}
+
+// One pass over warp w's segment of row[c0 + head, c1) (16-byte aligned from
+// there; the `head` keys before it go to warp 0 first): counts the keys >= thr
+// (kWrite = false), or writes them as (key, index) from slot base on (kWrite).
+// Returns the warp's count (warp-uniform).
+template <int NT, bool kWrite>
+__device__ int row_pass(const float *row, int c0, int c1, int head, uint32_t thr, int base, uint32_t *ck,
+                        int32_t *ci)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t lt = (1u << lane) - 1u;
+    const int v0 = c0 + head;
+    const int seg = (((c1 - v0 + (NT / 32) - 1) / (NT / 32)) + 3) & ~3;
+    const int s0 = v0 + warp * seg < c1 ? v0 + warp * seg : c1;
+    const int s1 = s0 + seg < c1 ? s0 + seg : c1;
+    int cnt = 0;
+    if (warp == 0 && head > 0) {
+        const int i = c0 + lane;
+        const uint32_t key = lane < head ? order_key(__ldg(row + i)) : 0u;
+        const bool f = lane < head && key >= thr;
+        const unsigned m = __ballot_sync(0xffffffffu, f);
+        if (kWrite && f) {
+            ck[base + __popc(m & lt)] = key;
+            ci[base + __popc(m & lt)] = i;
+        }
+        cnt = __popc(m);
+    }
+    for (int b0 = s0; b0 < s1; b0 += 128 * kUnroll) {
+        uint32_t kk[kUnroll][4];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int i = b0 + 128 * u + 4 * lane;
+            if (i + 3 < s1) {
+                const float4 v = __ldg(reinterpret_cast<const float4 *>(row + i));
+                kk[u][0] = order_key(v.x);
+                kk[u][1] = order_key(v.y);
+                kk[u][2] = order_key(v.z);
+                kk[u][3] = order_key(v.w);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    kk[u][e] = i + e < s1 ? order_key(__ldg(row + i + e)) : 0u;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int i = b0 + 128 * u + 4 * lane;
+            bool f[4];
+            int pre = 0, tot = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                f[e] = i + e < s1 && kk[u][e] >= thr;
+                const unsigned m = __ballot_sync(0xffffffffu, f[e]);
+                pre += __popc(m & lt);
+                tot += __popc(m);
+            }
+            if (kWrite) {
+                int slot = base + cnt + pre;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (f[e]) {
+                        ck[slot] = kk[u][e];
+                        ci[slot] = i + e;
+                        ++slot;
+                    }
+                }
+            }
+            cnt += tot;
+        }
+    }
+    return cnt;
+}
+
+// Candidate path for one row with k < n; false (nothing written) when the row
+// must take the four passes.  wc: kWarps + 1 ints of shared memory.
+template <int NT>
+__device__ bool topk_row_candidates(const float *row, int n, int k, int32_t *out, uint32_t *ck, int32_t *ci,
+                                    int *hist, int *scratch, int *sel, int *wc)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t thr = n > kRowCap ? row_threshold<NT>(row, n, k, hist, scratch, sel) : 0u;
+    int h = static_cast<int>((4u - ((reinterpret_cast<uintptr_t>(row) >> 2) & 3u)) & 3u);
+    h = h < n ? h : n;
+    const int c = row_pass<NT, false>(row, 0, n, h, thr, 0, ck, ci);
+    if (lane == 0)
+        wc[warp] = c;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int tot = 0;
+        for (int w = 0; w < (NT / 32); ++w) {
+            const int x = wc[w];
+            wc[w] = tot;
+            tot += x;
+        }
+        wc[(NT / 32)] = tot;
+    }
+    __syncthreads();
+    const int nc = wc[(NT / 32)];
+    if (nc < k || nc > kRowCap)
+        return false;
+    row_pass<NT, true>(row, 0, n, h, thr, wc[warp], ck, ci);
+    __syncthreads();
+    select_candidates<NT>(ck, ci, nc, k, out, hist, scratch, sel);
+    return true;
+}
+
+__global__ void __launch_bounds__(kRowThreads, 4)
+    topk_rows_kernel(const float *__restrict__ logits, int64_t ld, int T, const int32_t *__restrict__ valid_len, int k,
+                     int32_t *__restrict__ idx, unsigned *status)
+{
+    extern __shared__ __align__(16) uint32_t dsm[];
+    uint32_t *ck = dsm;
+    int32_t *ci = reinterpret_cast<int32_t *>(dsm + kRowCap);
+    int *hist = reinterpret_cast<int *>(dsm + 2 * kRowCap);
+    __shared__ int scratch[kRowThreads / 32 + 1];
     __shared__ int sel[2];
+    __shared__ int wc[kRowThreads / 32 + 1];
     grid_dep_wait();
     grid_dep_launch();
     for (int row = blockIdx.x; row < T; row += gridDim.x) {
@@ -517,15 +700,19 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         int32_t *out = idx + static_cast<int64_t>(row) * k;
         if (n <= k) {
-            for (int j = threadIdx.x; j < k; j += kThreads)
+            for (int j = threadIdx.x; j < k; j += kRowThreads)
                 out[j] = j < n ? j : -1;
             continue;
         }
         const float *r = logits + static_cast<int64_t>(row) * ld;
-        if ((reinterpret_cast<uintptr_t>(r) & 15u) == 0)
-            topk_row<true>(r, n, k, out, hist, scratch, sel);
-        else
-            topk_row<false>(r, n, k, out, hist, scratch, sel);
+        const bool done = topk_row_candidates<kRowThreads>(r, n, k, out, ck, ci, hist, scratch, sel, wc);
+        __syncthreads();
+        if (!done) {
+            if ((reinterpret_cast<uintptr_t>(r) & 15u) == 0)
+                topk_row<kRowThreads, true>(r, n, k, out, hist, scratch, sel);
+            else
+                topk_row<kRowThreads, false>(r, n, k, out, hist, scratch, sel);
+        }
         __syncthreads();
     }
 }
@@ -570,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float *r = logits + static_cast<int64_t>(row) * ld;
         const bool vec = (reinterpret_cast<uintptr_t>(r) & 15u) == 0;
-        const uint32_t thr = n > kGather ? sample_threshold(r, n, k, hist, scratch, sel) : 0u;
+        const uint32_t thr = n > kGather ? sample_threshold<kThreads>(r, n, k, hist, scratch, sel) : 0u;
         // keys before the row's first 16-byte boundary, then chunks of a multiple
         // of 4 keys from there (fp32 rows are 4-byte aligned)
         int h = static_cast<int>((4u - ((reinterpret_cast<uintptr_t>(r) >> 2) & 3u)) & 3u);
@@ -578,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int chunk = ((n - h + cs - 1) / cs + 3) & ~3;
         const int c0 = cr == 0 ? 0 : (h + cr * chunk < n ? h + cr * chunk : n);
         const int c1 = h + (cr + 1) * chunk < n ? h + (cr + 1) * chunk : n;
-        filter_segment(r, c0, c1, cr == 0 ? h : 0, thr, lkey, lidx, wc);
+        filter_segment<kThreads>(r, c0, c1, cr == 0 ? h : 0, thr, lkey, lidx, wc);
         cluster_sync_all(); // every CTA's count is in its wc[kWarps]
         if (threadIdx.x == 0) {
             int off = 0, tot = 0;
@@ -605,11 +792,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         cluster_sync_all(); // CTA 0's list is complete; nothing of a peer is touched after this
         if (cr == 0) {
             if (nc >= 0)
-                select_candidates(gkey, gidx, nc, k, out, hist, scratch, sel);
+                select_candidates<kThreads>(gkey, gidx, nc, k, out, hist, scratch, sel);
             else if (vec)
-                topk_row<true>(r, n, k, out, hist, scratch, sel);
+                topk_row<kThreads, true>(r, n, k, out, hist, scratch, sel);
             else
-                topk_row<false>(r, n, k, out, hist, scratch, sel);
+                topk_row<kThreads, false>(r, n, k, out, hist, scratch, sel);
         }
         __syncthreads();
     }
@@ -648,9 +835,20 @@ int launch_topk(const TopkArgs &a, cudaStream_t stream, char *err, size_t errlen
         e = launch_pdl(topk_cluster_kernel, dim3(static_cast<unsigned>(clusters * cs)), dim3(kThreads), kSmemTopk,
                        stream, static_cast<unsigned>(cs), a.logits, a.ld, a.T, a.valid_len, a.k, a.idx, status);
     } else {
+        static bool rows_attr[64] = {};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (dev < 64 && !rows_attr[dev]) {
+            e = cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowSmem);
+            if (e != cudaSuccess) {
+                snprintf(err, errlen, "cudaFuncSetAttribute(topk rows): %s", cudaGetErrorString(e));
+                return DSA_ERR_CUDA;
+            }
+            rows_attr[dev] = true;
+        }
         const int grid = a.T < 65535 * 4 ? a.T : 65535 * 4;
-        e = launch_pdl(topk_kernel, dim3(grid), dim3(kThreads), 0, stream, 1, a.logits, a.ld, a.T, a.valid_len, a.k,
-                       a.idx, status);
+        e = launch_pdl(topk_rows_kernel, dim3(grid), dim3(kRowThreads), kRowSmem, stream, 1, a.logits, a.ld, a.T,
+                       a.valid_len, a.k, a.idx, status);
     }
     if (e != cudaSuccess) {
         snprintf(err, errlen, "topk launch: %s", cudaGetErrorString(e));

@@ -55,9 +55,11 @@ def test_topk_from_gpu_logits_bit_exact():
         assert np.array_equal(idx.cpu().numpy(), ref), f"k={k}"
 
 
-# A grid of at most two rows per SM takes the candidate fast path, a larger one the
-# four-pass kernel; tiling the same rows REPS times sends them through the latter.
-REPS_MANY_ROWS = 20
+# At most two rows per SM run on the cluster kernel (one cluster per row), more rows on
+# the one-CTA-per-row kernel; tiling the same rows REPS_MANY_ROWS times (more than 304
+# rows) sends them through the latter.  Both fall back to the four histogram passes for
+# rows whose candidates overflow (the all-ties row below).
+REPS_MANY_ROWS = 40
 
 
 @pytest.mark.parametrize("reps", [1, REPS_MANY_ROWS])
