@@ -224,6 +224,43 @@ int dsa_sparse_mla_decode_paged(const void *q, const void *kv_pool, int num_page
                                 dsa_stream_t stream);
 
 /*
+ * dsa_prefill_host: the whole prefill path (dsa_indexer_logits -> dsa_topk ->
+ * dsa_sparse_mla_prefill, contiguous keys) on inputs in HOST memory, with the
+ * outputs written back to HOST memory.  Row r is the query at position
+ * q_pos[r] over keys [0, q_pos[r]] (release summary "DeepSeek-V3.2-Exp:
+ * Boosting Long-Context Efficiency with DeepSeek Sparse Attention", section
+ * "Method"); rows and their arguments mean what they mean for the three
+ * device entry points, whose results this call reproduces byte for byte.
+ *
+ *   host: q8 [T, H_I, d_I] FP8, q_scale [T], w [T, H_I], q_pos [T] int32,
+ *         k8 [S, d_I] FP8, k_scale [S], q [T, H, 576] bf16, kv [S, 576] bf16
+ *         -> out [T, H, 512] bf16, lse [T, H] fp32.  0 <= q_pos[r] < S.
+ *   workspace: device buffer of dsa_prefill_host_workspace_size(...) bytes,
+ *         256-byte aligned, owned by the caller.
+ *
+ * Query rows go in chunks of chunk_rows: the inputs of a chunk are copied in
+ * on a copy stream, its kernels run on `stream`, its outputs are copied out on
+ * a second copy stream, and two buffer slots let the copies of neighbouring
+ * chunks overlap the kernels.  The keys stay on the device for the call and are
+ * copied in as far as each chunk's positions need them.  Host buffers should be
+ * page-locked (cudaHostAlloc or cudaHostRegister) for the copies to overlap;
+ * pageable memory gives the same results more slowly.  The call returns once
+ * everything is enqueued; all of it is complete when `stream` reaches this
+ * point, and the host buffers must stay untouched until then.  The first call
+ * on a device creates the two copy streams and a few events, kept until exit;
+ * calls from several host threads enqueue one at a time.  Errors of the three
+ * stages are reported as they would be by their entry points.
+ */
+int dsa_prefill_host(const void *q8, const float *q_scale, const float *w, const int32_t *q_pos,
+                     const void *k8, const float *k_scale, const void *q, const void *kv,
+                     int T, int S, int H_I, int d_I, int H, int k, float sm_scale,
+                     void *out, float *lse, int chunk_rows,
+                     void *workspace, size_t workspace_bytes, dsa_stream_t stream);
+
+/* Device workspace bytes dsa_prefill_host needs (0 on bad input). */
+size_t dsa_prefill_host_workspace_size(int T, int S, int H_I, int d_I, int H, int k, int chunk_rows);
+
+/*
  * dsa_sparse_mla_decode_paged_noalloc: dsa_sparse_mla_decode_paged without a
  * caller-provided workspace.  The pages have no counterpart to this entry
  * point: it is for callers that cannot allocate device memory while they

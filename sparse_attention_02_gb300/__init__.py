@@ -53,10 +53,13 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.dsa_sparse_mla_prefill.argtypes = [P, P, i32, P, i32, i32, i32, f32, P, P, P]
     lib.dsa_sparse_mla_decode_paged.argtypes = [P, P, i32, i32, P, i32, P, P, i32, i32, i32, f32, P, P, P, sz, P]
     lib.dsa_sparse_mla_decode_paged_noalloc.argtypes = [P, P, i32, i32, P, i32, P, P, i32, i32, i32, f32, P, P, P]
+    lib.dsa_prefill_host.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, P, P, i32, P, sz, P]
+    lib.dsa_prefill_host_workspace_size.restype = sz
+    lib.dsa_prefill_host_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
     lib.dsa_sparse_mla_decode_workspace_size.restype = sz
     lib.dsa_sparse_mla_decode_workspace_size.argtypes = [i32, i32, i32]
     for name in ("dsa_quantize_fp8", "dsa_indexer_logits", "dsa_topk", "dsa_sparse_mla_prefill", "dsa_sparse_mla_decode_paged",
-                 "dsa_sparse_mla_decode_paged_noalloc", "dsa_get_device_status"):
+                 "dsa_sparse_mla_decode_paged_noalloc", "dsa_prefill_host", "dsa_get_device_status"):
         getattr(lib, name).restype = i32
     if path is None:
         _lib = lib
@@ -250,6 +253,44 @@ def dsa_sparse_mla_decode_paged_noalloc(q, kv_pool, block_table, ctx_len, idx, s
                                                               block_table.shape[1], _ptr(ctx_len), _ptr(idx), B, H,
                                                               k, float(sm_scale), _ptr(out), _ptr(lse),
                                                               _stream(stream)))
+    return out, lse
+
+
+def _host(t: torch.Tensor, dtype, name: str, dim: int):
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or t.is_cuda or not t.is_contiguous() or t.dim() != dim:
+        raise ValueError(f"{name}: expected a contiguous {dim}-d host tensor of {dtype}")
+
+
+def dsa_prefill_host_workspace_size(T: int, S: int, H_I: int, d_I: int, H: int, k: int, chunk_rows: int) -> int:
+    return int(load_library().dsa_prefill_host_workspace_size(T, S, H_I, d_I, H, k, chunk_rows))
+
+
+def dsa_prefill_host(q8, q_scale, w, q_pos, k8, k_scale, q, kv, sm_scale: float, k: int, out, lse,
+                     chunk_rows: int = 4096, workspace=None, stream=None):
+    """The whole prefill path on HOST tensors (pinned for overlapped copies): q8 uint8 [T, H_I, d_I],
+    q_scale f32 [T], w f32 [T, H_I], q_pos i32 [T], k8 uint8 [S, d_I], k_scale f32 [S], q bf16 [T, H, 576],
+    kv bf16 [S, 576] -> out bf16 [T, H, 512], lse f32 [T, H] (host).  ``workspace``: a uint8 CUDA tensor of
+    dsa_prefill_host_workspace_size(...) bytes, taken from PyTorch's allocator when None."""
+    _host(q8, torch.uint8, "q8", 3)
+    _host(q_scale, torch.float32, "q_scale", 1)
+    _host(w, torch.float32, "w", 2)
+    _host(q_pos, torch.int32, "q_pos", 1)
+    _host(k8, torch.uint8, "k8", 2)
+    _host(k_scale, torch.float32, "k_scale", 1)
+    _host(q, torch.bfloat16, "q", 3)
+    _host(kv, torch.bfloat16, "kv", 2)
+    _host(out, torch.bfloat16, "out", 3)
+    _host(lse, torch.float32, "lse", 2)
+    T, H_I, d_I = q8.shape
+    S = k8.shape[0]
+    H = q.shape[1]
+    need = dsa_prefill_host_workspace_size(T, S, H_I, d_I, H, k, chunk_rows)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=torch.cuda.current_device())
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().dsa_prefill_host(_ptr(q8), _ptr(q_scale), _ptr(w), _ptr(q_pos), _ptr(k8), _ptr(k_scale),
+                                           _ptr(q), _ptr(kv), T, S, H_I, d_I, H, k, float(sm_scale), _ptr(out),
+                                           _ptr(lse), chunk_rows, _ptr(workspace), ws_bytes, _stream(stream)))
     return out, lse
 
 

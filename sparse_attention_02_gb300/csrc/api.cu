@@ -53,6 +53,15 @@ int current_device()
 
 } // namespace
 
+int report_error(int code, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_err, sizeof t_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
 unsigned *device_status_ptr()
 {
     const int d = current_device();

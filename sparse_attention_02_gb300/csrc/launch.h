@@ -15,6 +15,9 @@ bool encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *bas
 
 int num_sms();
 
+// Records a message for dsa_last_error() on this host thread and returns `code`.
+int report_error(int code, const char *fmt, ...);
+
 // Launches `kernel` on `stream` with programmatic dependent launch allowed
 // (the kernel must call grid_dep_wait() before touching global memory) and,
 // when cluster_x > 1, thread-block clusters of cluster_x CTAs.
