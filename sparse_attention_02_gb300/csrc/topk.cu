@@ -757,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float *r = logits + static_cast<int64_t>(row) * ld;
         const bool vec = (reinterpret_cast<uintptr_t>(r) & 15u) == 0;
-        const uint32_t thr = n > kGather ? sample_threshold<kThreads>(r, n, k, hist, scratch, sel) : 0u;
+        const uint32_t thr = n > kGather ? row_threshold<kThreads>(r, n, k, hist, scratch, sel) : 0u;
         // keys before the row's first 16-byte boundary, then chunks of a multiple
         // of 4 keys from there (fp32 rows are 4-byte aligned)
         int h = static_cast<int>((4u - ((reinterpret_cast<uintptr_t>(r) >> 2) & 3u)) & 3u);
