@@ -19,9 +19,9 @@
 //
 // Decode-sized batches (at most two rows per SM): each row runs on a cluster
 // of cs CTAs (cs = 1, 2, 4 or 8, as many as the SMs allow): (1) rows longer
-// than kGather draw kSamples keys at a fixed stride, and a radix select over
-// those samples gives a key near sample rank
-// (1.5 k + 512) / n from the top, the threshold (every CTA of the cluster
+// than kGather draw kSamples keys at a fixed stride, and one 11-bit histogram
+// over the samples' key range gives a threshold near sample rank
+// (1.25 k + 256) / n from the top (row_threshold; every CTA of the cluster
 // draws the same samples and gets the same value; shorter rows use none);
 // (2) CTA c streams its own 1/cs of the row once, kUnroll 16-byte loads per
 // lane in flight, and keeps every key at or above the threshold: warp w scans
@@ -275,45 +275,6 @@ __device__ void topk_row(const float *row, int n, int k, int32_t *out, int *hist
             break; // block-uniform: every kept index has been written
     }
 }
-// Threshold of the candidate path: the 24-bit prefix (low 8 bits cleared) of
-// the key at rank ~ (1.5 k + 512) / n among kSamples keys drawn at a fixed
-// stride, so every sample at or above that rank passes it.  Deterministic: a
-// function of the row alone.
-template <int NT>
-__device__ uint32_t sample_threshold(const float *row, int n, int k, int *hist, int *scratch, int *sel)
-{
-    constexpr int kPer = kSamples / NT;
-    uint32_t sk[kPer];
-#pragma unroll
-    for (int e = 0; e < kPer; ++e)
-        sk[e] = order_key(__ldg(row + (int64_t)(threadIdx.x + e * NT) * n / kSamples));
-    int r = (int)((int64_t)(3 * k / 2 + 512) * kSamples / n);
-    r = r < 1 ? 1 : (r > kSamples ? kSamples : r);
-    for (int b = threadIdx.x; b < 4096; b += NT)
-        hist[b] = 0;
-    __syncthreads();
-#pragma unroll
-    for (int e = 0; e < kPer; ++e)
-        atomicAdd(&hist[sk[e] >> 20], 1);
-    __syncthreads();
-    select_bin<NT>(hist, 4096, r, scratch, sel);
-    const uint32_t d0 = sel[0];
-    r -= sel[1];
-    __syncthreads();
-    for (int b = threadIdx.x; b < 4096; b += NT)
-        hist[b] = 0;
-    __syncthreads();
-#pragma unroll
-    for (int e = 0; e < kPer; ++e)
-        if ((sk[e] >> 20) == d0)
-            atomicAdd(&hist[(sk[e] >> 8) & 0xFFFu], 1);
-    __syncthreads();
-    select_bin<NT>(hist, 4096, r, scratch, sel);
-    const uint32_t thr = ((d0 << 12) | static_cast<uint32_t>(sel[0])) << 8;
-    __syncthreads();
-    return thr;
-}
-
 // Keeps the keys >= thr of row[c0, c1) in index order.  The first `head`
 // keys (row + c0 + head is 16-byte aligned) go through warp 0 one per lane;
 // then warp w scans its own contiguous segment of the rest, kUnroll 16-byte
