@@ -71,6 +71,17 @@ int dsa_version(void);
 int dsa_get_device_status(dsa_stream_t stream, uint32_t *status_out);
 
 /*
+ * dsa_selftest_wait_timeout: exercises the failure detection that every
+ * kernel's pipeline waits share (the pages have no counterpart).  Launches
+ * one CTA that waits, through the same bounded mbarrier wait, on a barrier
+ * nothing arrives on; after limit_us microseconds (1 .. 1000000) the wait
+ * gives up, sets DSA_DEV_TIMEOUT in the device status word and the kernel
+ * returns, leaving the context usable.  Read the bit with
+ * dsa_get_device_status().  Nothing faults, traps or hangs.
+ */
+int dsa_selftest_wait_timeout(uint32_t limit_us, dsa_stream_t stream);
+
+/*
  * dsa_indexer_logits: lightning-indexer scores (stage 1).
  *
  * Defines, for each query row r at absolute position p = q_pos[r] and each key

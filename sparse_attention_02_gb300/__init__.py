@@ -56,6 +56,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.dsa_prefill_host.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, P, P, i32, P, sz, P]
     lib.dsa_prefill_host_workspace_size.restype = sz
     lib.dsa_prefill_host_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    lib.dsa_selftest_wait_timeout.argtypes = [ctypes.c_uint32, P]
+    lib.dsa_selftest_wait_timeout.restype = i32
     lib.dsa_sparse_mla_decode_workspace_size.restype = sz
     lib.dsa_sparse_mla_decode_workspace_size.argtypes = [i32, i32, i32]
     for name in ("dsa_quantize_fp8", "dsa_indexer_logits", "dsa_topk", "dsa_sparse_mla_prefill", "dsa_sparse_mla_decode_paged",
@@ -292,6 +294,11 @@ def dsa_prefill_host(q8, q_scale, w, q_pos, k8, k_scale, q, kv, sm_scale: float,
                                            _ptr(q), _ptr(kv), T, S, H_I, d_I, H, k, float(sm_scale), _ptr(out),
                                            _ptr(lse), chunk_rows, _ptr(workspace), ws_bytes, _stream(stream)))
     return out, lse
+
+
+def dsa_selftest_wait_timeout(limit_us: int, stream=None):
+    """Run one bounded pipeline wait that nothing completes; it sets DSA_DEV_TIMEOUT after limit_us."""
+    _check(load_library().dsa_selftest_wait_timeout(int(limit_us), _stream(stream)))
 
 
 def dsa_get_device_status(stream=None) -> int:

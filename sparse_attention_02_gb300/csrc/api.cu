@@ -10,6 +10,7 @@
 #include <string.h>
 
 #include "../../include/dsa.h"
+#include "common.cuh"
 #include "launch.h"
 
 namespace dsa {
@@ -312,6 +313,47 @@ int dsa_sparse_mla_decode_paged(const void *q, const void *kv_pool, int num_page
 }
 
 } // extern "C"
+
+// ---------------------------------------------------------------------------
+// Self-test of the failure detection: one CTA waits, through the same bounded
+// mbarrier wait every pipeline uses, on a barrier that nothing arrives on.
+namespace dsa {
+namespace {
+
+__global__ void wait_timeout_kernel(uint64_t limit_ns, unsigned *status)
+{
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    grid_dep_wait();
+    grid_dep_launch();
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // phase 0 never completes: the wait gives up after limit_ns, sets
+    // DSA_DEV_TIMEOUT and the kernel returns
+    mbar_wait_warp(b, 0, &abort_flag, status, limit_ns);
+}
+
+} // namespace
+} // namespace dsa
+
+extern "C" int dsa_selftest_wait_timeout(uint32_t limit_us, dsa_stream_t stream)
+{
+    if (limit_us == 0 || limit_us > 1000000u)
+        return fail(DSA_ERR_INVALID_ARG, "limit_us must be in [1, 1000000]");
+    unsigned *status = device_status_ptr();
+    if (!status)
+        return fail(DSA_ERR_CUDA, "device status word unavailable");
+    cudaError_t e = launch_pdl(wait_timeout_kernel, dim3(1), dim3(32), 0, reinterpret_cast<cudaStream_t>(stream), 1,
+                               (uint64_t)limit_us * 1000u, status);
+    if (e != cudaSuccess)
+        return fail(DSA_ERR_CUDA, "self-test launch: %s", cudaGetErrorString(e));
+    return ok();
+}
 
 // ---------------------------------------------------------------------------
 // Allocation-free decode attention.  The workspace lives in this file-scope

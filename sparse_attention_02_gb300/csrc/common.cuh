@@ -113,7 +113,7 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 // (after flagging) on timeout or when another role already aborted.
 template <bool kClusterScope = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          unsigned *status)
+                                          unsigned *status, uint64_t limit_ns = DSA_WAIT_LIMIT_NS)
 {
     auto poll = [&]() {
         return kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
@@ -127,7 +127,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         if ((n & 15) == 0) {
             if (*abort_flag)
                 return false;
-            if (global_timer_ns() - t0 > DSA_WAIT_LIMIT_NS) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 atomicOr(status, DSA_DEV_TIMEOUT);
                 *abort_flag = 1;
                 return false;
@@ -139,9 +139,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // Warp-uniform form: every lane polls, and the warp proceeds only if all did.
 template <bool kClusterScope = false>
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                               unsigned *status)
+                                               unsigned *status, uint64_t limit_ns = DSA_WAIT_LIMIT_NS)
 {
-    bool ok = mbar_wait<kClusterScope>(bar, parity, abort_flag, status);
+    bool ok = mbar_wait<kClusterScope>(bar, parity, abort_flag, status, limit_ns);
     return __all_sync(0xffffffffu, ok);
 }
 
