@@ -776,8 +776,8 @@ int launch_topk(const TopkArgs &a, cudaStream_t stream, char *err, size_t errlen
     cudaError_t e;
     if (a.T <= 2 * sms) {
         // Few rows (decode): each row's latency is the cost, so a row gets as
-        // many CTAs as the SMs allow and is read once.  Many rows (prefill): the
-        // four-pass kernel's 16 KB footprint keeps two rows in flight per SM.
+        // many CTAs as the SMs allow and is read once.  Many rows (prefill): one
+        // small CTA per row keeps four rows in flight per SM.
         static bool attr_set[64] = {};
         int dev = 0;
         cudaGetDevice(&dev);
