@@ -600,8 +600,10 @@ struct FlatCfg {
     static constexpr int OFF_K = ((2 * QTILE + 1023) / 1024) * 1024; // key ring
     static constexpr int OFF_W = OFF_K + NSTAGE * KSTAGE;           // [2][HI] folded weights
     static constexpr int OFF_PRE = OFF_W + 2 * HI * 4;              // [kFlatRows + 1] tile prefix
-    static constexpr int OFF_BAR = ((OFF_PRE + (kFlatRows + 1) * 4 + 7) / 8) * 8;
-    static constexpr int NBAR = 2 * NSTAGE + 2 + 2 + 2 + 2 + 1;
+    static constexpr int OFF_SC = ((OFF_PRE + (kFlatRows + 1) * 4 + 127) / 128) * 128; // [NSTAGE][128] key scales
+    static constexpr int OFF_SA = OFF_SC + NSTAGE * kTileKeys * 4;  // [2][128] scales of each accumulator's tile
+    static constexpr int OFF_BAR = OFF_SA + 2 * kTileKeys * 4;
+    static constexpr int NBAR = 2 * NSTAGE + 2 + 2 + 2 + 2 + 2 + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 64 + 1024;
     static_assert(DI == 128 && N % 32 == 0 && N >= 32 && N <= 128, "flat indexer shape");
@@ -635,7 +637,7 @@ struct FlatUnits {
 template <int HI, int DI>
 __global__ void __launch_bounds__(FlatCfg<HI, DI>::THREADS, 2)
     indexer_paged_flat_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                              Params p)
+                              const __grid_constant__ CUtensorMap tm_ks, Params p)
 {
     using C = FlatCfg<HI, DI>;
     extern __shared__ uint8_t smem_raw[];
@@ -650,7 +652,12 @@ __global__ void __launch_bounds__(FlatCfg<HI, DI>::THREADS, 2)
     auto acce_bar = [&](int a) { return bar0 + 8u * (2 * C::NSTAGE + 2 + a); };
     auto qfull_bar = [&](int b) { return bar0 + 8u * (2 * C::NSTAGE + 4 + b); };
     auto qempty_bar = [&](int b) { return bar0 + 8u * (2 * C::NSTAGE + 6 + b); };
-    const uint32_t done_bar = bar0 + 8u * (2 * C::NSTAGE + 8);
+    auto sready_bar = [&](int a) { return bar0 + 8u * (2 * C::NSTAGE + 8 + a); };
+    const uint32_t done_bar = bar0 + 8u * (2 * C::NSTAGE + 10);
+    // key scales: each stage's, copied by the TMA beside the keys, then each
+    // accumulator's, copied there by the MMA warp for the epilogue
+    float *sc_stage = reinterpret_cast<float *>(smem + C::OFF_SC);
+    float *sc_acc = reinterpret_cast<float *>(smem + C::OFF_SA);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     int *pos_s = reinterpret_cast<int *>(smem + C::OFF_MISC + 8); // [2]: position of the row in each buffer
@@ -710,6 +717,7 @@ __global__ void __launch_bounds__(FlatCfg<HI, DI>::THREADS, 2)
             mbar_init(acce_bar(a), C::NEPI);
             mbar_init(qfull_bar(a), 1);
             mbar_init(qempty_bar(a), 1 + C::NEPI); // the MMAs of the row, then each epilogue warp
+            mbar_init(sready_bar(a), 1);
         }
         mbar_init(done_bar, 1);
         *abort_flag = 0;
@@ -771,15 +779,19 @@ __global__ void __launch_bounds__(FlatCfg<HI, DI>::THREADS, 2)
                     break;
                 }
                 const uint32_t dst = sbase + C::OFF_K + s * C::KSTAGE;
+                const uint32_t sdst = smem_u32(sc_stage + s * kTileKeys);
                 if (lane == 0)
-                    mbar_arrive_expect_tx(full_bar(s), C::KSTAGE);
+                    mbar_arrive_expect_tx(full_bar(s), C::KSTAGE + kTileKeys * 4);
                 for (int j = 0; j < per_tile; ++j) {
                     const int page = __shfl_sync(0xffffffffu, bt_page, lp0 + j - bt_base);
-                    // an invalid page loads rows past the pool: TMA fills zeros and the
-                    // epilogue skips those keys
-                    const int row = (page >= 0 && page < p.num_pages) ? page * p.page_size : p.num_pages * p.page_size;
-                    if (lane == 0)
+                    // an invalid page loads rows past the pool: TMA fills the codes and the
+                    // scales with zeros, and a zero scale makes the epilogue skip the key
+                    const bool pok = page >= 0 && page < p.num_pages;
+                    const int row = pok ? page * p.page_size : p.num_pages * p.page_size;
+                    if (lane == 0) {
                         tma_load_2d(dst + j * p.page_size * DI, &tm_k, full_bar(s), 0, row);
+                        tma_load_2d(sdst + j * p.page_size * 4, &tm_ks, full_bar(s), 0, pok ? page : p.num_pages);
+                    }
                 }
                 __syncwarp();
             }
@@ -810,6 +822,11 @@ __global__ void __launch_bounds__(FlatCfg<HI, DI>::THREADS, 2)
                     break;
                 }
                 tc_fence_after();
+                // the tile's key scales go with its accumulator (the epilogue released
+                // this slot's previous scales together with the accumulator)
+                reinterpret_cast<float4 *>(sc_acc + acc * kTileKeys)[lane] =
+                    reinterpret_cast<const float4 *>(sc_stage + s * kTileKeys)[lane];
+                __syncwarp();
                 if (lane == 0) {
                     const uint32_t abase = sbase + C::OFF_K + s * C::KSTAGE;
                     const uint32_t bbase = sbase + C::OFF_Q + qb * C::QTILE;
@@ -820,6 +837,7 @@ __global__ void __launch_bounds__(FlatCfg<HI, DI>::THREADS, 2)
                         umma_f8f6f4(tmem + acc * C::N, ad, bd, idesc, kk > 0 ? 1u : 0u);
                     }
                     umma_commit(accf_bar(acc));
+                    mbar_arrive(sready_bar(acc));
                     umma_commit(empty_bar(s));
                 }
                 __syncwarp();
@@ -847,33 +865,19 @@ __global__ void __launch_bounds__(FlatCfg<HI, DI>::THREADS, 2)
                 break;
             const int pos = pos_s[qb];
             const float4 *w4 = reinterpret_cast<const float4 *>(wq_s + qb * HI);
-            // this thread's key's pool page and scale, two and one tiles ahead
-            auto page_of = [&](int kt) -> int {
-                const int lp = (int)(((int64_t)kt * kTileKeys + key_in_tile) / p.page_size);
-                return (kt < tb && lp < p.max_pages) ? __ldg(p.block_table + (int64_t)r * p.max_pages + lp) : -1;
-            };
-            auto scale_of = [&](int kt, int page) -> float {
-                const int64_t sk = (int64_t)kt * kTileKeys + key_in_tile;
-                return (page >= 0 && page < p.num_pages)
-                           ? __ldg(p.k_scale + (int64_t)page * p.page_size + sk % p.page_size)
-                           : 0.f;
-            };
-            int pg0 = page_of(ta), pg1 = page_of(ta + 1);
-            float ks0 = scale_of(ta, pg0);
             for (int kt = ta; kt < tb; ++kt, ++it) {
                 const int64_t s = (int64_t)kt * kTileKeys + key_in_tile;
-                const bool key_ok = pg0 >= 0 && pg0 < p.num_pages;
-                if (!key_ok && s <= pos && lane == 0)
-                    atomicOr(p.status, DSA_DEV_BAD_PAGE);
-                const float ks = ks0;
-                ks0 = scale_of(kt + 1, pg1);
-                pg0 = pg1;
-                pg1 = page_of(kt + 2);
                 const int acc = it & 1, use = it >> 1;
-                if (!mbar_wait_warp(accf_bar(acc), use & 1, abort_flag, p.status)) {
+                if (!mbar_wait_warp(accf_bar(acc), use & 1, abort_flag, p.status) ||
+                    !mbar_wait_warp(sready_bar(acc), use & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
+                // the key's scale (zero for a key on a page outside the pool)
+                const float ks = sc_acc[acc * kTileKeys + key_in_tile];
+                const bool key_ok = ks > 0.f;
+                if (!key_ok && s <= pos && lane == 0)
+                    atomicOr(p.status, DSA_DEV_BAD_PAGE);
                 tc_fence_after();
                 uint32_t v[HI];
 #pragma unroll
@@ -963,8 +967,14 @@ int launch_cfg(const IndexerArgs &a, cudaStream_t stream, char *err, size_t errl
     if constexpr (PAGED && DI == 128 && (HI == 64 || HI == 32)) {
         // decode-sized batches: the persistent flat schedule (tile counts fit int)
         const int64_t keys = (int64_t)a.max_pages * a.page_size < a.ld ? (int64_t)a.max_pages * a.page_size : a.ld;
-        if (a.T <= kFlatRows && (int64_t)a.T * ((keys + kTileKeys - 1) / kTileKeys) < INT_MAX) {
+        // (the key scales travel by TMA, which wants a 16-byte aligned base)
+        if (a.T <= kFlatRows && (int64_t)a.T * ((keys + kTileKeys - 1) / kTileKeys) < INT_MAX &&
+            (reinterpret_cast<uintptr_t>(a.k_scale) & 15u) == 0) {
             using F = FlatCfg<HI, DI>;
+            CUtensorMap tks; // k_scale as [num_pages, page_size] fp32, one page per box
+            if (!encode_tmap_2d(&tks, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.k_scale, a.page_size, a.num_pages,
+                                (uint64_t)a.page_size * 4, a.page_size, 1, CU_TENSOR_MAP_SWIZZLE_NONE, err, errlen))
+                return DSA_ERR_CUDA;
             static bool flat_attr[64] = {};
             if (dev < 64 && !flat_attr[dev]) {
                 cudaError_t e = cudaFuncSetAttribute(indexer_paged_flat_kernel<HI, DI>,
@@ -977,7 +987,7 @@ int launch_cfg(const IndexerArgs &a, cudaStream_t stream, char *err, size_t errl
             }
             p.splits = 1;
             cudaError_t e = launch_pdl(indexer_paged_flat_kernel<HI, DI>, dim3(2 * num_sms()), dim3(F::THREADS),
-                                       F::SMEM, stream, 1, tq, tk, p);
+                                       F::SMEM, stream, 1, tq, tk, tks, p);
             if (e != cudaSuccess) {
                 snprintf(err, errlen, "indexer launch: %s", cudaGetErrorString(e));
                 return DSA_ERR_CUDA;
