@@ -611,27 +611,38 @@ __device__ bool topk_row_candidates(const float *row, int n, int k, int32_t *out
                                     int *hist, int *scratch, int *sel, int *wc)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t thr = n > kRowCap ? row_threshold<NT>(row, n, k, hist, scratch, sel) : 0u;
     int h = static_cast<int>((4u - ((reinterpret_cast<uintptr_t>(row) >> 2) & 3u)) & 3u);
     h = h < n ? h : n;
-    const int c = row_pass<NT, false>(row, 0, n, h, thr, 0, ck, ci);
-    if (lane == 0)
-        wc[warp] = c;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int tot = 0;
-        for (int w = 0; w < (NT / 32); ++w) {
-            const int x = wc[w];
-            wc[w] = tot;
-            tot += x;
+    int nc, base;
+    if (n <= kRowCap) {
+        // every key is a candidate: warp w's slots start after the keys of the
+        // segments before it (the segment split of row_pass), no counting pass
+        const int seg = (((n - h + (NT / 32) - 1) / (NT / 32)) + 3) & ~3;
+        const int s0 = h + warp * seg < n ? h + warp * seg : n;
+        base = warp == 0 ? 0 : s0;
+        nc = n;
+        row_pass<NT, true>(row, 0, n, h, 0u, base, ck, ci);
+    } else {
+        const uint32_t thr = row_threshold<NT>(row, n, k, hist, scratch, sel);
+        const int c = row_pass<NT, false>(row, 0, n, h, thr, 0, ck, ci);
+        if (lane == 0)
+            wc[warp] = c;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int tot = 0;
+            for (int w = 0; w < (NT / 32); ++w) {
+                const int x = wc[w];
+                wc[w] = tot;
+                tot += x;
+            }
+            wc[(NT / 32)] = tot;
         }
-        wc[(NT / 32)] = tot;
+        __syncthreads();
+        nc = wc[(NT / 32)];
+        if (nc < k || nc > kRowCap)
+            return false;
+        row_pass<NT, true>(row, 0, n, h, thr, wc[warp], ck, ci);
     }
-    __syncthreads();
-    const int nc = wc[(NT / 32)];
-    if (nc < k || nc > kRowCap)
-        return false;
-    row_pass<NT, true>(row, 0, n, h, thr, wc[warp], ck, ci);
     __syncthreads();
     select_candidates<NT>(ck, ci, nc, k, out, hist, scratch, sel);
     return true;
