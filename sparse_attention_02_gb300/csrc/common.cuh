@@ -194,12 +194,6 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32
                  : "memory");
 }
 
-// Prefetch the cache line holding `src` into L2 (an ordinary load-unit instruction).
-__device__ __forceinline__ void prefetch_l2_line(const void *src)
-{
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
-}
-
 // --------------------------------------------------------------- cp.async 16B
 
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src)

@@ -82,7 +82,7 @@ constexpr int kKVAtom = kBN * 128;       // bytes of one KV atom (64 rows x 128 
 constexpr int kKVHalf = kBN * 64;        // bytes of the RoPE half atom (64 rows x 64 B, SW64)
 constexpr int kStage = kVAtoms * kKVAtom + kKVHalf; // 36 KB
 constexpr int kNStage = 4;
-constexpr int kPf = 3;                   // blocks ahead whose rows the producers prefetch into L2
+constexpr int kPf = 3;                   // paged: blocks ahead whose latent rows the producers resolve
 constexpr int kXBuf = 128 * kBN * 2;     // one swap buffer: 128 heads x 64 fp16
 constexpr int kProdWarps = 4;
 constexpr int kPvWarp = kProdWarps;      // all PV MMAs (fixed accumulation order) + TMEM owner
@@ -450,14 +450,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     atomicOr(p.status, DSA_DEV_BAD_PAGE);
                 return r;
             };
-            // Paged (decode): L2 prefetch of this CTA's columns of the rows kPf
-            // blocks ahead, so the stages fill from L2 although the rows come from
-            // HBM.  Five 128-byte lines per row: lanes 0..15 take lines 0..2 of the
-            // V quarter of row q_row0 + (lane & 15), lanes 16..31 line 3 and the
-            // line holding the RoPE half.  (Prefill's latent rows sit in L2.)
-            // The two dependent loads that locate a row (selected position, then
-            // block-table entry) run as a software pipeline one block apart, so
-            // no load result is waited for in the iteration that issued it.
+            // Paged (decode): the two dependent loads that locate a latent row
+            // (selected position, then block-table entry) run as a software
+            // pipeline one block apart, kPf blocks ahead of the gather, so no
+            // load result is waited for in the iteration that issued it.  (An L2
+            // prefetch of the rows kPf blocks ahead measured 2 us slower per
+            // launch at 64 rows and is not issued.)
             auto pf_raw_of = [&](int jj) -> int { // selected position of block jb + jj for this lane's row
                 const int i = (un.jb + jj) * kBN + q_row0 + (lane & 15);
                 return (jj < nb && i < p.k) ? __ldg(idx_row + i) : -1;
@@ -477,23 +475,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 return page * p.page_size + sp % p.page_size;
             };
-            auto prefetch = [&](int row) {
-                if (row >= 0) {
-                    const __nv_bfloat16 *v = kv_cols + (int64_t)row * kD;
-                    if (lane < 16) {
-                        prefetch_l2_line(v);
-                        prefetch_l2_line(v + 64);
-                        prefetch_l2_line(v + 128);
-                    } else {
-                        prefetch_l2_line(v + 192);
-                        prefetch_l2_line(rope_cols + (int64_t)row * kD);
-                    }
-                }
-            };
             // Paged: rw[q] is this lane's latent row of block j + q; the rows of
             // block j + kPf come out of a pipeline whose loads are a block apart
             // (position of block j + kPf + 2, page of block j + kPf + 1 issued
-            // now), get prefetched into L2 and join the ring.
+            // now) and join the ring.
             int rw[kPf];
             int pf_s = -1, pf_page = -1, pf_raw = -1;
             int my_row = -1;
@@ -506,11 +491,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int jj = 0; jj < kPf + 1; ++jj)
                     pg[jj] = pf_page_of(sp[jj]);
 #pragma unroll
-                for (int jj = 0; jj < kPf; ++jj) {
+                for (int jj = 0; jj < kPf; ++jj)
                     rw[jj] = pf_row_of(sp[jj], pg[jj]);
-                    if (jj > 0)
-                        prefetch(rw[jj]);
-                }
                 pf_s = sp[kPf];
                 pf_page = pg[kPf];
                 pf_raw = sp[kPf + 1];
@@ -526,7 +508,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     for (int q = 0; q + 1 < kPf; ++q)
                         rw[q] = rw[q + 1];
                     rw[kPf - 1] = pf_row_of(pf_s, pf_page); // block j + kPf
-                    prefetch(rw[kPf - 1]);
                     pf_s = pf_raw;                          // block j + kPf + 1: its page
                     pf_page = pf_page_of(pf_raw);
                     pf_raw = pf_raw_of(j + kPf + 2);        // block j + kPf + 2: its position
