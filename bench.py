@@ -162,7 +162,10 @@ def oracle_sample(cfg: W.Config, rows: np.ndarray, x):
     import oracle
 
     n = int(rows.max()) + 1
-    r = torch.as_tensor(rows, device=x["q"].device)
+    pos = x["q_pos"].cpu().numpy()  # positions of x's query rows (all L, or a subset)
+    at = np.searchsorted(pos, rows)
+    assert np.array_equal(pos[at], rows), "sampled rows missing from the inputs"
+    r = torch.as_tensor(at, device=x["q"].device)
     h = {"q8": x["q8"][r].cpu(), "qs": x["qs"][r].cpu(), "w": x["w"][r].cpu(), "q": x["q"][r].cpu(),
          "k8": x["k8"][:n].cpu(), "ks": x["ks"][:n].cpu(), "kv": x["kv"][:n].cpu()}
     rows = np.asarray(rows)
@@ -192,14 +195,18 @@ def oracle_full_estimate(rates, L, k):
 def cpu_baseline(cfg, x, rows=None):
     L = cfg.L
     if rows is None:
+        # ~10-15 s of fp64 work on 16 cores: fixed rows around the k boundary and both
+        # ends, plus rows drawn uniformly over the whole prefill
         rng = np.random.default_rng(7)
-        rows = np.unique(np.concatenate([[0, 1, 255, 1023, 2047, 2048, 3071, 4095], rng.integers(0, 4096, 8)]))
+        fixed = [r for r in (0, 1, 255, 1023, 2047, 2048, 3071, 4095, L // 2 - 1, L - 1) if r < L]
+        rows = np.unique(np.concatenate([fixed, rng.integers(0, L, 126)]))
     rates = oracle_sample(cfg, np.asarray(rows), x)
     est = oracle_full_estimate(rates, L, cfg.k)
     return {"value": L / est, "unit": "tokens/s", "cores": rates["cores"], "kind": "oracle",
-            "sample": (f"{rates['rows']} query rows of the L={L} prefill (positions < 4096, all of their keys "
-                       f"and selections), {rates['wall_s']:.1f} s of CPU work; per-unit rates extrapolated "
-                       f"to all {L} rows (indexer and top-k per key-row, attention per selected pair)"),
+            "sample": (f"{rates['rows']} query rows of the L={L} prefill (ten fixed positions, the rest uniform "
+                       f"over [0, {L}); all of their keys and selections), {rates['wall_s']:.1f} s of CPU work; "
+                       f"per-unit rates extrapolated to all {L} rows (indexer and top-k per key-row, attention "
+                       f"per selected pair)"),
             "extrapolated_seconds_per_step": est}
 
 
@@ -210,10 +217,16 @@ def run_reference(args, rank, world):
     cfg = W.CONFIGS[args.workload]
     L = cfg.L
     rng = np.random.default_rng(11)
-    x = W.prefill_inputs(cfg, "cpu", L=1024)  # the first 1024 rows of the workload's shapes
+    # a pool of query rows spread over the whole prefill: every row of eight of the
+    # input generator's query chunks, evenly spaced (the keys are drawn in full)
+    per = max(1, W._CHUNK_ELEMS // (cfg.H * cfg.D))
+    nchunk = (L + per - 1) // per
+    chunks = np.unique(np.linspace(0, nchunk - 1, min(8, nchunk)).round().astype(np.int64))
+    pool = np.concatenate([np.arange(c * per, min(L, (c + 1) * per)) for c in chunks])
+    x = W.prefill_rows(cfg, "cpu", pool)
 
     def step(i):
-        rows = np.unique(rng.integers(0, 1024, 8))
+        rows = np.sort(rng.choice(pool, size=min(48, len(pool)), replace=False))
         return oracle_sample(cfg, rows, x)
 
     for i in range(args.warmup):
@@ -233,7 +246,8 @@ def run_reference(args, rank, world):
             "config": {"workload": f"{args.workload}: L={L} causal, k={cfg.k}, H_I={cfg.HI}, d_I={cfg.dI}, H={cfg.H}, "
                                    "D=576, Dv=512", "l2": "n/a (CPU)"},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                             "sample": f"each step: 8 query rows at positions < 1024 (all keys and selections); "
+                             "sample": f"each step: 48 distinct query rows drawn from {len(pool)} rows spread over all {L} "
+                                       f"positions (all keys and selections); "
                                        f"per-unit rates extrapolated to the full {L}-row prefill; median over "
                                        f"{args.steps} steps ({statistics.mean(walls):.2f} s CPU wall per step)"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

@@ -88,6 +88,25 @@ def randn(shape, device, seed: int, tid: int, std: float = 1.0, dtype=torch.floa
     return out
 
 
+def randn_rows(shape, rows, device, seed: int, tid: int, std: float = 1.0, dtype=torch.float32) -> torch.Tensor:
+    """Rows ``rows`` (ascending) of ``randn(shape, ...)``, drawing only the chunks that hold them."""
+    shape = tuple(int(s) for s in shape)
+    rows = torch.as_tensor(rows, dtype=torch.int64)
+    row = int(math.prod(shape[1:]))
+    rows_per = max(1, _CHUNK_ELEMS // max(row, 1))
+    out = torch.empty((len(rows), row), dtype=dtype, device=device)
+    chunk_of = rows // rows_per
+    for c in torch.unique(chunk_of).tolist():
+        r0 = c * rows_per
+        r1 = min(shape[0], r0 + rows_per)
+        x = torch.randn((r1 - r0, row), generator=_gen(device, seed, tid, c), device=device)
+        if std != 1.0:
+            x.mul_(std)
+        sel = (chunk_of == c).nonzero().flatten()
+        out[sel.to(device)] = x[(rows[sel] - r0).to(device)].to(dtype)
+    return out.view((len(rows),) + shape[1:])
+
+
 def quantize_fp8_per_token(x: torch.Tensor):
     """Fixture quantiser: one scale per leading index over all trailing elements.
 
@@ -134,6 +153,23 @@ def prefill_inputs(cfg: Config, device, L: int | None = None, seed: int | None =
     q = randn((L, cfg.H, cfg.D), device, seed, 20, dtype=torch.bfloat16)
     kv = randn((L, cfg.D), device, seed, 21, dtype=torch.bfloat16)
     q_pos = torch.arange(L, dtype=torch.int32, device=device)
+    return dict(q8=q8, qs=qs, w=w, k8=k8, ks=ks, q=q, kv=kv, q_pos=q_pos)
+
+
+def prefill_rows(cfg: Config, device, rows, seed: int | None = None):
+    """The query rows ``rows`` (ascending positions) of ``prefill_inputs(cfg)`` with all
+    of the keys: the same bytes, without drawing the query chunks no row falls in."""
+    seed = cfg.seed if seed is None else seed
+    rows = torch.as_tensor(rows, dtype=torch.int64)
+    L = cfg.L
+    qI = randn_rows((L, cfg.HI, cfg.dI), rows, device, seed, 10)
+    q8, qs = quantize_fp8_per_token(qI)
+    del qI
+    w = randn_rows((L, cfg.HI), rows, device, seed, 11, std=cfg.w_std)
+    k8, ks = indexer_keys(cfg, L, device, seed)
+    q = randn_rows((L, cfg.H, cfg.D), rows, device, seed, 20, dtype=torch.bfloat16)
+    kv = randn((L, cfg.D), device, seed, 21, dtype=torch.bfloat16)
+    q_pos = rows.to(torch.int32).to(device)
     return dict(q8=q8, qs=qs, w=w, k8=k8, ks=ks, q=q, kv=kv, q_pos=q_pos)
 
 

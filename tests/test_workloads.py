@@ -54,3 +54,17 @@ def test_decode_layout_pool_is_a_permutation():
             assert torch.isnan(d["kv_pool"][page, c % 64:].float()).all()
             assert torch.isnan(d["ks_pool"][page, c % 64:]).all()
             assert torch.isfinite(d["kv_pool"][page, : c % 64].float()).all()
+
+
+def test_prefill_rows_match_the_full_draw(monkeypatch):
+    """prefill_rows gives the bytes of prefill_inputs at the chosen rows, also when the
+    rows fall in several generator chunks (chunk size shrunk so that they do)."""
+    monkeypatch.setattr(W, "_CHUNK_ELEMS", 1 << 14)
+    cfg = W.CONFIGS["tiny"]
+    full = W.prefill_inputs(cfg, "cpu")
+    rows = np.array([0, 3, 70, 71, 128, 200, 255])
+    part = W.prefill_rows(cfg, "cpu", rows)
+    for key in ("q8", "qs", "w", "q", "q_pos"):
+        assert torch.equal(part[key], full[key][rows]), key
+    for key in ("k8", "ks", "kv"):
+        assert torch.equal(part[key], full[key]), key
