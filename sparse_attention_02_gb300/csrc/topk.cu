@@ -25,7 +25,7 @@
 // draws the same samples and gets the same value; shorter rows use none);
 // (2) CTA c streams its own 1/cs of the row once, kUnroll 16-byte loads per
 // lane in flight, and keeps every key at or above the threshold: warp w scans
-// a contiguous segment and appends (key, index) to its own region of shared
+// a contiguous segment and appends (score bits, index) to its own region of shared
 // memory with ballot prefix counts, so the regions taken in warp order list
 // the CTA's candidates in index order; (3) each CTA pushes its candidates,
 // in order, into CTA 0's list through distributed shared memory; (4) CTA 0
@@ -53,12 +53,21 @@ constexpr int kUnroll = 8;              // 16-byte loads per lane in flight in t
 // candidate keys and indices (own, then gathered), histogram
 constexpr int kSmemTopk = (2 * kCand + 2 * kGather + 4096) * 4;
 
-__device__ __forceinline__ uint32_t order_key(float x)
+__device__ __forceinline__ uint32_t order_key_bits(uint32_t u)
 {
-    uint32_t u = __float_as_uint(x);
     if (u == 0x80000000u)
         u = 0u; // -0 ties with +0
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ uint32_t order_key(float x) { return order_key_bits(__float_as_uint(x)); }
+
+// The float whose key is `key` (order_key's inverse; -0 for the key between
+// the negatives and +0).  For finite x, order_key(x) >= key  <=>  x >= key_float(key),
+// so the filters below compare floats and form keys only for the keys they keep.
+__device__ __forceinline__ float key_float(uint32_t key)
+{
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
 // Exclusive prefix sum over the block in thread order; returns the prefix and
@@ -275,14 +284,15 @@ __device__ void topk_row(const float *row, int n, int k, int32_t *out, int *hist
             break; // block-uniform: every kept index has been written
     }
 }
-// Keeps the keys >= thr of row[c0, c1) in index order.  The first `head`
-// keys (row + c0 + head is 16-byte aligned) go through warp 0 one per lane;
+// Keeps the keys >= thr (kAll: every key) of row[c0, c1) in index order,
+// comparing floats (key_float) and forming keys only for the kept ones.  The
+// first `head` keys (row + c0 + head is 16-byte aligned) go through warp 0 one per lane;
 // then warp w scans its own contiguous segment of the rest, kUnroll 16-byte
-// loads per lane in flight.  Keys are appended with (key, index) to the warp's
+// loads per lane in flight.  Keys are appended as (score bits, index) to the warp's
 // region ck/ci[w * kSeg, +kSeg) with ballot prefix counts.  Leaves in wc[w]
 // the offset of warp w's region in the CTA's flat candidate list and in
 // wc[kWarps] the CTA's count, or -1 if a region overflowed.
-template <int NT>
+template <int NT, bool kAll>
 __device__ void filter_segment(const float *row, int c0, int c1, int head, uint32_t thr, uint32_t *ck, int32_t *ci,
                                int *wc)
 {
@@ -294,33 +304,34 @@ __device__ void filter_segment(const float *row, int c0, int c1, int head, uint3
     const int s1 = s0 + seg < c1 ? s0 + seg : c1;
     uint32_t *wk = ck + warp * kSeg;
     int32_t *wi = ci + warp * kSeg;
+    const float thr_f = key_float(thr);
     int cnt = 0; // warp-uniform
     if (warp == 0 && head > 0) {
         const int i = c0 + lane;
-        const uint32_t key = lane < head ? order_key(__ldg(row + i)) : 0u;
-        const bool f = lane < head && key >= thr;
+        const float x = lane < head ? __ldg(row + i) : 0.f;
+        const bool f = lane < head && (kAll || x >= thr_f);
         const unsigned m = __ballot_sync(0xffffffffu, f);
         if (f) {
-            wk[__popc(m & lt)] = key;
+            wk[__popc(m & lt)] = __float_as_uint(x);
             wi[__popc(m & lt)] = i;
         }
         cnt = __popc(m);
     }
     for (int base = s0; base < s1; base += 128 * kUnroll) {
-        uint32_t kk[kUnroll][4];
+        float xx[kUnroll][4];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int i = base + 128 * u + 4 * lane;
             if (i + 3 < s1) {
                 const float4 v = __ldg(reinterpret_cast<const float4 *>(row + i));
-                kk[u][0] = order_key(v.x);
-                kk[u][1] = order_key(v.y);
-                kk[u][2] = order_key(v.z);
-                kk[u][3] = order_key(v.w);
+                xx[u][0] = v.x;
+                xx[u][1] = v.y;
+                xx[u][2] = v.z;
+                xx[u][3] = v.w;
             } else {
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    kk[u][e] = i + e < s1 ? order_key(__ldg(row + i + e)) : 0u;
+                    xx[u][e] = i + e < s1 ? __ldg(row + i + e) : 0.f;
             }
         }
 #pragma unroll
@@ -330,7 +341,7 @@ __device__ void filter_segment(const float *row, int c0, int c1, int head, uint3
             int pre = 0, tot = 0;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                f[e] = i + e < s1 && kk[u][e] >= thr;
+                f[e] = i + e < s1 && (kAll || xx[u][e] >= thr_f);
                 const unsigned m = __ballot_sync(0xffffffffu, f[e]);
                 pre += __popc(m & lt);
                 tot += __popc(m);
@@ -340,7 +351,7 @@ __device__ void filter_segment(const float *row, int c0, int c1, int head, uint3
             for (int e = 0; e < 4; ++e) {
                 if (f[e]) {
                     if (slot < kSeg) {
-                        wk[slot] = kk[u][e];
+                        wk[slot] = __float_as_uint(xx[u][e]);
                         wi[slot] = i + e;
                     }
                     ++slot;
@@ -375,19 +386,20 @@ __device__ __forceinline__ int cand_slot(const int *wc, int f)
     return w * kSeg + (f - wc[w]);
 }
 
-// Exact top-k of nc >= k candidates ck/ci listed in ascending index order;
-// writes the kept indices to out in that order.
+// Exact top-k of nc >= k candidates ck/ci listed in ascending index order (ck
+// holds the raw fp32 score bits; the keys are formed as they are read); writes
+// the kept indices to out in that order.
 template <int NT>
 __device__ void select_candidates(const uint32_t *ck, const int32_t *ci, int nc, int k, int32_t *out, int *hist,
                                   int *scratch, int *sel)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Radix select on d = key - kmin: the candidates span a narrow key range,
-    // so passes of at most 12 bits over d spread close scores over the bins
+    // so passes of at most 10 bits over d spread close scores over the bins
     // instead of piling them into a few bins of the raw top digit.
     uint32_t lo = 0xFFFFFFFFu, hi = 0u;
     for (int f = threadIdx.x; f < nc; f += NT) {
-        const uint32_t key = ck[f];
+        const uint32_t key = order_key_bits(ck[f]);
         lo = key < lo ? key : lo;
         hi = key > hi ? key : hi;
     }
@@ -411,8 +423,8 @@ __device__ void select_candidates(const uint32_t *ck, const int32_t *ci, int nc,
     __syncthreads();
     const uint32_t range = kmax - kmin;
     const int bits = range == 0u ? 0 : 32 - __clz(range); // d has `bits` significant bits
-    int shift = bits > 12 ? bits - 12 : 0;  // this pass sorts d into bins of d >> shift ...
-    int nbins = 1 << (bits - shift);        // ... of which there are nbins (at most 4096)
+    int shift = bits > 10 ? bits - 10 : 0;  // this pass sorts d into bins of d >> shift ...
+    int nbins = 1 << (bits - shift);        // ... of which there are nbins (at most 1024)
     int prev = 32;                          // bits of d at and above `prev` are fixed to `prefix`
     uint32_t prefix = 0u;
     int k_rem = k;
@@ -421,7 +433,7 @@ __device__ void select_candidates(const uint32_t *ck, const int32_t *ci, int nc,
             hist[q] = 0;
         __syncthreads();
         for (int f = threadIdx.x; f < nc; f += NT) {
-            const uint32_t d = ck[f] - kmin;
+            const uint32_t d = order_key_bits(ck[f]) - kmin;
             if (prev == 32 || (d >> prev) == prefix)
                 atomicAdd(&hist[(d >> shift) & static_cast<uint32_t>(nbins - 1)], 1);
         }
@@ -434,7 +446,7 @@ __device__ void select_candidates(const uint32_t *ck, const int32_t *ci, int nc,
         if (shift == 0)
             break;
         prev = shift;
-        shift = shift > 12 ? shift - 12 : 0;
+        shift = shift > 10 ? shift - 10 : 0;
         nbins = 1 << (prev - shift);
     }
     const uint32_t tau = kmin + prefix; // every bit of d fixed: the k-th largest candidate key
@@ -445,7 +457,7 @@ __device__ void select_candidates(const uint32_t *ck, const int32_t *ci, int nc,
     const int f1 = f0 + per < nc ? f0 + per : nc;
     int gt = 0, eq = 0;
     for (int f = f0; f < f1; ++f) {
-        const uint32_t key = ck[f];
+        const uint32_t key = order_key_bits(ck[f]);
         gt += key > tau;
         eq += key == tau;
     }
@@ -453,7 +465,7 @@ __device__ void select_candidates(const uint32_t *ck, const int32_t *ci, int nc,
     const int pre = block_exclusive_scan<NT>((gt << 16) | eq, scratch, &total);
     int g_before = pre >> 16, e_before = pre & 0xFFFF;
     for (int f = f0; f < f1; ++f) {
-        const uint32_t key = ck[f];
+        const uint32_t key = order_key_bits(ck[f]);
         if (key > tau) {
             out[g_before + (e_before < need_eq ? e_before : need_eq)] = ci[f];
             ++g_before;
@@ -475,7 +487,7 @@ __device__ void select_candidates(const uint32_t *ck, const int32_t *ci, int nc,
 //     ~ (1.25 k + 256) / n from the top.  (2) A counting pass over the row
 //     (warp w scans its own contiguous segment, ballot counts) and a block
 //     scan place every warp's keys at or above the threshold; a second pass
-//     (L1/L2 hits) writes (key, index) there, so the list is in index order.
+//     (L1/L2 hits) writes (score bits, index) there, so the list is in index order.
 //     (3) The exact radix select over those candidates and the ordered
 //     compaction of select_candidates.  A row whose count misses [k, kRowCap]
 //     takes the four passes instead; the result is the same.
@@ -534,73 +546,84 @@ __device__ uint32_t row_threshold(const float *row, int n, int k, int *hist, int
 
 // One pass over warp w's segment of row[c0 + head, c1) (16-byte aligned from
 // there; the `head` keys before it go to warp 0 first): counts the keys >= thr
-// (kWrite = false), or writes them as (key, index) from slot base on (kWrite).
-// Returns the warp's count (warp-uniform).
-template <int NT, bool kWrite>
+// (kWrite = false), or writes them as (score bits, index) from slot base on (kWrite;
+// kAll: every key, no compare).  Returns the warp's count (warp-uniform).
+template <int NT, bool kWrite, bool kAll = false>
 __device__ int row_pass(const float *row, int c0, int c1, int head, uint32_t thr, int base, uint32_t *ck,
                         int32_t *ci)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t lt = (1u << lane) - 1u;
+    const float thr_f = key_float(thr);
     const int v0 = c0 + head;
     const int seg = (((c1 - v0 + (NT / 32) - 1) / (NT / 32)) + 3) & ~3;
     const int s0 = v0 + warp * seg < c1 ? v0 + warp * seg : c1;
     const int s1 = s0 + seg < c1 ? s0 + seg : c1;
-    int cnt = 0;
+    int cnt = 0;  // kWrite: the warp's count so far; else this lane's
     if (warp == 0 && head > 0) {
         const int i = c0 + lane;
-        const uint32_t key = lane < head ? order_key(__ldg(row + i)) : 0u;
-        const bool f = lane < head && key >= thr;
-        const unsigned m = __ballot_sync(0xffffffffu, f);
-        if (kWrite && f) {
-            ck[base + __popc(m & lt)] = key;
-            ci[base + __popc(m & lt)] = i;
+        const float x = lane < head ? __ldg(row + i) : 0.f;
+        const bool f = lane < head && (kAll || x >= thr_f);
+        if (kWrite) {
+            const unsigned m = __ballot_sync(0xffffffffu, f);
+            if (f) {
+                ck[base + __popc(m & lt)] = __float_as_uint(x);
+                ci[base + __popc(m & lt)] = i;
+            }
+            cnt = __popc(m);
+        } else {
+            cnt = f ? 1 : 0;
         }
-        cnt = __popc(m);
     }
     for (int b0 = s0; b0 < s1; b0 += 128 * kUnroll) {
-        uint32_t kk[kUnroll][4];
+        float xx[kUnroll][4];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int i = b0 + 128 * u + 4 * lane;
             if (i + 3 < s1) {
                 const float4 v = __ldg(reinterpret_cast<const float4 *>(row + i));
-                kk[u][0] = order_key(v.x);
-                kk[u][1] = order_key(v.y);
-                kk[u][2] = order_key(v.z);
-                kk[u][3] = order_key(v.w);
+                xx[u][0] = v.x;
+                xx[u][1] = v.y;
+                xx[u][2] = v.z;
+                xx[u][3] = v.w;
             } else {
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    kk[u][e] = i + e < s1 ? order_key(__ldg(row + i + e)) : 0u;
+                    xx[u][e] = i + e < s1 ? __ldg(row + i + e) : 0.f;
             }
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int i = b0 + 128 * u + 4 * lane;
             bool f[4];
-            int pre = 0, tot = 0;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                f[e] = i + e < s1 && kk[u][e] >= thr;
-                const unsigned m = __ballot_sync(0xffffffffu, f[e]);
-                pre += __popc(m & lt);
-                tot += __popc(m);
-            }
+            for (int e = 0; e < 4; ++e)
+                f[e] = i + e < s1 && (kAll || xx[u][e] >= thr_f);
             if (kWrite) {
+                int pre = 0, tot = 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const unsigned m = __ballot_sync(0xffffffffu, f[e]);
+                    pre += __popc(m & lt);
+                    tot += __popc(m);
+                }
                 int slot = base + cnt + pre;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     if (f[e]) {
-                        ck[slot] = kk[u][e];
+                        ck[slot] = __float_as_uint(xx[u][e]);
                         ci[slot] = i + e;
                         ++slot;
                     }
                 }
+                cnt += tot;
+            } else {
+                cnt += (f[0] ? 1 : 0) + (f[1] ? 1 : 0) + (f[2] ? 1 : 0) + (f[3] ? 1 : 0);
             }
-            cnt += tot;
         }
     }
+    if (!kWrite)
+        cnt = __reduce_add_sync(0xffffffffu, cnt);
     return cnt;
 }
 
@@ -621,7 +644,7 @@ __device__ bool topk_row_candidates(const float *row, int n, int k, int32_t *out
         const int s0 = h + warp * seg < n ? h + warp * seg : n;
         base = warp == 0 ? 0 : s0;
         nc = n;
-        row_pass<NT, true>(row, 0, n, h, 0u, base, ck, ci);
+        row_pass<NT, true, true>(row, 0, n, h, 0u, base, ck, ci);
     } else {
         const uint32_t thr = row_threshold<NT>(row, n, k, hist, scratch, sel);
         const int c = row_pass<NT, false>(row, 0, n, h, thr, 0, ck, ci);
@@ -737,7 +760,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int chunk = ((n - h + cs - 1) / cs + 3) & ~3;
         const int c0 = cr == 0 ? 0 : (h + cr * chunk < n ? h + cr * chunk : n);
         const int c1 = h + (cr + 1) * chunk < n ? h + (cr + 1) * chunk : n;
-        filter_segment<kThreads>(r, c0, c1, cr == 0 ? h : 0, thr, lkey, lidx, wc);
+        if (thr == 0u) // rows that fit the gathered list: every key is a candidate
+            filter_segment<kThreads, true>(r, c0, c1, cr == 0 ? h : 0, thr, lkey, lidx, wc);
+        else
+            filter_segment<kThreads, false>(r, c0, c1, cr == 0 ? h : 0, thr, lkey, lidx, wc);
         cluster_sync_all(); // every CTA's count is in its wc[kWarps]
         if (threadIdx.x == 0) {
             int off = 0, tot = 0;

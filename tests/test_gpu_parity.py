@@ -58,7 +58,7 @@ def test_topk_from_gpu_logits_bit_exact():
 # At most two rows per SM run on the cluster kernel (one cluster per row), more rows on
 # the one-CTA-per-row kernel; tiling the same rows REPS_MANY_ROWS times (more than 304
 # rows) sends them through the latter.  Both fall back to the four histogram passes for
-# rows whose candidates overflow (the all-ties row below).
+# rows whose candidates miss [k, cap] (the all-ties row below, the planted rows after it).
 REPS_MANY_ROWS = 40
 
 
@@ -105,6 +105,34 @@ def test_topk_deterministic_large_row(reps):
     assert torch.equal(a, b)
     ref = oracle.topk(vals.cpu().double().numpy(), n.cpu().numpy(), 2048)
     assert np.array_equal(a.cpu().numpy(), np.tile(ref, (reps, 1)))
+
+
+@pytest.mark.parametrize("k", [1000, 2048, 2049])
+def test_topk_many_rows_planted_and_ties(k):
+    """More rows than two per SM.  Rows 0-1 hold scores that grow along the row with the
+    row's largest scores planted at 512 evenly spaced positions, so a sampled threshold can
+    miss the k-th key (those rows then take the four histogram passes); row 2 is integer
+    ties, the rest random; unaligned rows; k below, at and above the workload's 2048."""
+    dsa = lib()
+    g = torch.Generator(device=DEV).manual_seed(9)
+    ld = 32771
+    n = torch.tensor([ld, 32768, 20000, 9000, 5000, 3500, 3073, ld - 2], dtype=torch.int32)
+    vals = torch.randn((len(n), ld), generator=g, device=DEV)
+    for r in (0, 1):
+        nr = int(n[r])
+        vals[r, :nr] = torch.arange(nr, device=DEV, dtype=torch.float32) * 1e-3
+        pos = (torch.arange(512, device=DEV, dtype=torch.int64) * nr) // 512
+        vals[r, pos] = 1e6 + torch.arange(512, device=DEV, dtype=torch.float32)
+    vals[2] = torch.randint(-8, 9, (ld,), generator=g, device=DEV).float()
+    for r in range(len(n)):
+        vals[r, int(n[r]):] = float("nan")
+    reps = REPS_MANY_ROWS
+    idx = torch.empty((len(n) * reps, k), dtype=torch.int32, device=DEV)
+    dsa.dsa_topk(vals.repeat(reps, 1), n.repeat(reps).to(DEV), k, idx)
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_device_status() == 0
+    ref = oracle.topk(np.nan_to_num(vals.cpu().double().numpy(), nan=-np.inf), n.numpy(), k)
+    assert np.array_equal(idx.cpu().numpy(), np.tile(ref, (reps, 1)))
 
 
 def _mla_case(T, S, H, k, seed, invalid_frac=0.0, rows=None):
