@@ -37,6 +37,7 @@ METRIC = "DSA tokens/s at L=32K,k=2048 (prefill) and decode; % of FP8/BF16/HBM r
 WORKLOAD = "prefill_32k"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+NOMINAL = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0, "fp8_tflops": 4500.0}  # GB300 datasheet, dense
 PROFILES = os.path.join(ROOT, "profiles")
 
 
@@ -319,7 +320,8 @@ def quantize_bench(dsa, cfg, steps, warmup, flush, hbm, dev):
     ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
     nbytes = 5.0 * (xq.numel() + xk.numel()) + 8.0 * L
     gbs = nbytes / (ms / 1e3) / 1e9
-    return {"ms": ms, "gbs": gbs, "bound": "hbm", "peak": hbm, "frac": gbs / hbm, "bytes": nbytes,
+    return {"ms": ms, "gbs": gbs, "bound": "hbm", "peak": hbm, "frac": gbs / hbm,
+            "frac_nominal": gbs / NOMINAL["hbm_gbs"], "bytes": nbytes,
             "in_step": False, "mode": "amax/448",
             "what": f"q^I [{L},{cfg.HI},{cfg.dI}] and k^I [{L},{cfg.dI}] fp32 -> E4M3 codes + per-token scales"}
 
@@ -386,7 +388,8 @@ def decode_bench(dsa, steps, warmup, flush, peaks, dev):
                              "timed over whole steps",
             "algorithmic_bytes": float(total),
             "hbm": {"achieved_gbs": total / (ms / 1e3) / 1e9, "peak_gbs": hbm,
-                    "frac": total / (ms / 1e3) / 1e9 / hbm},
+                    "frac": total / (ms / 1e3) / 1e9 / hbm,
+                    "frac_nominal": total / (ms / 1e3) / 1e9 / NOMINAL["hbm_gbs"]},
             "stage_hbm_frac": {"indexer": (key_bytes + ctx.sum() * 4 + q_bytes) / (st[0] / 1e3) / 1e9 / hbm,
                                "topk": (ctx.sum() * 4 + B * cfg.k * 4) / (st[1] / 1e3) / 1e9 / hbm,
                                "sparse_mla": attn_bytes / (st[2] / 1e3) / 1e9 / hbm}}
@@ -524,18 +527,22 @@ def main():
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "kernel": "sparse_mla_prefill", "achieved": mla_tflops,
                      "peak": bf16_peak, "unit": "TFLOP/s", "frac": mla_tflops / bf16_peak,
+                     "frac_nominal": mla_tflops / NOMINAL["bf16_tflops"],
                      "traffic": traffic,
                      "peak_source": f"{peaks_src} bf16 sustained (kernel timed inside the step)",
                      "algorithmic_flop_per_launch": work["mla_flop"]},
         "stages": {
             "indexer": {"ms": float(stage_ms[0]), "tflops": idx_tflops, "bound": "tensor (fp8)",
                         "peak": fp8_peak, "frac": idx_tflops / fp8_peak,
+                        "frac_nominal": idx_tflops / NOMINAL["fp8_tflops"],
                         "peak_source": f"{peaks_src} bf16 sustained x {FP8_OVER_BF16} (nominal fp8/bf16 ratio)",
                         "flop": work["indexer_flop"], "tokens_per_s": L / (stage_ms[0] / 1e3)},
             "topk": {"ms": float(stage_ms[1]), "gbs": topk_gbs, "bound": "hbm", "peak": hbm,
-                     "frac": topk_gbs / hbm, "bytes": work["topk_bytes"], "tokens_per_s": L / (stage_ms[1] / 1e3)},
+                     "frac": topk_gbs / hbm, "frac_nominal": topk_gbs / NOMINAL["hbm_gbs"], "bytes": work["topk_bytes"],
+                     "tokens_per_s": L / (stage_ms[1] / 1e3)},
             "sparse_mla": {"ms": float(stage_ms[2]), "tflops": mla_tflops, "bound": "tensor (bf16)",
-                           "peak": bf16_peak, "frac": mla_tflops / bf16_peak, "flop": work["mla_flop"],
+                           "peak": bf16_peak, "frac": mla_tflops / bf16_peak,
+                           "frac_nominal": mla_tflops / NOMINAL["bf16_tflops"], "flop": work["mla_flop"],
                            "tokens_per_s": L / (stage_ms[2] / 1e3)},
         },
         "clocks": clk,
