@@ -90,8 +90,9 @@ struct IdxCfg {
 
 // In the fragment epilogue every kAbsEvery-th column repeat forms ReLU(x) * w
 // as (x + |x|) * (w / 2), which is the same rounded product and FMA, on the FMA
-// pipe instead of the ALU pipe that carries the max of the other repeats.
-constexpr int kAbsEvery = 4;
+// pipe instead of the ALU pipe that carries the max of the other repeats
+// (L = 32768: every 3rd or 4th 5.21 ms, 5th 5.13, 6th 5.04-5.06, 8th 5.12).
+constexpr int kAbsEvery = 6;
 
 struct Params {
     const float *q_scale;
