@@ -59,14 +59,13 @@ struct IdxCfg {
     static constexpr int NC = N / EPI_SPLIT;
     static constexpr int TPT = NC / HI;
     // fragment epilogue: lane halves per warp, columns per warp, 8-column
-    // repeats per warp, tokens per warp, repeats per token, 64-column chunks
+    // repeats per warp, tokens per warp, repeats per token, repeats per 64-column chunk
     static constexpr int NLH = EPI_SPLIT >= 2 ? 1 : 2;
     static constexpr int NCW = N / (EPI_SPLIT >= 2 ? EPI_SPLIT / 2 : 1);
     static constexpr int REPS = NCW / 8;
     static constexpr int TPW = NCW / HI;
     static constexpr int RPT = HI / 8;
     static constexpr int CHUNK_REPS = REPS >= 8 ? 8 : REPS;
-    static constexpr int NCHUNK = REPS / CHUNK_REPS;
     static constexpr int QTILE = N * DI;                  // bytes
     static constexpr int KSTAGE = kTileKeys * DI;         // bytes
     static constexpr int ACC_COLS = N < 32 ? 32 : N;
