@@ -391,9 +391,17 @@ __device__ __forceinline__ int cand_slot(const int *wc, int f)
 // the kept indices to out in that order.
 template <int NT>
 __device__ void select_candidates(const uint32_t *ck, const int32_t *ci, int nc, int k, int32_t *out, int *hist,
-                                  int *scratch, int *sel)
+                                  int *sel)
 {
+    constexpr int NW = NT / 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // hist: two 1024-bin histograms that alternate between passes (the next one
+    // is cleared while warp 0 picks the bin in the current one), then the
+    // per-warp totals of the ordered output and the per-warp minima and maxima.
+    int *wsum = hist + 2048;
+    int *mm = hist + 2048 + NW;
+    for (int q = threadIdx.x; q < 1024; q += NT)
+        hist[q] = 0;
     // Radix select on d = key - kmin: the candidates span a narrow key range,
     // so passes of at most 10 bits over d spread close scores over the bins
     // instead of piling them into a few bins of the raw top digit.
@@ -410,17 +418,17 @@ __device__ void select_candidates(const uint32_t *ck, const int32_t *ci, int nc,
         hi = h2 > hi ? h2 : hi;
     }
     if (lane == 0) {
-        hist[2 * warp] = static_cast<int>(lo);
-        hist[2 * warp + 1] = static_cast<int>(hi);
+        mm[2 * warp] = static_cast<int>(lo);
+        mm[2 * warp + 1] = static_cast<int>(hi);
     }
     __syncthreads();
     uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-    for (int w = 0; w < (NT / 32); ++w) {
-        const uint32_t l2 = static_cast<uint32_t>(hist[2 * w]), h2 = static_cast<uint32_t>(hist[2 * w + 1]);
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        const uint32_t l2 = static_cast<uint32_t>(mm[2 * w]), h2 = static_cast<uint32_t>(mm[2 * w + 1]);
         kmin = l2 < kmin ? l2 : kmin;
         kmax = h2 > kmax ? h2 : kmax;
     }
-    __syncthreads();
     const uint32_t range = kmax - kmin;
     const int bits = range == 0u ? 0 : 32 - __clz(range); // d has `bits` significant bits
     int shift = bits > 10 ? bits - 10 : 0;  // this pass sorts d into bins of d >> shift ...
@@ -428,20 +436,53 @@ __device__ void select_candidates(const uint32_t *ck, const int32_t *ci, int nc,
     int prev = 32;                          // bits of d at and above `prev` are fixed to `prefix`
     uint32_t prefix = 0u;
     int k_rem = k;
-    for (;;) {
-        for (int q = threadIdx.x; q < nbins; q += NT)
-            hist[q] = 0;
-        __syncthreads();
+    for (int pass = 0;; ++pass) {
+        int *cur = hist + 1024 * (pass & 1);
+        int *nxt = hist + 1024 * ((pass & 1) ^ 1);
         for (int f = threadIdx.x; f < nc; f += NT) {
             const uint32_t d = order_key_bits(ck[f]) - kmin;
             if (prev == 32 || (d >> prev) == prefix)
-                atomicAdd(&hist[(d >> shift) & static_cast<uint32_t>(nbins - 1)], 1);
+                atomicAdd(&cur[(d >> shift) & static_cast<uint32_t>(nbins - 1)], 1);
         }
         __syncthreads();
-        select_bin<NT>(hist, nbins, k_rem, scratch, sel);
+        if (warp == 0) {
+            // the bin with (keys above it) < k_rem <= (keys at or above it); lane l
+            // reads bins 32 l .. 32 l + 31 (bins past nbins are empty)
+            const int4 *b4 = reinterpret_cast<const int4 *>(cur + 32 * lane);
+            int sum = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int4 v = b4[q];
+                sum += v.x + v.y + v.z + v.w;
+            }
+            int incl = sum; // keys in the bins of this lane and of the lanes above it
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_down_sync(0xffffffffu, incl, o);
+                if (lane + o < 32)
+                    incl += y;
+            }
+            const int excl = incl - sum;
+            const unsigned m = __ballot_sync(0xffffffffu, excl < k_rem && incl >= k_rem);
+            if (lane == (m ? __ffs(m) - 1 : 0)) {
+                int above = excl;
+                for (int j = 31; j >= 0; --j) {
+                    const int c = cur[32 * lane + j];
+                    if (above + c >= k_rem) {
+                        sel[0] = 32 * lane + j;
+                        sel[1] = above;
+                        break;
+                    }
+                    above += c;
+                }
+            }
+        } else {
+            for (int q = threadIdx.x - 32; q < 1024; q += NT - 32)
+                nxt[q] = 0;
+        }
+        __syncthreads();
         const uint32_t bsel = static_cast<uint32_t>(sel[0]);
         k_rem -= sel[1];
-        __syncthreads();
         prefix = prev == 32 ? bsel : ((prefix << (prev - shift)) | bsel); // = d >> shift of the chosen keys
         if (shift == 0)
             break;
@@ -451,7 +492,8 @@ __device__ void select_candidates(const uint32_t *ck, const int32_t *ci, int nc,
     }
     const uint32_t tau = kmin + prefix; // every bit of d fixed: the k-th largest candidate key
     const int need_eq = k_rem;          // keys equal to tau to keep (the smallest indices)
-    // ordered output: thread t walks candidates [t * per, t * per + per)
+    // ordered output: thread t walks candidates [t * per, t * per + per); one
+    // prefix count over threads of (#greater << 16 | #equal) gives its slots
     const int per = (nc + NT - 1) / NT;
     const int f0 = threadIdx.x * per < nc ? threadIdx.x * per : nc;
     const int f1 = f0 + per < nc ? f0 + per : nc;
@@ -461,8 +503,20 @@ __device__ void select_candidates(const uint32_t *ck, const int32_t *ci, int nc,
         gt += key > tau;
         eq += key == tau;
     }
-    int total;
-    const int pre = block_exclusive_scan<NT>((gt << 16) | eq, scratch, &total);
+    const int v = (gt << 16) | eq;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o)
+            x += y;
+    }
+    if (lane == 31)
+        wsum[warp] = x;
+    __syncthreads();
+    int pre = x - v;
+    for (int w = 0; w < warp; ++w)
+        pre += wsum[w];
     int g_before = pre >> 16, e_before = pre & 0xFFFF;
     for (int f = f0; f < f1; ++f) {
         const uint32_t key = order_key_bits(ck[f]);
@@ -667,7 +721,7 @@ __device__ bool topk_row_candidates(const float *row, int n, int k, int32_t *out
         row_pass<NT, true>(row, 0, n, h, thr, wc[warp], ck, ci);
     }
     __syncthreads();
-    select_candidates<NT>(ck, ci, nc, k, out, hist, scratch, sel);
+    select_candidates<NT>(ck, ci, nc, k, out, hist, sel);
     return true;
 }
 
@@ -790,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         cluster_sync_all(); // CTA 0's list is complete; nothing of a peer is touched after this
         if (cr == 0) {
             if (nc >= 0)
-                select_candidates<kThreads>(gkey, gidx, nc, k, out, hist, scratch, sel);
+                select_candidates<kThreads>(gkey, gidx, nc, k, out, hist, sel);
             else if (vec)
                 topk_row<kThreads, true>(r, n, k, out, hist, scratch, sel);
             else
