@@ -249,8 +249,10 @@ int dsa_sparse_mla_decode_paged(const void *q, const void *kv_pool, int num_page
  *   workspace: device buffer of dsa_prefill_host_workspace_size(...) bytes,
  *         256-byte aligned, owned by the caller.
  *
- * Query rows go in chunks of chunk_rows: the inputs of a chunk are copied in
- * on a copy stream, its kernels run on `stream`, its outputs are copied out on
+ * Query rows go in chunks of at most chunk_rows (C): C/4 and C/2 rows first,
+ * so the kernels start after a short copy, then C, and a last chunk of C/4,
+ * so little is left to copy out after the last kernels.  The inputs of a chunk
+ * are copied in on a copy stream, its kernels run on `stream`, its outputs are copied out on
  * a second copy stream, and two buffer slots let the copies of neighbouring
  * chunks overlap the kernels.  The keys stay on the device for the call and are
  * copied in as far as each chunk's positions need them.  Host buffers should be

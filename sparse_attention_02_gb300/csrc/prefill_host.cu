@@ -1,7 +1,8 @@
 // Prefill from host memory: the whole hot path (indexer -> top-k -> sparse MLA)
 // on inputs that sit in host memory, with the outputs returned to host memory.
 //
-// Query rows go in chunks.  Chunk c's inputs are copied host -> device on one
+// Query rows go in chunks (short ones first and last, see chunk_starts).
+// Chunk c's inputs are copied host -> device on one
 // stream, its three kernels run on the caller's stream, and its outputs are
 // copied device -> host on a third stream; two buffer slots let the input copy
 // of chunk c + 1 and the output copy of chunk c - 1 overlap the kernels of
@@ -13,6 +14,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <vector>
 #include <stdio.h>
 
 #include "common.cuh"
@@ -61,6 +63,34 @@ bool make_pipe(HostPipe &p)
 }
 
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Chunk starts for T rows in chunks of at most C: C/4 and C/2 first, so the
+// kernels start after a short first copy, then C, and a last chunk of C/4, so
+// little is left to copy out after the last kernels.  Returns the starts and T.
+std::vector<int> chunk_starts(int T, int C)
+{
+    std::vector<int> st;
+    const int q = std::max(1, C / 4), h = std::max(1, C / 2);
+    int r = 0;
+    for (int first : {q, h}) {
+        if (r < T) {
+            st.push_back(r);
+            r += std::min(first, T - r);
+        }
+    }
+    while (T - r > C + q) {
+        st.push_back(r);
+        r += C;
+    }
+    if (T - r > q) {
+        st.push_back(r);
+        r = T - q;
+    }
+    if (r < T)
+        st.push_back(r);
+    st.push_back(T);
+    return st;
+}
 
 // Workspace layout; every region starts on a 256-byte boundary.
 struct Layout {
@@ -159,11 +189,12 @@ extern "C" int dsa_prefill_host(const void *q8, const float *q_scale, const floa
     chk(cudaStreamWaitEvent(P.d2h, P.start, 0));
 
     int keys_in = 0; // key rows [0, keys_in) already on the device
-    const int nchunks = (T + C - 1) / C;
+    const std::vector<int> starts = chunk_starts(T, C);
+    const int nchunks = static_cast<int>(starts.size()) - 1;
     int rc = DSA_OK;
     for (int c = 0; c < nchunks && rc == DSA_OK && e == cudaSuccess; ++c) {
         const int s = c % kSlots;
-        const int r0 = c * C, n = std::min(C, T - r0);
+        const int r0 = starts[c], n = starts[c + 1] - r0; // 1 <= n <= C
         int kmax = 0;
         for (int r = r0; r < r0 + n; ++r)
             kmax = std::max(kmax, q_pos[r] + 1);
