@@ -417,18 +417,22 @@ def e2e_bench(dsa, x, b, cfg, steps, dev, chunk_rows=2048):
 
     step()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
+    # back to back, with an event between steps (each call already waits for the
+    # previous one on the stream, so the events add no serialisation)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record()
+    for i in range(steps):
         step()
-    e1.record()
+        ev[i + 1].record()
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
+    each = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    ms = ev[0].elapsed_time(ev[steps]) / steps
     # the host outputs are the device path's outputs (same kernels, same rows)
     same = bool(torch.equal(out_h.view(torch.int16), b["out"].cpu().view(torch.int16)))
     del ws, host
     return {"value": cfg.L / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms, "api": "dsa_prefill_host",
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms, "ms_each_step": [round(x, 3) for x in each],
+            "api": "dsa_prefill_host",
             "chunk_rows": chunk_rows, "matches_device_path": same}
 
 
@@ -552,7 +556,7 @@ def main():
         "timed_wall_s": t_wall1 - t_wall0,
     }
     if not args.no_e2e:
-        line["e2e"] = e2e_bench(dsa, x, b, cfg, max(2, min(args.steps, 5)), dev)
+        line["e2e"] = e2e_bench(dsa, x, b, cfg, max(2, min(args.steps, 8)), dev)
         line["e2e"]["value"] *= world
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, x)
