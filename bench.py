@@ -398,7 +398,9 @@ def decode_bench(dsa, steps, warmup, flush, peaks, dev):
 def e2e_bench(dsa, x, b, cfg, steps, dev, chunk_rows=2048):
     """The same step through the public C ABI on pinned HOST buffers: dsa_prefill_host copies the
     inputs in, runs the three stages chunk by chunk (copies of one chunk overlap the kernels of
-    the next) and copies out and lse back; every copy is inside the timed region."""
+    the next) and copies out and lse back; every copy is inside the timed region.  The value is
+    the mean over the steps; each step's time and the median are reported beside it (a single
+    step of a run has been seen to take several times the others)."""
     names = ["q8", "qs", "w", "q_pos", "q", "k8", "ks", "kv"]
     host = {n: torch.empty(x[n].shape, dtype=x[n].dtype, pin_memory=True) for n in names}
     for n in names:
@@ -432,6 +434,7 @@ def e2e_bench(dsa, x, b, cfg, steps, dev, chunk_rows=2048):
     del ws, host
     return {"value": cfg.L / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": ms, "ms_each_step": [round(x, 3) for x in each],
+            "median_ms_per_step": float(np.median(each)),
             "api": "dsa_prefill_host",
             "chunk_rows": chunk_rows, "matches_device_path": same}
 
@@ -556,7 +559,7 @@ def main():
         "timed_wall_s": t_wall1 - t_wall0,
     }
     if not args.no_e2e:
-        line["e2e"] = e2e_bench(dsa, x, b, cfg, max(2, min(args.steps, 8)), dev)
+        line["e2e"] = e2e_bench(dsa, x, b, cfg, max(2, min(args.steps, 16)), dev)
         line["e2e"]["value"] *= world
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, x)
