@@ -232,6 +232,34 @@ def test_decode_paged_pipeline():
     check_attention(out.cpu().double().numpy(), lse.cpu().double().numpy(), o_ref, l_ref)
 
 
+@pytest.mark.parametrize("H", [16, 64])
+@pytest.mark.parametrize("B", [5, 96])  # rows split over the clusters, and whole rows
+def test_decode_fewer_heads(H, B):
+    """Paged decode attention with fewer than 128 query heads (the MMA rows past H are
+    zero and never stored), split and whole rows, against the oracle."""
+    cfg = W.CONFIGS["decode_paged"]
+    dsa = lib()
+    k = 256
+    g = np.random.default_rng(7 * H + B)
+    ctx = g.integers(1, 3 * k, size=B)
+    d = W.decode_inputs(cfg, DEV, ctx=ctx.tolist(), seed=H + B)
+    idx_np = np.full((B, k), -1, np.int32)
+    for b in range(B):
+        c = int(ctx[b])
+        m = min(k, c)
+        idx_np[b, :m] = g.choice(c, size=m, replace=False)
+    idx = torch.from_numpy(idx_np).to(DEV)
+    q = d["q"][:, :H].contiguous()
+    out = torch.full((B, H, 512), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((B, H), float("nan"), dtype=torch.float32, device=DEV)
+    dsa.dsa_sparse_mla_decode_paged(q, d["kv_pool"], d["block_table"], d["ctx"], idx, cfg.sm_scale, out, lse)
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_device_status() == 0
+    o_ref, l_ref = oracle.sparse_mla_paged(bits16(q), bits16(d["kv_pool"]), d["block_table"].cpu().numpy(),
+                                           ctx.astype(np.int32), idx_np, cfg.sm_scale)
+    check_attention(out.cpu().double().numpy(), lse.cpu().double().numpy(), o_ref, l_ref)
+
+
 @pytest.mark.parametrize("B,k", [(1, 2048), (3, 100), (5, 64), (17, 2048), (64, 2048), (75, 256), (100, 300)])
 def test_decode_split_pieces(B, k):
     """Decode batches with fewer rows than SM pairs cut each row into pieces over
