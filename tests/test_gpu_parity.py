@@ -4,6 +4,8 @@ Sizes are chosen so the oracle finishes in seconds while still spanning several
 tiles and a ragged tail (query rows, key tiles of 128, attention blocks of 64,
 pages of 64).  Seeded synthetic inputs only.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -41,6 +43,33 @@ def test_indexer_h64_ragged(L):
     rng = np.random.default_rng(L)
     rows = np.unique(np.concatenate([[0, L - 1, min(127, L - 1), min(128, L - 1)], rng.integers(0, L, 40)]))
     _indexer_case(W.CONFIGS["prefill_4k"], L, rows)
+
+
+@pytest.mark.parametrize("L", [129, 700])
+def test_indexer_h32_ragged(L):
+    """The H_I = 32 instantiation of the contiguous indexer (half the heads per token)."""
+    cfg = dataclasses.replace(W.CONFIGS["prefill_4k"], HI=32)
+    rng = np.random.default_rng(L + 32)
+    rows = np.unique(np.concatenate([[0, L - 1, min(127, L - 1), min(128, L - 1)], rng.integers(0, L, 40)]))
+    _indexer_case(cfg, L, rows)
+
+
+def test_paged_indexer_h32():
+    """The H_I = 32 instantiation of the paged indexer over a shuffled page pool."""
+    cfg = dataclasses.replace(W.CONFIGS["decode_paged"], HI=32)
+    dsa = lib()
+    ctx = [1, 64, 65, 2047, 3001, 5000]
+    d = W.decode_inputs(cfg, DEV, ctx=ctx)
+    B, ld = len(ctx), max(ctx) + 3
+    logits = torch.full((B, ld), float("nan"), device=DEV)
+    dsa.dsa_indexer_logits(d["q8"], d["qs"], d["w"], d["k8_pool"], d["ks_pool"], d["q_pos"], logits,
+                           block_table=d["block_table"])
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_device_status() == 0
+    h = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in d.items()}
+    ref = oracle.indexer_paged(h["q8"].numpy(), h["qs"].numpy(), h["w"].numpy(), h["ctx"].numpy(),
+                               h["k8_pool"].numpy(), h["ks_pool"].numpy(), h["block_table"].numpy(), ld)
+    check_logits(logits.cpu().double().numpy(), ref, h["q_pos"].numpy())
 
 
 def test_topk_from_gpu_logits_bit_exact():
