@@ -95,3 +95,23 @@ def test_binding_raises_without_the_library(tmp_path):
 
     with pytest.raises(RuntimeError, match="missing"):
         dsa.load_library(str(tmp_path / "nope.so"))
+
+
+def test_every_declaration_is_documented_and_cites_its_page():
+    """Each function in dsa.h has a comment right above it (or above its macro); the
+    entry points of the method's steps cite the page that defines them."""
+    text = open(HEADER).read()
+    pages = ("AMD Instinct MI355X GPUs Power DeepSeek-V3.2-Exp", "DeepSeek-V3.2-Exp: Boosting Long-Context")
+    steps = {"dsa_indexer_logits", "dsa_quantize_fp8", "dsa_topk", "dsa_sparse_mla_prefill",
+             "dsa_sparse_mla_decode_paged"}
+    for name in declared_functions():
+        m = re.search(r"^[A-Za-z_][\w\s\*]*\b" + name + r"\s*\(", text, flags=re.M)
+        assert m, f"{name}: declaration not found"
+        before = text[: m.start()].rstrip()
+        while before.endswith(")") or re.search(r"#define [^\n]*$", before):  # macros placed between
+            before = before[: before.rfind("\n")].rstrip()
+        assert before.endswith("*/"), f"{name} has no comment above its declaration"
+        comment = before[before.rfind("/*"):]
+        if name in steps:
+            flat = " ".join(comment.replace("*", " ").split())
+            assert any(" ".join(pg.split()) in flat for pg in pages), f"{name}: no page cited"
