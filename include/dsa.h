@@ -199,8 +199,8 @@ int dsa_sparse_mla_prefill(const void *q, const void *kv, int S,
  * dsa_sparse_mla_decode_paged: the same attention over a paged latent cache
  * (decode form of stage 3; "DeepSeek-V3.2-Exp: Boosting Long-Context
  * Efficiency with DeepSeek Sparse Attention", section "Key claims": the
- * sparse-attention and indexer kernels come in paged versions; the attention
- * itself is that of section "Method").
+ * released kernels are indexer-logit kernels, paged versions included, and
+ * sparse-attention kernels; the attention itself is that of section "Method").
  *
  * Row b is one query: its token sits at position ctx_len[b]-1 of the sequence
  * whose pages block_table row b lists.  Rows are independent, so a batch may
