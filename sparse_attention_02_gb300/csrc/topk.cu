@@ -24,10 +24,10 @@
 // (1.25 k + 256) / n from the top (row_threshold; every CTA of the cluster
 // draws the same samples and gets the same value; shorter rows use none);
 // (2) CTA c streams its own 1/cs of the row once, kUnroll 16-byte loads per
-// lane in flight, and keeps every key at or above the threshold: warp w scans
-// a contiguous segment and appends (score bits, index) to its own region of shared
-// memory with ballot prefix counts, so the regions taken in warp order list
-// the CTA's candidates in index order; (3) each CTA pushes its candidates,
+// lane in flight, and keeps every key at or above the threshold: warp w
+// scans a contiguous segment and appends (score bits, index) to its own
+// region of shared memory with ballot prefix counts, so the regions taken in
+// warp order list the CTA's candidates in index order; (3) each CTA pushes its candidates,
 // in order, into CTA 0's list through distributed shared memory; (4) CTA 0
 // runs the exact radix select on those few thousand candidates and one
 // block-wide prefix count over the ordered list writes the kept indices in
