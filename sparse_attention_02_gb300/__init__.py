@@ -82,6 +82,14 @@ def _stream(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _same_device(t: torch.Tensor, name: str):
+    # the library runs on the current device (cudaGetDevice); a tensor elsewhere would
+    # hand it another GPU's pointer
+    cur = torch.cuda.current_device()
+    if t.device.index != cur:
+        raise ValueError(f"{name} is on {t.device}, but the current device is cuda:{cur}")
+
+
 def _need(t: torch.Tensor, dtype, name: str, dim: int | None = None):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
@@ -89,6 +97,7 @@ def _need(t: torch.Tensor, dtype, name: str, dim: int | None = None):
         raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    _same_device(t, name)
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dim is not None and t.dim() != dim:
@@ -99,6 +108,7 @@ def _need_rows(t: torch.Tensor, dtype, name: str):
     """A 2-D tensor whose rows may be strided (leading dimension >= width)."""
     if not isinstance(t, torch.Tensor) or t.dtype != dtype or not t.is_cuda or t.dim() != 2:
         raise TypeError(f"{name}: expected a 2-D CUDA {dtype} tensor")
+    _same_device(t, name)
     if t.stride(1) != 1 or t.stride(0) < t.shape[1]:
         raise ValueError(f"{name}: rows must be contiguous with a leading dimension >= width")
 
