@@ -30,7 +30,7 @@ def _worker(rank, world, port, out):
 def test_two_rank_aggregation():
     world = 2
     port = _free_port()
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()  # no fork of a process that may hold threads
     mp.start_processes(_worker, args=(world, port, out), nprocs=world, start_method="spawn")
     for r in range(world):
         ms, value = out[r]
