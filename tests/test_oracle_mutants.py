@@ -38,6 +38,12 @@ MUTANTS = {
     "paged_index_slot": ("int64_t slot = (int64_t)page * page_size + s % page_size;",
                          "int64_t slot = (int64_t)page * page_size;"),
     "prefill_bound": ("rows_sel[i] = (s >= 0 && s < S) ? (int64_t)s : -1;", "rows_sel[i] = (int64_t)s;"),
+    "query_scale_dropped": ("(dsa_oracle_e4m3(q8t[(int64_t)j * dI + d]) * qs)",
+                            "(dsa_oracle_e4m3(q8t[(int64_t)j * dI + d]))"),
+    "paged_table_row": ("block_table[(int64_t)r * max_pages + s / page_size]", "block_table[s / page_size]"),
+    "rope_dropped": ("for (int d = 0; d < D; ++d)\n            dot += dsa_oracle_bf16(q_rh[d])",
+                     "for (int d = 0; d < 512; ++d)\n            dot += dsa_oracle_bf16(q_rh[d])"),
+    "topk_pad_zero": ("            o[i] = -1;", "            o[i] = 0;"),
     "e4m3_ties_up": ("code = (lo % 2 == 0) ? lo : hi;", "code = hi;"),
     "e4m3_saturates_to_nan": ("return (uint8_t)(sign | 0x7E);", "return (uint8_t)(sign | 0x7F);"),
     "quant_scale_constant": ("const float ratio = amax / 448.f;", "const float ratio = amax / 447.f;"),
