@@ -44,6 +44,10 @@ MUTANTS = {
     "rope_dropped": ("for (int d = 0; d < D; ++d)\n            dot += dsa_oracle_bf16(q_rh[d])",
                      "for (int d = 0; d < 512; ++d)\n            dot += dsa_oracle_bf16(q_rh[d])"),
     "topk_pad_zero": ("            o[i] = -1;", "            o[i] = 0;"),
+    "topk_k_off_by_one": ("int m = n < k ? n : k;", "int m = n < k ? n : k - 1;"),
+    "lse_log2": ("*lse = m + log(z);", "*lse = m + log2(z);"),
+    "paged_ctx_bound": ("if (s < 0 || s >= ctx_len[r] || s / page_size >= max_pages)",
+                        "if (s < 0 || s / page_size >= max_pages)"),
     "e4m3_ties_up": ("code = (lo % 2 == 0) ? lo : hi;", "code = hi;"),
     "e4m3_saturates_to_nan": ("return (uint8_t)(sign | 0x7E);", "return (uint8_t)(sign | 0x7F);"),
     "quant_scale_constant": ("const float ratio = amax / 448.f;", "const float ratio = amax / 447.f;"),
