@@ -44,7 +44,7 @@ typedef struct CUstream_st *dsa_stream_t; /* same type as cudaStream_t */
 typedef enum {
     DSA_OK = 0,
     DSA_ERR_INVALID_ARG = 1, /* null pointer, negative size, inconsistent shapes   */
-    DSA_ERR_UNSUPPORTED = 2, /* a size this build has no kernel for (see below)     */
+    DSA_ERR_UNSUPPORTED = 2, /* a size the library has no kernel for (see below)   */
     DSA_ERR_ALIGNMENT = 3,   /* a pointer or stride breaks a 16-byte TMA rule       */
     DSA_ERR_WORKSPACE = 4,   /* workspace missing or smaller than the query says    */
     DSA_ERR_CUDA = 5,        /* a CUDA runtime/driver call or a launch failed       */

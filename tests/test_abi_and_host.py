@@ -90,6 +90,36 @@ def test_host_validation_rejects_bad_arguments(lib):
                                            fake, None, 0, None) == 1
 
 
+def test_host_prefill_validation(lib):
+    """dsa_prefill_host's own checks, all taken on the host before any CUDA call (no call
+    here passes them all, so nothing reaches the device)."""
+    import numpy as np
+
+    P = ctypes.c_void_p
+    fake = P(4096)
+    T, S, HI, dI, H, k, C = 4, 8, 64, 128, 128, 64, 4
+    need = lib.dsa_prefill_host_workspace_size(T, S, HI, dI, H, k, C)
+    assert need > 0 and lib.dsa_prefill_host_workspace_size(T, S, HI, dI, 129, k, C) == 0
+    q_pos = np.arange(T, dtype=np.int32)
+    qp = q_pos.ctypes.data_as(P)
+
+    def call(t=T, h=H, chunk=C, ws=P(1 << 20), ws_bytes=need, pos=qp):
+        return lib.dsa_prefill_host(fake, fake, fake, pos, fake, fake, fake, fake, t, S, HI, dI, h, k,
+                                    ctypes.c_float(0.04), fake, fake, chunk, ws, ws_bytes, None)
+
+    assert call(t=-1) == 1
+    assert call(chunk=0) == 1
+    assert call(t=0) == 0                       # no rows: nothing to do
+    assert call(ws=None) == 1                   # null workspace
+    assert call(h=129) == 1                     # heads out of range
+    assert call(ws=P((1 << 20) + 16)) == 3      # workspace not 256-byte aligned
+    assert call(ws_bytes=need - 1) == 4         # workspace short by one byte
+    assert "workspace" in _err(lib)
+    bad = np.array([0, 1, S, 3], dtype=np.int32)
+    assert call(pos=bad.ctypes.data_as(P)) == 1  # a query position past the keys
+    assert "q_pos[2]" in _err(lib)
+
+
 def test_binding_raises_without_the_library(tmp_path):
     import sparse_attention_02_gb300 as dsa
 
