@@ -185,6 +185,12 @@ int dsa_topk(const float *logits, int64_t ld, int T, const int32_t *valid_len,
  * first 512 columns are V, the last 64 are the RoPE part used only in scores.)
  * A row with no valid entry gets out = 0 and lse = -inf.
  *
+ * Precision: scores accumulate in fp32 (each token runs on two SMs that each
+ * hold half of the 576 score columns and exchange their fp32 partial scores,
+ * so a score is off by a few fp32 ulps of its magnitude, however large); P is
+ * rounded to bf16 before the PV product and out to bf16 (nearest even) at the
+ * end.
+ *
  *   q    [T, H, 576] bf16;  kv [S, 576] bf16;  idx [T, k] int32
  *   out  [T, H, 512] bf16 (rounded to nearest even);  lse [T, H] fp32
  * Supported: 1 <= H <= 128 (fewer than 128 heads run as zero-padded rows

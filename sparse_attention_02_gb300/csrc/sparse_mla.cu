@@ -23,13 +23,18 @@
 //   96 of this CTA's Q columns live in TMEM (the score MMA reads them as a TMEM
 //   A operand), the first 192 in shared memory.
 
-// The swap carries the log2-scaled partial scores rounded to fp16 (saturating,
-// 16 KB per 64-key block instead of 32 KB in fp32); each CTA rounds its own
-// half the same way before adding.  At the scores' scale (|s| of a few units
-// in log2 terms) this perturbs each softmax weight by ~2^-11 relative, below
-// the bf16 rounding of P that the PV product applies anyway.
+// The swap carries the raw fp32 partial scores (32 KB per 64-key block).  The
+// sender warps add the peer's partials to their own in fp32 and apply the log2
+// softmax scale, (own + peer) * scale, written back over the block's S buffer:
+// the add commutes, so both CTAs hold bit-identical scores whose error is that
+// of the fp32 accumulation alone, a few fp32 ulps of |S| at any score
+// magnitude (a sharp, one-key softmax with scores of tens of nats included).
+// Partials rounded to fp16 would halve the swap, which bounds the rate (the
+// pair's link carries ~16 KB per 0.4 us), but put an error of ~|S| * 2^-11 on
+// every score and hence on LSE.
 //
-// Per 64-key block j (double-buffered S, swap and P buffers, four KV stages):
+// Per 64-key block j (double-buffered S and P buffers, one swap buffer, four
+// KV stages):
 //   producer warps  four warps cp.async the 64 selected rows x 576 B into the
 //                   SW128 / SW64 K-major layouts (one 128-byte line per 8
 //                   lanes), zero-fill invalid entries, and arrive on the
@@ -45,16 +50,17 @@
 //                   per instruction whatever N is, so the N=64 score MMAs need
 //                   two issuing warps to keep the tensor pipe fed;
 //   sender warps    thread = head, one warp per TMEM lane quadrant: the
-//                   block's partial S from TMEM, log2-scaled and rounded to
-//                   fp16 pairs, st.async to the peer (completion counted in
-//                   bytes on the peer's mbarrier) and parked in place over the
-//                   block's S buffer.  They run ahead of the softmax, so the swap of one
-//                   block overlaps the softmax of the previous one and the
-//                   softmax warps never stall on the slow DSMEM stores;
+//                   block's 64 partial scores from TMEM, st.async to the peer
+//                   in fp32 (completion counted in bytes on the peer's
+//                   mbarrier) as soon as the peer has read the previous
+//                   block's, so the swap of one block overlaps the softmax of
+//                   the previous one and the softmax warps never issue the
+//                   slow DSMEM stores themselves;
 //   softmax warps   thread = head, two warps per TMEM lane quadrant, each with
-//                   32 of the block's keys: own half from the S buffer (then
-//                   free for the next score MMAs), peer half from the swap
-//                   buffer, mask, max (agreed with the sibling warp through a
+//                   32 of the block's keys: own partial from the S buffer
+//                   (then free for the next score MMAs once the senders have
+//                   read it too), peer partial from the swap buffer, sum,
+//                   scale, mask, max (agreed with the sibling warp through a
 //                   spare TMEM column), exp2, running sum; P (bf16) into the
 //                   block's P buffer once its previous PV is done.  The
 //                   running max only moves when a block exceeds it by more
@@ -66,7 +72,6 @@
 #include "common.cuh"
 #include "launch.h"
 
-#include <cuda_fp16.h>
 #include <stdio.h>
 
 namespace dsa {
@@ -83,7 +88,8 @@ constexpr int kKVHalf = kBN * 64;        // bytes of the RoPE half atom (64 rows
 constexpr int kStage = kVAtoms * kKVAtom + kKVHalf; // 36 KB
 constexpr int kNStage = 4;
 constexpr int kPf = 3;                   // paged: blocks ahead whose latent rows the producers resolve
-constexpr int kXBuf = 128 * kBN * 2;     // one swap buffer: 128 heads x 64 fp16
+constexpr int kXBuf = 128 * kBN * 4;     // one swap buffer: 128 heads x 64 fp32 partial scores
+constexpr int kNX = 1; // swap buffers (32 KB each): one beside four stages; a second with three stages measured no faster
 constexpr int kProdWarps = 4;
 constexpr int kPvWarp = kProdWarps;      // all PV MMAs (fixed accumulation order) + TMEM owner
 constexpr int kQkWarp0 = kProdWarps + 1; // score MMAs of even blocks; kQkWarp0 + 1: odd blocks
@@ -92,29 +98,29 @@ constexpr int kSendWarps = 4;            // one per TMEM lane quadrant: partial 
 constexpr int kSoftWarp0 = kSendWarp0 + kSendWarps;
 constexpr int kSoftWarps = 8;            // two per TMEM lane quadrant, 32 keys of each block apiece
 constexpr int kThreads = 32 * (kSoftWarp0 + kSoftWarps);
-constexpr int kSoftThread0 = 32 * kSoftWarp0;
 constexpr float kRescaleLog2 = 8.f;      // move the running max only when exceeded by this
 
 constexpr int OFF_Q = 0;                                  // 3 full atoms
 constexpr int OFF_KV = OFF_Q + kQSmemAtoms * kQAtom;     // 48 KB
 constexpr int OFF_X = OFF_KV + kNStage * kStage;         // 192 KB
-constexpr int OFF_BAR = OFF_X + 2 * kXBuf;               // 224 KB
+constexpr int OFF_BAR = OFF_X + kNX * kXBuf;             // 224 KB
 constexpr int NBAR = 40;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int kSmem = OFF_MISC + 64 + 1024;
+static_assert(kSmem <= 232448, "dynamic shared memory above the 227 KB a CTA may hold");
 
 // barrier slots
-// [parity] for S and swap buffers, [J % kNP] for P buffers
+// [J & 1] for S buffers, [J % kNX] for swap buffers, [J % kNP] for P buffers
 constexpr int kNP = 2; // P buffers in TMEM
 constexpr int B_KVF = 0, B_KVE = 4, B_SF = 8, B_SE = 10, B_XF = 12, B_XE = 14, B_PF = 16, B_PE = 18,
-              B_PK = 20,  // senders parked the block's own fp16 partial scores in its P buffer
+              B_ST = 20, // [J & 1]: the senders wrote the block's scaled total scores over its S buffer
               B_QF = 22, B_QE = 23, B_QA = 24, B_OF = 25, B_OE = 26, B_DONE = 27,
               B_RB = 28,  // [quad][parity]: sibling softmax warps swapped their block max
               B_RL = 36;  // [quad]: sibling softmax warps swapped their row sums
 
 // TMEM columns
 constexpr uint32_t TM_O = 0;
-constexpr uint32_t TM_S = 256;  // two buffers of 64
+constexpr uint32_t TM_S = 256;  // two buffers of 64 fp32 partial scores
 constexpr uint32_t TM_P = 384;  // kNP buffers of 32 (bf16 pairs)
 constexpr uint32_t TM_QT = 448; // Q: the 4th atom (32 columns of bf16 pairs) and the RoPE half (16)
 constexpr uint32_t TM_RED = 496; // per-head values swapped between the two softmax warps of a quadrant
@@ -237,19 +243,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return r;
 }
 
-// Two fp32 -> one f16x2 word, round to nearest even, saturating to +-65504.
-__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi)
-{
-    uint32_t r;
-    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-__device__ __forceinline__ float2 unpack_f16x2(uint32_t w)
-{
-    return __half22float2(*reinterpret_cast<const __half2 *>(&w));
-}
-
 template <bool PAGED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_q, Params p)
@@ -277,12 +270,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_SF + i), 1);
+            mbar_init(bar(B_ST + i), kSendWarps);
             mbar_init(bar(B_SE + i), kSoftWarps);
+        }
+        for (int i = 0; i < kNX; ++i) {
             mbar_init(bar(B_XF + i), 1);
-            mbar_init(bar(B_XE + i), kSoftWarps);
+            mbar_init(bar(B_XE + i), kSendWarps); // the peer's senders have added its contents
         }
         for (int i = 0; i < kNP; ++i) {
-            mbar_init(bar(B_PK + i), kSendWarps);
             mbar_init(bar(B_PF + i), kSoftWarps);
             mbar_init(bar(B_PE + i), 1);
         }
@@ -672,18 +667,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp < kSoftWarp0) {
-        // ------------------------------------------------- score senders
-        // Thread = head (TMEM lane), all 64 keys of each block: this CTA's
-        // partial scores, log2-scaled and rounded to fp16 pairs, go to the peer
-        // by st.async (completion counted in bytes on the peer's mbarrier) and
-        // back over the first half of the block's S buffer, where the softmax
-        // warps read them.
+        // -------------------------------- score senders
+        // Thread = head (TMEM lane), all 64 keys of each block.  This CTA's fp32
+        // partial scores go to the peer by st.async (completion counted in bytes
+        // on the peer's mbarrier); once the peer's partials have landed here,
+        // the same warp writes (own + peer) * scale over the block's S buffer
+        // (fp32: the add commutes, so both CTAs hold the same bits) and frees
+        // the swap buffer at once, so the next block's swap never waits for the
+        // softmax.  The row of head h in the swap buffer is 16 chunks of 16
+        // bytes, chunk c stored at c ^ (h & 7): eight consecutive heads reading
+        // the same chunk hit eight different banks.
         const int quad = warp & 3;
         const int h = quad * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t hsw = static_cast<uint32_t>(h & 7); // swap-buffer chunk swizzle (bank spread)
-        const uint32_t x_remote0 = mapa_shared(sbase + OFF_X + h * 128, peer);
+        const uint32_t hsw = static_cast<uint32_t>(h & 7);
+        const uint32_t x_remote0 = mapa_shared(sbase + OFF_X + h * (kBN * 4), peer);
         const uint32_t xf_remote0 = mapa_shared(bar(B_XF), peer);
+        const uint32_t xe_remote0 = mapa_shared(bar(B_XE), peer);
+        const uint8_t *xrow = smem + OFF_X + h * (kBN * 4);
         uint32_t J = 0;
         int u = 0;
         bool ok = true;
@@ -700,41 +701,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 mbar_arrive(bar(B_QA)); // this token's nb slot has been read
             for (int j = 0; j < nb; ++j, ++J) {
                 const int b = J & 1;
-                if (!mbar_wait_warp(bar(B_SF + b), (J >> 1) & 1, abort_flag, p.status)) {
+                const int xb = J % kNX;
+                const uint32_t s_cols = tmem + lane_off + TM_S + 64 * b;
+                // arm this CTA's swap buffer for the peer's half of block J (its bytes may
+                // already be landing; this thread saw the buffer's phase of block J - kNX complete)
+                if (quad == 0 && lane == 0)
+                    mbar_arrive_expect_tx(bar(B_XF + xb), kXBuf);
+                // the peer's swap buffer must be free (its senders have added block J - kNX)
+                if (!mbar_wait_warp(bar(B_SF + b), (J >> 1) & 1, abort_flag, p.status) ||
+                    (J >= kNX &&
+                     !mbar_wait_warp<true>(bar(B_XE + xb), ((J / kNX) - 1) & 1, abort_flag, p.status))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                uint32_t own[32];
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + lane_off + TM_S + 64 * b + 32 * hh, r);
+                const uint32_t xr = x_remote0 + xb * kXBuf, xfr = xf_remote0 + 8u * xb;
+#pragma unroll 1
+                for (int qq = 0; qq < 4; ++qq) {
+                    uint32_t r[16];
+                    tmem_ld16(s_cols + 16 * qq, r);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        own[16 * hh + c] = pack_f16x2_sat(__uint_as_float(r[2 * c]) * p.scale_log2,
-                                                          __uint_as_float(r[2 * c + 1]) * p.scale_log2);
+                    for (int cc = 0; cc < 4; ++cc)
+                        st_async_v4_b32(xr + ((static_cast<uint32_t>(4 * qq + cc) ^ hsw) << 4), r[4 * cc],
+                                        r[4 * cc + 1], r[4 * cc + 2], r[4 * cc + 3], xfr);
                 }
-                // the peer's buffer b must be free (its softmax warps read block J-2)
-                if (J >= 2 && !mbar_wait_warp<true>(bar(B_XE + b), ((J >> 1) - 1) & 1, abort_flag, p.status)) {
+                if (!mbar_wait_warp<true>(bar(B_XF + xb), (J / kNX) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
-                const uint32_t xr = x_remote0 + b * kXBuf, xfr = xf_remote0 + 8u * b;
+#pragma unroll 1
+                for (int qq = 0; qq < 4; ++qq) {
+                    uint32_t r[16];
+                    tmem_ld16(s_cols + 16 * qq, r);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc)
-                    st_async_v4_b32(xr + ((static_cast<uint32_t>(cc) ^ hsw) << 4), own[4 * cc], own[4 * cc + 1],
-                                    own[4 * cc + 2], own[4 * cc + 3], xfr);
-                // park the own half in place, over the first 32 columns of S buffer b
-                // (this warp's lanes were read whole above); the softmax warps read
-                // it back and then free the buffer for the score MMAs of block J + 2
-                tmem_st32(tmem + lane_off + TM_S + 64 * b, own);
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 pw = *reinterpret_cast<const uint4 *>(
+                            xrow + xb * kXBuf + ((static_cast<uint32_t>(4 * qq + c) ^ hsw) << 4));
+                        const uint32_t pws[4] = {pw.x, pw.y, pw.z, pw.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            r[4 * c + e] = __float_as_uint((__uint_as_float(r[4 * c + e]) + __uint_as_float(pws[e])) *
+                                                           p.scale_log2);
+                    }
+                    tmem_st16(s_cols + 16 * qq, r);
+                }
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(bar(B_PK + b));
+                if (lane == 0) {
+                    mbar_arrive(bar(B_ST + b));                      // totals of block J ready
+                    mbar_arrive_remote_relaxed(xe_remote0 + 8u * xb); // this CTA's swap buffer is free again
+                }
             }
         }
     } else {
@@ -747,8 +766,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int hf = sw >> 2;
         const int h = quad * 32 + lane;                  // head = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t hsw = static_cast<uint32_t>(h & 7); // swap-buffer chunk swizzle (bank spread)
-        const uint32_t xe_remote0 = mapa_shared(bar(B_XE), peer);
         const uint32_t red = tmem + lane_off + TM_RED;
         uint32_t J = 0;
         int u = 0, v = 0;
@@ -801,47 +818,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int n0 = (un.jb + j + 1) * kBN + 32 * hf + lane;
                     raw = n0 < p.k ? idx_row[n0] : -1;
                 }
-                // 1. this CTA's partial scores (fp16 pairs parked by the senders) and the peer's half
+                // 1. the block's scaled total scores of this warp's 32 keys, written over the S
+                //    buffer by the senders; then the buffer is free for block J + 2
                 const int pb = J % kNP;
-                if (!mbar_wait_warp(bar(B_PK + b), (J >> 1) & 1, abort_flag, p.status)) {
+                if (!mbar_wait_warp(bar(B_ST + b), (J >> 1) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                uint32_t own[16];
-                tmem_ld16(tmem + lane_off + TM_S + 64 * b + 16 * hf, own);
-                tmem_ld_wait();
+                float sc[32];
+                {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_off + TM_S + 64 * b + 32 * hf, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        sc[c] = __uint_as_float(r[c]);
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(bar(B_SE + b)); // S buffer b is free for the score MMAs of block J + 2
-                // arm buffer b for the peer's half of block J (its bytes may already be landing);
-                // this thread has seen the phase of block J-2 complete
-                if (threadIdx.x == kSoftThread0)
-                    mbar_arrive_expect_tx(bar(B_XF + b), kXBuf);
-                if (!mbar_wait_warp<true>(bar(B_XF + b), (J >> 1) & 1, abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
-                // 3. scores = own half + peer half (the same sum in both CTAs), mask
-                float sc[32];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint32_t cc = 4u * hf + c;
-                    const uint4 pw = *reinterpret_cast<const uint4 *>(smem + OFF_X + b * kXBuf + h * 128 +
-                                                                      ((cc ^ hsw) << 4));
-                    const uint32_t pws[4] = {pw.x, pw.y, pw.z, pw.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 a = unpack_f16x2(own[4 * c + e]);
-                        const float2 o = unpack_f16x2(pws[e]);
-                        sc[8 * c + 2 * e] = a.x + o.x;
-                        sc[8 * c + 2 * e + 1] = a.y + o.y;
-                    }
-                }
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive_remote_relaxed(xe_remote0 + 8u * b); // our buffer b is free again
+                    mbar_arrive(bar(B_SE + b));
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
@@ -1109,17 +1106,11 @@ Plan plan(bool paged, int T, int k)
 template <bool PAGED>
 int launch(const MlaArgs &a, cudaStream_t stream, char *err, size_t errlen)
 {
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(sparse_mla_kernel<PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmem);
-        if (e != cudaSuccess) {
-            snprintf(err, errlen, "cudaFuncSetAttribute(sparse_mla): %s", cudaGetErrorString(e));
-            return DSA_ERR_CUDA;
-        }
-        attr_set[dev] = true;
+    static std::atomic<bool> attr_set[64];
+    if (cudaError_t e_attr = raise_smem_limit_once(sparse_mla_kernel<PAGED>, kSmem, attr_set);
+        e_attr != cudaSuccess) {
+        snprintf(err, errlen, "cudaFuncSetAttribute(sparse_mla): %s", cudaGetErrorString(e_attr));
+        return DSA_ERR_CUDA;
     }
     // Q as [T*H rows, 576 cols]: 64-column boxes (SW128)
     CUtensorMap tq;
