@@ -919,17 +919,11 @@ template <int HI, int DI, bool PAGED>
 int launch_cfg(const IndexerArgs &a, cudaStream_t stream, char *err, size_t errlen)
 {
     using C = IdxCfg<HI, DI, PAGED>;
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(indexer_kernel<HI, DI, PAGED>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) {
-            snprintf(err, errlen, "cudaFuncSetAttribute(indexer): %s", cudaGetErrorString(e));
-            return DSA_ERR_CUDA;
-        }
-        attr_set[dev] = true;
+    static std::atomic<bool> attr_set[64];
+    if (cudaError_t e_attr = raise_smem_limit_once(indexer_kernel<HI, DI, PAGED>, C::SMEM, attr_set);
+        e_attr != cudaSuccess) {
+        snprintf(err, errlen, "cudaFuncSetAttribute(indexer): %s", cudaGetErrorString(e_attr));
+        return DSA_ERR_CUDA;
     }
     const CUtensorMapSwizzle swz = DI == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                              : (DI == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
@@ -975,15 +969,11 @@ int launch_cfg(const IndexerArgs &a, cudaStream_t stream, char *err, size_t errl
             if (!encode_tmap_2d(&tks, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.k_scale, a.page_size, a.num_pages,
                                 (uint64_t)a.page_size * 4, a.page_size, 1, CU_TENSOR_MAP_SWIZZLE_NONE, err, errlen))
                 return DSA_ERR_CUDA;
-            static bool flat_attr[64] = {};
-            if (dev < 64 && !flat_attr[dev]) {
-                cudaError_t e = cudaFuncSetAttribute(indexer_paged_flat_kernel<HI, DI>,
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, F::SMEM);
-                if (e != cudaSuccess) {
-                    snprintf(err, errlen, "cudaFuncSetAttribute(indexer flat): %s", cudaGetErrorString(e));
-                    return DSA_ERR_CUDA;
-                }
-                flat_attr[dev] = true;
+            static std::atomic<bool> flat_attr[64];
+            if (cudaError_t e_attr = raise_smem_limit_once(indexer_paged_flat_kernel<HI, DI>, F::SMEM, flat_attr);
+                e_attr != cudaSuccess) {
+                snprintf(err, errlen, "cudaFuncSetAttribute(indexer flat): %s", cudaGetErrorString(e_attr));
+                return DSA_ERR_CUDA;
             }
             p.splits = 1;
             cudaError_t e = launch_pdl(indexer_paged_flat_kernel<HI, DI>, dim3(2 * num_sms()), dim3(F::THREADS),

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace dsa {
 
 // Encodes a 2-D tiled tensor map (dims/box in elements, row stride in bytes).
@@ -17,6 +19,25 @@ int num_sms();
 
 // Records a message for dsa_last_error() on this host thread and returns `code`.
 int report_error(int code, const char *fmt, ...);
+
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per device (`done` holds one flag per device; a device past the
+// table's end sets it on every call).  Two host threads may both find the flag
+// clear and both set the attribute: the call is idempotent and the flag atomic.
+template <typename... KArgs>
+cudaError_t raise_smem_limit_once(void (*kernel)(KArgs...), int bytes, std::atomic<bool> (&done)[64])
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 64 && done[dev].load(std::memory_order_acquire))
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && dev < 64)
+        done[dev].store(true, std::memory_order_release);
+    return e;
+}
 
 // Launches `kernel` on `stream` with programmatic dependent launch allowed
 // (the kernel must call grid_dep_wait() before touching global memory) and,

@@ -869,16 +869,11 @@ int launch_topk(const TopkArgs &a, cudaStream_t stream, char *err, size_t errlen
         // Few rows (decode): each row's latency is the cost, so a row gets as
         // many CTAs as the SMs allow and is read once.  Many rows (prefill): one
         // small CTA per row keeps four rows in flight per SM.
-        static bool attr_set[64] = {};
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (dev < 64 && !attr_set[dev]) {
-            e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTopk);
-            if (e != cudaSuccess) {
-                snprintf(err, errlen, "cudaFuncSetAttribute(topk): %s", cudaGetErrorString(e));
-                return DSA_ERR_CUDA;
-            }
-            attr_set[dev] = true;
+        static std::atomic<bool> attr_set[64];
+        if (cudaError_t e_attr = raise_smem_limit_once(topk_cluster_kernel, kSmemTopk, attr_set);
+            e_attr != cudaSuccess) {
+            snprintf(err, errlen, "cudaFuncSetAttribute(topk): %s", cudaGetErrorString(e_attr));
+            return DSA_ERR_CUDA;
         }
         int cs = 1;
         while (cs < 8 && a.T * cs * 2 <= sms)
@@ -887,16 +882,10 @@ int launch_topk(const TopkArgs &a, cudaStream_t stream, char *err, size_t errlen
         e = launch_pdl(topk_cluster_kernel, dim3(static_cast<unsigned>(clusters * cs)), dim3(kThreads), kSmemTopk,
                        stream, static_cast<unsigned>(cs), a.logits, a.ld, a.T, a.valid_len, a.k, a.idx, status);
     } else {
-        static bool rows_attr[64] = {};
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (dev < 64 && !rows_attr[dev]) {
-            e = cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowSmem);
-            if (e != cudaSuccess) {
-                snprintf(err, errlen, "cudaFuncSetAttribute(topk rows): %s", cudaGetErrorString(e));
-                return DSA_ERR_CUDA;
-            }
-            rows_attr[dev] = true;
+        static std::atomic<bool> rows_attr[64];
+        if (cudaError_t e_attr = raise_smem_limit_once(topk_rows_kernel, kRowSmem, rows_attr); e_attr != cudaSuccess) {
+            snprintf(err, errlen, "cudaFuncSetAttribute(topk rows): %s", cudaGetErrorString(e_attr));
+            return DSA_ERR_CUDA;
         }
         const int grid = a.T < 65535 * 4 ? a.T : 65535 * 4;
         e = launch_pdl(topk_rows_kernel, dim3(grid), dim3(kRowThreads), kRowSmem, stream, 1, a.logits, a.ld, a.T,
