@@ -36,7 +36,8 @@ import dsa_workloads as W  # noqa: E402
 METRIC = "DSA tokens/s at L=32K,k=2048 (prefill) and decode; % of FP8/BF16/HBM roofline"
 WORKLOAD = "prefill_32k"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s): the derived FP8 peak, a side column
+OTHER_WORKLOADS = ("tiny", "prefill_4k", "chunked_128k")
 NOMINAL = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0, "fp8_tflops": 4500.0}  # GB300 datasheet, dense
 PROFILES = os.path.join(ROOT, "profiles")
 
@@ -64,6 +65,66 @@ def prefill_work(L: int, k: int, HI: int, dI: int, H: int, D: int = 576, Dv: int
     mla_bytes = 2 * L * H * D + 2 * L * D + 4 * L * k + 2 * L * H * Dv + 4 * L * H
     return dict(indexer_flop=idx_flop, indexer_bytes=idx_bytes, topk_bytes=topk_bytes, mla_flop=mla_flop,
                 mla_bytes=mla_bytes, selected_pairs=sel.sum(), key_rows=t1.sum())
+
+
+def workload_desc(cfg: W.Config) -> str:
+    """One string per workload, the same in both arms of the bench."""
+    if cfg.chunk:
+        return (f"{cfg.name}: batch 1, L={cfg.L} causal in {cfg.L // cfg.chunk} chunks of {cfg.chunk} query rows, each "
+                f"over its whole prefix, k={cfg.k}, indexer H_I={cfg.HI} d_I={cfg.dI} FP8 E4M3 per-token scales, "
+                f"MLA H={cfg.H} D={cfg.D} Dv={cfg.Dv} bf16, inputs N(0,1)")
+    return (f"{cfg.name}: batch 1, L={cfg.L} causal, k={cfg.k}, indexer H_I={cfg.HI} d_I={cfg.dI} FP8 E4M3 per-token "
+            f"scales, MLA H={cfg.H} D={cfg.D} Dv={cfg.Dv} bf16, inputs N(0,1)")
+
+
+def clock_adjusted(burst: float, clk: dict, what: str):
+    """The peak a kernel timed inside this run can reach: the burst figure when the run's
+    clock record shows the SM clock held at its maximum with no throttle reason, else
+    the burst figure scaled by median / max SM clock.  Returns (peak, how)."""
+    sm, mx = clk.get("sm_mhz"), clk.get("sm_max_mhz")
+    reasons = [r for r in clk.get("reasons", []) if r != "nvidia-smi unavailable"]
+    if sm and mx and sm >= 0.97 * mx and not reasons:
+        return burst, f"{what} burst (SM clock median {sm:.0f} of max {mx:.0f} MHz, no throttle reason)"
+    if sm and mx:
+        return burst * sm / mx, (f"{what} burst x median/max SM clock ({sm:.0f}/{mx:.0f} MHz; "
+                                 f"reasons {reasons or 'none'})")
+    return burst, f"{what} burst (no clock record)"
+
+
+def measure_matmul_peaks(dev, n: int = 8192, reps: int = 10):
+    """Dense GEMM throughput on this GPU, best of `reps` single n^3 products (burst):
+    bf16 through torch.matmul and FP8 E4M3 (fp32 accumulate, bf16 out) through
+    torch._scaled_mm, the library routes to the tensor cores.  FP8 is None if the
+    routine is unavailable here."""
+    g = torch.Generator(device=dev).manual_seed(0)
+    a = torch.randn((n, n), generator=g, device=dev).to(torch.bfloat16)
+    b = torch.randn((n, n), generator=g, device=dev).to(torch.bfloat16)
+
+    def best(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return 2.0 * n ** 3 / (min(ts) / 1e3) / 1e12
+
+    out = {"n": n, "bf16_tflops": best(lambda: torch.matmul(a, b)), "fp8_tflops": None}
+    try:
+        a8, b8 = a.to(torch.float8_e4m3fn), b.to(torch.float8_e4m3fn)
+        one = torch.ones((), dtype=torch.float32, device=dev)
+        out["fp8_tflops"] = best(lambda: torch._scaled_mm(a8, b8.t(), scale_a=one, scale_b=one,
+                                                          out_dtype=torch.bfloat16))
+    except Exception as e:  # noqa: BLE001
+        out["fp8_error"] = f"{type(e).__name__}: {e}"[:200]
+    out["how"] = (f"best of {reps} single {n}^3 products after 3 warm-ups, CUDA events: torch.matmul bf16, "
+                  "torch._scaled_mm E4M3 x E4M3 (per-tensor scales, bf16 out)")
+    return out
 
 
 class ClockSampler:
@@ -244,13 +305,15 @@ def run_reference(args, rank, world):
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 0, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": est * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": f"{args.workload}: L={L} causal, k={cfg.k}, H_I={cfg.HI}, d_I={cfg.dI}, H={cfg.H}, "
-                                   "D=576, Dv=512", "l2": "n/a (CPU)"},
+            "config": {"workload": workload_desc(cfg), "l2": "n/a (CPU)"},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": f"each step: 48 distinct query rows drawn from {len(pool)} rows spread over all {L} "
-                                       f"positions (all keys and selections); "
-                                       f"per-unit rates extrapolated to the full {L}-row prefill; median over "
-                                       f"{args.steps} steps ({statistics.mean(walls):.2f} s CPU wall per step)"},
+                                       f"positions (all keys and selections), timed on the host cores; "
+                                       f"per-unit rates extrapolated to the full {L}-row prefill (indexer and top-k "
+                                       f"per key-row, attention per selected pair); median over {args.steps} steps "
+                                       f"({statistics.mean(walls):.2f} s CPU wall per step). value and ms_per_step "
+                                       f"are that extrapolation: a whole step is never run, so ms_per_step "
+                                       f"({est:.0f} s) is far longer than this run's own wall time"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -293,6 +356,133 @@ def time_prefill(dsa, x, b, cfg, steps, warmup, flush):
     torch.cuda.synchronize()
     st = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in ev])  # ms
     return step_ms, st
+
+
+def stage_records(work, stage_ms, L, pk):
+    """Per-stage ms, throughput and roofline fractions of one prefill pass.  `pk` holds the
+    peaks this run's kernels are held to (see `run_peaks`)."""
+    idx_tflops = work["indexer_flop"] / (stage_ms[0] / 1e3) / 1e12
+    topk_gbs = work["topk_bytes"] / (stage_ms[1] / 1e3) / 1e9
+    mla_tflops = work["mla_flop"] / (stage_ms[2] / 1e3) / 1e12
+    return {
+        "indexer": {"ms": float(stage_ms[0]), "tflops": idx_tflops, "bound": "tensor (fp8)",
+                    "peak": pk["fp8"], "frac": idx_tflops / pk["fp8"], "peak_source": pk["fp8_how"],
+                    "frac_derived_fp8": idx_tflops / pk["fp8_derived"],
+                    "frac_nominal": idx_tflops / NOMINAL["fp8_tflops"],
+                    "flop": work["indexer_flop"], "tokens_per_s": L / (stage_ms[0] / 1e3)},
+        "topk": {"ms": float(stage_ms[1]), "gbs": topk_gbs, "bound": "hbm", "peak": pk["hbm"],
+                 "frac": topk_gbs / pk["hbm"], "frac_nominal": topk_gbs / NOMINAL["hbm_gbs"],
+                 "bytes": work["topk_bytes"], "tokens_per_s": L / (stage_ms[1] / 1e3)},
+        "sparse_mla": {"ms": float(stage_ms[2]), "tflops": mla_tflops, "bound": "tensor (bf16)",
+                       "peak": pk["bf16"], "frac": mla_tflops / pk["bf16"], "peak_source": pk["bf16_how"],
+                       "frac_sustained": mla_tflops / pk["bf16_sustained"],
+                       "frac_nominal": mla_tflops / NOMINAL["bf16_tflops"], "flop": work["mla_flop"],
+                       "tokens_per_s": L / (stage_ms[2] / 1e3)},
+    }
+
+
+def run_peaks(peaks, peaks_src, clk, mm):
+    """The denominators for one timed region: BF16 from the peaks file's burst figure and
+    FP8 from this process's own measured burst figure (the derived 2 x BF16 when the
+    measurement failed), each taken at the clock the region ran at (`clock_adjusted`)."""
+    bf16, bf16_how = clock_adjusted(peaks["bf16_tflops"], clk, f"{peaks_src} bf16")
+    fp8_derived = FP8_OVER_BF16 * bf16
+    if mm and mm.get("fp8_tflops"):
+        fp8, fp8_how = clock_adjusted(mm["fp8_tflops"], clk, "measured fp8 (torch._scaled_mm 8192^3 in this run)")
+    else:
+        fp8, fp8_how = fp8_derived, f"derived: {FP8_OVER_BF16} x ({bf16_how}); the FP8 measurement failed"
+    return {"bf16": bf16, "bf16_how": bf16_how, "fp8": fp8, "fp8_how": fp8_how, "fp8_derived": fp8_derived,
+            "bf16_sustained": peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]), "hbm": peaks["hbm_gbs"]}
+
+
+def prefill_buffers(cfg, x, dev, rows=None):
+    rows = cfg.L if rows is None else rows
+    return {"logits": torch.empty((rows, cfg.L), dtype=torch.float32, device=dev),
+            "valid_len": x["q_pos"] + 1,
+            "idx": torch.empty((rows, cfg.k), dtype=torch.int32, device=dev),
+            "out": torch.empty((cfg.L, cfg.H, cfg.Dv), dtype=torch.bfloat16, device=dev),
+            "lse": torch.empty((cfg.L, cfg.H), dtype=torch.float32, device=dev)}
+
+
+def chunked_stage_calls(dsa, x, b, cfg):
+    """The three stages of each chunk of a chunked prefill, as (stage, thunk) pairs in
+    launch order: chunk c holds query rows [C c, C (c + 1)) over keys [0, C (c + 1))."""
+    C = cfg.chunk
+    calls = []
+    for c in range(cfg.L // C):
+        r0, r1 = c * C, (c + 1) * C
+        calls.append((0, lambda r0=r0, r1=r1: dsa.dsa_indexer_logits(
+            x["q8"][r0:r1], x["qs"][r0:r1], x["w"][r0:r1], x["k8"][:r1], x["ks"][:r1], x["q_pos"][r0:r1],
+            b["logits"])))
+        calls.append((1, lambda r0=r0, r1=r1: dsa.dsa_topk(b["logits"], b["valid_len"][r0:r1], cfg.k, b["idx"])))
+        calls.append((2, lambda r0=r0, r1=r1: dsa.dsa_sparse_mla_prefill(
+            x["q"][r0:r1], x["kv"][:r1], b["idx"], cfg.sm_scale, b["out"][r0:r1], b["lse"][r0:r1])))
+    return calls
+
+
+def time_calls(calls, steps, warmup, flush):
+    """Whole steps of `calls` (events only at step boundaries), then the same steps with an
+    event around every call, summed per stage.  Returns (step ms [steps], stage ms [3])."""
+    for _ in range(warmup):
+        for _, f in calls:
+            f()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for e in ev:
+        flush.zero_()
+        e[0].record()
+        for _, f in calls:
+            f()
+        e[1].record()
+    torch.cuda.synchronize()
+    step_ms = np.array([e[0].elapsed_time(e[1]) for e in ev])
+    per = np.zeros((steps, 3))
+    for s in range(steps):
+        flush.zero_()
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+        es[0].record()
+        for i, (_, f) in enumerate(calls):
+            f()
+            es[i + 1].record()
+        torch.cuda.synchronize()
+        for i, (st, _) in enumerate(calls):
+            per[s, st] += es[i].elapsed_time(es[i + 1])
+    return step_ms, per.mean(0)
+
+
+def workload_bench(dsa, name, steps, warmup, flush, peaks, peaks_src, mm, dev):
+    """One more configured prefill workload (tiny, L = 4096, or the chunked L = 131072):
+    per-stage ms, tokens/s and roofline fractions, clocks sampled over its own timed region."""
+    cfg = W.CONFIGS[name]
+    L = cfg.L
+    x = W.prefill_inputs(cfg, dev)
+    b = prefill_buffers(cfg, x, dev, rows=cfg.chunk or None)
+    if cfg.chunk:
+        calls = chunked_stage_calls(dsa, x, b, cfg)
+    else:
+        calls = [(0, lambda: dsa.dsa_indexer_logits(x["q8"], x["qs"], x["w"], x["k8"], x["ks"], x["q_pos"],
+                                                    b["logits"])),
+                 (1, lambda: dsa.dsa_topk(b["logits"], b["valid_len"], cfg.k, b["idx"])),
+                 (2, lambda: dsa.dsa_sparse_mla_prefill(x["q"], x["kv"], b["idx"], cfg.sm_scale, b["out"],
+                                                        b["lse"]))]
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    step_ms, stage_ms = time_calls(calls, steps, warmup, flush)
+    clk = clocks.stop()
+    pk = run_peaks(peaks, peaks_src, clk, mm)
+    work = prefill_work(L, cfg.k, cfg.HI, cfg.dI, cfg.H)
+    ms = float(step_ms.mean())
+    rec = {"workload": workload_desc(cfg), "ms_per_step": ms, "tokens_per_s": L / (ms / 1e3),
+           "steps": steps, "warmup": warmup, "launches_per_step": len(calls),
+           "stages": stage_records(work, stage_ms, L, pk), "clocks": clk,
+           "l2": "flushed before every timed step (256 MB write, outside the timed events)"}
+    if cfg.chunk:
+        # the logits each chunk's indexer writes and its top-k reads back (causal part only)
+        rec["logits_bytes_write_read"] = 8.0 * work["key_rows"]
+        rec["logits_hbm_ms_at_peak"] = rec["logits_bytes_write_read"] / (pk["hbm"] * 1e9) * 1e3
+    del x, b, calls
+    torch.cuda.empty_cache()
+    return rec
 
 
 def quantize_bench(dsa, cfg, steps, warmup, flush, hbm, dev):
@@ -449,6 +639,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="skip tiny, L=4096 and the chunked L=131072")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -470,14 +661,12 @@ def main():
 
     dsa.load_library()  # fails loudly when the CUDA library is missing
     peaks, peaks_src = load_peaks()
+    mm = measure_matmul_peaks(dev)
+    torch.cuda.empty_cache()
     cfg = W.CONFIGS[args.workload]
     L = cfg.L
     x = W.prefill_inputs(cfg, dev)
-    b = {"logits": torch.empty((L, L), dtype=torch.float32, device=dev),
-         "valid_len": x["q_pos"] + 1,
-         "idx": torch.empty((L, cfg.k), dtype=torch.int32, device=dev),
-         "out": torch.empty((L, cfg.H, 512), dtype=torch.bfloat16, device=dev),
-         "lse": torch.empty((L, cfg.H), dtype=torch.float32, device=dev)}
+    b = prefill_buffers(cfg, x, dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     if dist:
@@ -497,12 +686,9 @@ def main():
     stage_ms = st.mean(0)
     ms, value = aggregate_over_ranks(float(step_ms.mean()), L, dist, dev)
     work = prefill_work(L, cfg.k, cfg.HI, cfg.dI, cfg.H)
-    bf16_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    fp8_peak = FP8_OVER_BF16 * bf16_peak
-    hbm = peaks["hbm_gbs"]
-    mla_tflops = work["mla_flop"] / (stage_ms[2] / 1e3) / 1e12
-    idx_tflops = work["indexer_flop"] / (stage_ms[0] / 1e3) / 1e12
-    topk_gbs = work["topk_bytes"] / (stage_ms[1] / 1e3) / 1e9
+    pk = run_peaks(peaks, peaks_src, clk, mm)
+    stages = stage_records(work, stage_ms, L, pk)
+    mla = stages["sparse_mla"]
     traffic = recorded_traffic(f"sparse_mla_{args.workload}", ["sparse_mla.cu", "common.cuh"])
 
     out_hash = None
@@ -525,33 +711,19 @@ def main():
         "vs_baseline": None,
         "dtype": "fp8e4m3+bf16 (fp32 accumulate)",
         "data": "synthetic",
-        "config": {"workload": f"{args.workload}: batch 1, L={L} causal, k={cfg.k}, indexer H_I={cfg.HI} d_I={cfg.dI} "
-                               f"FP8 E4M3 per-token scales, MLA H={cfg.H} D=576 Dv=512 bf16, inputs N(0,1)",
+        "config": {"workload": workload_desc(cfg),
                    "l2": "flushed before every timed step (256 MB write, outside the timed events)",
                    "timing": "ms_per_step: CUDA events at step boundaries only (kernels launched with programmatic "
                              "dependent launch overlap their launch with the previous kernel's tail); stage ms: "
                              "a second pass of the same steps with an event between stages",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"bound": "tensor", "kernel": "sparse_mla_prefill", "achieved": mla_tflops,
-                     "peak": bf16_peak, "unit": "TFLOP/s", "frac": mla_tflops / bf16_peak,
-                     "frac_nominal": mla_tflops / NOMINAL["bf16_tflops"],
-                     "traffic": traffic,
-                     "peak_source": f"{peaks_src} bf16 sustained (kernel timed inside the step)",
+        "roofline": {"bound": "tensor", "kernel": "sparse_mla_prefill", "achieved": mla["tflops"],
+                     "peak": pk["bf16"], "unit": "TFLOP/s", "frac": mla["frac"],
+                     "frac_sustained": mla["frac_sustained"], "frac_nominal": mla["frac_nominal"],
+                     "traffic": traffic, "peak_source": pk["bf16_how"],
                      "algorithmic_flop_per_launch": work["mla_flop"]},
-        "stages": {
-            "indexer": {"ms": float(stage_ms[0]), "tflops": idx_tflops, "bound": "tensor (fp8)",
-                        "peak": fp8_peak, "frac": idx_tflops / fp8_peak,
-                        "frac_nominal": idx_tflops / NOMINAL["fp8_tflops"],
-                        "peak_source": f"{peaks_src} bf16 sustained x {FP8_OVER_BF16} (nominal fp8/bf16 ratio)",
-                        "flop": work["indexer_flop"], "tokens_per_s": L / (stage_ms[0] / 1e3)},
-            "topk": {"ms": float(stage_ms[1]), "gbs": topk_gbs, "bound": "hbm", "peak": hbm,
-                     "frac": topk_gbs / hbm, "frac_nominal": topk_gbs / NOMINAL["hbm_gbs"], "bytes": work["topk_bytes"],
-                     "tokens_per_s": L / (stage_ms[1] / 1e3)},
-            "sparse_mla": {"ms": float(stage_ms[2]), "tflops": mla_tflops, "bound": "tensor (bf16)",
-                           "peak": bf16_peak, "frac": mla_tflops / bf16_peak,
-                           "frac_nominal": mla_tflops / NOMINAL["bf16_tflops"], "flop": work["mla_flop"],
-                           "tokens_per_s": L / (stage_ms[2] / 1e3)},
-        },
+        "stages": stages,
+        "matmul_peaks": mm,
         "clocks": clk,
         "gpu_launches": 3 * args.steps,
         "device_status": status,
@@ -563,12 +735,20 @@ def main():
         line["e2e"]["value"] *= world
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, x)
+    del b, x
+    torch.cuda.empty_cache()
     if not args.no_decode:
-        del b, x
-        torch.cuda.empty_cache()
-        line["stages"]["quantize"] = quantize_bench(dsa, cfg, args.steps, args.warmup, flush, hbm, dev)
+        line["stages"]["quantize"] = quantize_bench(dsa, cfg, args.steps, args.warmup, flush, pk["hbm"], dev)
         torch.cuda.empty_cache()
         line["decode"] = decode_bench(dsa, args.steps, args.warmup, flush, peaks, dev)
+    if not args.no_workloads:
+        line["workloads"] = {}
+        for name in OTHER_WORKLOADS:
+            if name == args.workload:
+                continue
+            n_steps = 3 if W.CONFIGS[name].chunk else max(3, min(args.steps, 10))
+            line["workloads"][name] = workload_bench(dsa, name, n_steps, args.warmup, flush, peaks, peaks_src, mm,
+                                                     dev)
     if dist:
         dist.barrier()
         dist.destroy_process_group()
