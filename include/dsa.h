@@ -172,6 +172,48 @@ int dsa_topk(const float *logits, int64_t ld, int T, const int32_t *valid_len,
              int k, int32_t *idx, dsa_stream_t stream);
 
 /*
+ * dsa_indexer_topk: stages 1 and 2 in one call, without the index scores ever
+ * reaching memory.
+ *
+ * Result: exactly what dsa_indexer_logits (contiguous keys) followed by
+ * dsa_topk with valid_len[r] = min(q_pos[r] + 1, S) writes to idx, byte for
+ * byte: for each query row r, the k keys s in [0, q_pos[r]] with the highest
+ * index score (score descending, position ascending), in ascending order,
+ * padded with -1 (release summary "DeepSeek-V3.2-Exp: Boosting Long-Context
+ * Efficiency with DeepSeek Sparse Attention", section "Method"; "AMD Instinct
+ * MI355X GPUs Power DeepSeek-V3.2-Exp", section "Computational Efficiency":
+ * attention drops from O(L^2) to O(Lk), which leaves the indexer's L x L
+ * scores as the long-context cost; here they are neither written nor read).
+ *
+ * How: a per-row threshold from the scores of 2048 keys sampled at a fixed
+ * stride (about 2k of the row's keys score at or above it; rows of at most
+ * max(4096, 4k) keys take every key), then the indexer appends only the keys
+ * at or above it to per-row lists, and an exact top-k runs over each list.  A
+ * row whose list misses [k, max(4096, 4k)] (a row unlike its samples) is
+ * redone from its full scores, so the result never depends on the sample.
+ *
+ *   q8, q_scale, w, q_pos, k8, k_scale, S: as for dsa_indexer_logits with
+ *             contiguous keys ([S, d_I] codes, [S] scales); (H_I, d_I) =
+ *             (64, 128) or (32, 128); 1 <= S <= DSA_INDEXER_TOPK_MAX_KEYS.
+ *   k         1 <= k <= 4096;   idx [T, k] int32 output.
+ *   workspace a device buffer of dsa_indexer_topk_workspace_size(T, S, H_I,
+ *             d_I, k) bytes, 256-byte aligned, owned by the caller, used only
+ *             while the call's kernels run on `stream` (calls sharing one must
+ *             be ordered).  It holds the sampled keys and scores, the per-row
+ *             candidate lists (T x max(4096, 4k) entries of 8 bytes) and, for
+ *             the rows redone from full scores, T x S fp32 scores: most of it
+ *             stays untouched; callers with long rows pass rows in chunks.
+ * A position q_pos[r] >= S is clamped to S-1 and flagged DSA_DEV_BAD_POSITION.
+ */
+#define DSA_INDEXER_TOPK_MAX_KEYS 262144
+int dsa_indexer_topk(const void *q8, const float *q_scale, const float *w, int T, int H_I, int d_I,
+                     const void *k8, const float *k_scale, int S, const int32_t *q_pos,
+                     int k, int32_t *idx, void *workspace, size_t workspace_bytes, dsa_stream_t stream);
+
+/* Bytes of workspace dsa_indexer_topk needs (0 on unsupported sizes). */
+size_t dsa_indexer_topk_workspace_size(int T, int S, int H_I, int d_I, int k);
+
+/*
  * dsa_sparse_mla_prefill: MQA-mode sparse MLA over the selected rows (stage 3).
  *
  * For query row t, head h and its valid selected rows s_i = idx[t*k + i]

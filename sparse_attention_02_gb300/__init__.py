@@ -60,7 +60,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.dsa_selftest_wait_timeout.restype = i32
     lib.dsa_sparse_mla_decode_workspace_size.restype = sz
     lib.dsa_sparse_mla_decode_workspace_size.argtypes = [i32, i32, i32]
-    for name in ("dsa_quantize_fp8", "dsa_indexer_logits", "dsa_topk", "dsa_sparse_mla_prefill", "dsa_sparse_mla_decode_paged",
+    lib.dsa_indexer_topk.argtypes = [P, P, P, i32, i32, i32, P, P, i32, P, i32, P, P, sz, P]
+    lib.dsa_indexer_topk_workspace_size.restype = sz
+    lib.dsa_indexer_topk_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    for name in ("dsa_quantize_fp8", "dsa_indexer_logits", "dsa_topk", "dsa_indexer_topk", "dsa_sparse_mla_prefill",
+                 "dsa_sparse_mla_decode_paged",
                  "dsa_sparse_mla_decode_paged_noalloc", "dsa_prefill_host", "dsa_get_device_status"):
         getattr(lib, name).restype = i32
     if path is None:
@@ -182,6 +186,40 @@ def dsa_topk(logits, valid_len, k: int, idx, stream=None):
         raise ValueError("inconsistent shapes")
     _check(load_library().dsa_topk(_ptr(logits), logits.stride(0), T, _ptr(valid_len), k, _ptr(idx),
                                    _stream(stream)))
+    return idx
+
+
+def dsa_indexer_topk_workspace_size(T: int, S: int, H_I: int, d_I: int, k: int) -> int:
+    return int(load_library().dsa_indexer_topk_workspace_size(T, S, H_I, d_I, k))
+
+
+def dsa_indexer_topk(q8, q_scale, w, k8, k_scale, q_pos, k: int, idx, workspace=None, stream=None):
+    """Fused indexer -> top-k: the top-k key positions of each query row into ``idx`` [T, k]
+    (ascending, -1 padded) without writing the index scores.  Inputs as for
+    dsa_indexer_logits with contiguous keys.  ``workspace``: a uint8 CUDA tensor of at least
+    dsa_indexer_topk_workspace_size(T, S, H_I, d_I, k) bytes; taken from PyTorch's
+    allocator when None."""
+    _need(q8, torch.uint8, "q8", 3)
+    T, HI, dI = q8.shape
+    _need(q_scale, torch.float32, "q_scale", 1)
+    _need(w, torch.float32, "w", 2)
+    _need(q_pos, torch.int32, "q_pos", 1)
+    _need(k8, torch.uint8, "k8", 2)
+    _need(k_scale, torch.float32, "k_scale", 1)
+    _need(idx, torch.int32, "idx", 2)
+    S = k8.shape[0]
+    if q_scale.shape[0] != T or tuple(w.shape) != (T, HI) or q_pos.shape[0] != T or tuple(idx.shape) != (T, k) \
+            or k8.shape[1] != dI or k_scale.shape[0] != S:
+        raise ValueError("inconsistent shapes")
+    if workspace is None:
+        need = dsa_indexer_topk_workspace_size(T, S, HI, dI, k)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q8.device)
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    _same_device(workspace, "workspace")
+    _check(load_library().dsa_indexer_topk(_ptr(q8), _ptr(q_scale), _ptr(w), T, HI, dI, _ptr(k8), _ptr(k_scale), S,
+                                           _ptr(q_pos), k, _ptr(idx), _ptr(workspace),
+                                           workspace.numel() * workspace.element_size(), _stream(stream)))
     return idx
 
 

@@ -187,6 +187,41 @@ int dsa_indexer_logits(const void *q8, const float *q_scale, const float *w, int
     return rc == DSA_OK ? ok() : rc;
 }
 
+size_t dsa_indexer_topk_workspace_size(int T, int S, int H_I, int d_I, int k)
+{
+    if (T < 0 || S < 1 || S > DSA_INDEXER_TOPK_MAX_KEYS || k < 1 || k > 4096 || d_I != 128 ||
+        (H_I != 64 && H_I != 32))
+        return 0;
+    return indexer_topk_workspace_bytes(T, S, d_I, k);
+}
+
+int dsa_indexer_topk(const void *q8, const float *q_scale, const float *w, int T, int H_I, int d_I, const void *k8,
+                     const float *k_scale, int S, const int32_t *q_pos, int k, int32_t *idx, void *workspace,
+                     size_t workspace_bytes, dsa_stream_t stream)
+{
+    if (T < 0)
+        return fail(DSA_ERR_INVALID_ARG, "T < 0");
+    if (T == 0)
+        return ok();
+    if (!q8 || !q_scale || !w || !k8 || !k_scale || !q_pos || !idx)
+        return fail(DSA_ERR_INVALID_ARG, "null pointer argument");
+    if (d_I != 128 || (H_I != 64 && H_I != 32))
+        return fail(DSA_ERR_UNSUPPORTED, "fused indexer -> top-k: (H_I, d_I) must be (64, 128) or (32, 128)");
+    if (S < 1 || S > DSA_INDEXER_TOPK_MAX_KEYS)
+        return fail(DSA_ERR_UNSUPPORTED, "fused indexer -> top-k: S must be in [1, %d]", DSA_INDEXER_TOPK_MAX_KEYS);
+    if (k < 1 || k > 4096)
+        return fail(DSA_ERR_UNSUPPORTED, "k must be in [1, 4096]");
+    if (!aligned16(q8) || !aligned16(k8))
+        return fail(DSA_ERR_ALIGNMENT, "q8 and k8 must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(DSA_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+    if (!workspace || workspace_bytes < indexer_topk_workspace_bytes(T, S, d_I, k))
+        return fail(DSA_ERR_WORKSPACE, "workspace missing or smaller than dsa_indexer_topk_workspace_size");
+    IndexerTopkArgs a{q8, q_scale, w, T, H_I, d_I, k8, k_scale, S, q_pos, k, idx, workspace, workspace_bytes};
+    int rc = launch_indexer_topk(a, reinterpret_cast<cudaStream_t>(stream), t_err, sizeof t_err);
+    return rc == DSA_OK ? ok() : rc;
+}
+
 int dsa_quantize_fp8(const float *x, int64_t rows, int64_t cols, int scale_mode, void *codes, float *scale,
                      dsa_stream_t stream)
 {

@@ -103,13 +103,27 @@ struct Params {
     int64_t ld;
     int T, S, max_pages, num_pages, page_size, splits;
     unsigned *status;
+    // candidate mode and row filter (see IndexerArgs)
+    const float *thr;
+    uint32_t *cand_key;
+    int32_t *cand_idx;
+    int32_t *cand_cnt;
+    int cap;
+    const int32_t *row_flag;
 };
 
-template <int HI, int DI, bool PAGED>
+// FUSED: candidate mode.  Instead of writing logits, the epilogue appends
+// every key whose score is >= the row's threshold to the row's candidate list
+// (warp-aggregated slots from a shared-memory counter per row); the counts go
+// to cand_cnt when the CTA ends.  Same arithmetic, so the same fp32 scores.
+template <int HI, int DI, bool PAGED, bool FUSED = false>
 __global__ void __launch_bounds__(IdxCfg<HI, DI, PAGED>::THREADS, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k, Params p)
 {
     using C = IdxCfg<HI, DI, PAGED>;
+    static_assert(!FUSED || (C::FRAG && C::R <= 8), "candidate mode: fragment epilogue, at most 8 rows per CTA");
+    __shared__ float thr_s[FUSED ? C::R : 1];
+    __shared__ int cnt_s[FUSED ? C::R : 1];
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -133,6 +147,14 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI, PAGED>::THREADS, 1)
 
     grid_dep_wait();
     grid_dep_launch();
+    if (p.row_flag) {
+        // row filter: a CTA none of whose rows is flagged has nothing to do
+        int any = 0;
+        for (int i = 0; i < C::R; ++i)
+            any |= (r0 + i < p.T) ? p.row_flag[r0 + i] : 0;
+        if (!any)
+            return; // uniform
+    }
     // ---- setup: row positions, folded weights, tile range
     const int64_t key_limit = PAGED ? (int64_t)p.max_pages * p.page_size : (int64_t)p.S;
     const int64_t lim = (key_limit < p.ld ? key_limit : p.ld) - 1;
@@ -148,6 +170,10 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI, PAGED>::THREADS, 1)
             pos = qp < 0 ? -1 : (int)qp;
         }
         pos_s[threadIdx.x] = pos;
+        if constexpr (FUSED) {
+            thr_s[threadIdx.x] = r < p.T ? p.thr[r] : INFINITY;
+            cnt_s[threadIdx.x] = 0;
+        }
     }
     for (int i = threadIdx.x; i < C::R * HI; i += C::THREADS) {
         const int r = r0 + i / HI;
@@ -181,8 +207,13 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI, PAGED>::THREADS, 1)
     }
     __syncthreads();
     const int kt0 = tiles_s[0], kt1 = tiles_s[1];
-    if (kt1 <= kt0)
+    if (kt1 <= kt0) {
+        if constexpr (FUSED) {
+            if (threadIdx.x < C::R && r0 + threadIdx.x < p.T)
+                p.cand_cnt[r0 + threadIdx.x] = 0;
+        }
         return; // uniform: nothing to score in this split
+    }
 
     if (warp == 1) {
         tmem_alloc(sbase + C::OFF_MISC, C::TMEM_COLS);
@@ -454,8 +485,29 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI, PAGED>::THREADS, 1)
                     for (int i = 0; i < H; ++i) {
                         const int lr = tb + (C::TPW >= 2 ? b0 * H : 0) + i;
                         const int rg = r0 + lr;
-                        if (rg < p.T && s <= pos_s[lr])
-                            p.logits[(int64_t)rg * p.ld + s] = y[i] * ks[l];
+                        if constexpr (!FUSED) {
+                            if (rg < p.T && s <= pos_s[lr])
+                                p.logits[(int64_t)rg * p.ld + s] = y[i] * ks[l];
+                        } else {
+                            const float v = y[i] * ks[l];
+                            const bool f = rg < p.T && s <= pos_s[lr] && v >= thr_s[lr];
+                            const unsigned fm = __ballot_sync(__activemask(), f);
+                            if (f) {
+                                // one shared-memory atomic per (warp, row): lanes of the same row
+                                // take consecutive slots
+                                const unsigned grp = __match_any_sync(fm, lr);
+                                const int leader = __ffs(grp) - 1;
+                                int base = 0;
+                                if (lane == leader)
+                                    base = atomicAdd(&cnt_s[lr], __popc(grp));
+                                base = __shfl_sync(grp, base, leader);
+                                const int slot = base + __popc(grp & ((1u << lane) - 1u));
+                                if (slot < p.cap) {
+                                    p.cand_key[(int64_t)rg * p.cap + slot] = __float_as_uint(v);
+                                    p.cand_idx[(int64_t)rg * p.cap + slot] = s;
+                                }
+                            }
+                        }
                     }
                 }
             }
@@ -566,6 +618,10 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI, PAGED>::THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    if constexpr (FUSED) {
+        if (threadIdx.x < C::R && r0 + threadIdx.x < p.T)
+            p.cand_cnt[r0 + threadIdx.x] = cnt_s[threadIdx.x];
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
@@ -953,6 +1009,12 @@ int launch_cfg(const IndexerArgs &a, cudaStream_t stream, char *err, size_t errl
     p.max_pages = a.max_pages;
     p.num_pages = a.num_pages;
     p.page_size = a.page_size;
+    p.thr = a.thr;
+    p.cand_key = a.cand_key;
+    p.cand_idx = a.cand_idx;
+    p.cand_cnt = a.cand_cnt;
+    p.cap = a.cap;
+    p.row_flag = a.row_flag;
     p.status = device_status_ptr();
     if (!p.status) {
         snprintf(err, errlen, "device status word unavailable");
@@ -996,7 +1058,28 @@ int launch_cfg(const IndexerArgs &a, cudaStream_t stream, char *err, size_t errl
     }
     p.splits = splits;
     dim3 grid(groups, splits);
-    cudaError_t e = launch_pdl(indexer_kernel<HI, DI, PAGED>, grid, dim3(C::THREADS), C::SMEM, stream, 1, tq, tk, p);
+    cudaError_t e;
+    if constexpr (C::FRAG && C::R <= 8) {
+        if (a.cand_key) {
+            static std::atomic<bool> fused_attr[64];
+            if (cudaError_t e_attr = raise_smem_limit_once(indexer_kernel<HI, DI, PAGED, true>, C::SMEM, fused_attr);
+                e_attr != cudaSuccess) {
+                snprintf(err, errlen, "cudaFuncSetAttribute(indexer candidates): %s", cudaGetErrorString(e_attr));
+                return DSA_ERR_CUDA;
+            }
+            e = launch_pdl(indexer_kernel<HI, DI, PAGED, true>, grid, dim3(C::THREADS), C::SMEM, stream, 1, tq, tk, p);
+            if (e != cudaSuccess) {
+                snprintf(err, errlen, "indexer launch: %s", cudaGetErrorString(e));
+                return DSA_ERR_CUDA;
+            }
+            return DSA_OK;
+        }
+    }
+    if (a.cand_key) {
+        snprintf(err, errlen, "indexer: candidate mode needs contiguous keys and H_I in {32, 64}");
+        return DSA_ERR_UNSUPPORTED;
+    }
+    e = launch_pdl(indexer_kernel<HI, DI, PAGED>, grid, dim3(C::THREADS), C::SMEM, stream, 1, tq, tk, p);
     if (e != cudaSuccess) {
         snprintf(err, errlen, "indexer launch: %s", cudaGetErrorString(e));
         return DSA_ERR_CUDA;

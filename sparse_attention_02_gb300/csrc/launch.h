@@ -91,6 +91,15 @@ struct IndexerArgs {
     const int32_t *q_pos;
     float *logits;
     int64_t ld;
+    // Candidate mode (cand_key != nullptr; contiguous keys, H_I in {32, 64}):
+    // no logits are written; a key whose score is >= thr[r] is appended to
+    // row r's list as (raw fp32 score bits, position) in no particular order.
+    const float *thr = nullptr;        // [T]
+    uint32_t *cand_key = nullptr;      // [T, cap]
+    int32_t *cand_idx = nullptr;       // [T, cap]
+    int32_t *cand_cnt = nullptr;       // [T] candidates found (only the first cap are stored)
+    int cap = 0;
+    const int32_t *row_flag = nullptr; // score only rows with row_flag[r] != 0 (nullptr: all rows)
 };
 // Returns 0 on success, else a dsa_status with `err` filled.
 int launch_indexer(const IndexerArgs &a, cudaStream_t stream, char *err, size_t errlen);
@@ -102,8 +111,35 @@ struct TopkArgs {
     const int32_t *valid_len;
     int k;
     int32_t *idx;
+    const int32_t *row_flag = nullptr; // only rows with row_flag[r] != 0 (nullptr: all rows)
 };
 int launch_topk(const TopkArgs &a, cudaStream_t stream, char *err, size_t errlen);
+
+// Fused indexer -> top-k pieces (topk.cu): the per-row threshold from sampled
+// scores, and the exact top-k over each row's candidate list.
+int launch_topk_threshold(const float *samp, int ld_s, int T, const int32_t *q_pos, const int32_t *qpos_s, int S,
+                          int k, int cap, float *thr, cudaStream_t stream, char *err, size_t errlen);
+int launch_topk_candidates(const uint32_t *cand_key, const int32_t *cand_idx, const int32_t *cand_cnt, int cap,
+                           int T, const int32_t *q_pos, int S, int k, int32_t *idx, int32_t *flag,
+                           cudaStream_t stream, char *err, size_t errlen);
+size_t topk_candidates_smem(int S, int cap);
+
+struct IndexerTopkArgs {
+    const void *q8;
+    const float *q_scale;
+    const float *w;
+    int T, HI, dI;
+    const void *k8;
+    const float *k_scale;
+    int S;
+    const int32_t *q_pos;
+    int k;
+    int32_t *idx;
+    void *workspace;
+    size_t workspace_bytes;
+};
+int launch_indexer_topk(const IndexerTopkArgs &a, cudaStream_t stream, char *err, size_t errlen);
+size_t indexer_topk_workspace_bytes(int T, int S, int dI, int k);
 
 struct MlaArgs {
     const void *q;      // [T, H, 576] bf16

@@ -182,8 +182,11 @@ __device__ __forceinline__ void select_bin(const int *hist, int nbins, int k_rem
     __syncthreads();
 }
 
+// The key of the k-th largest of row[0, n) (1 <= k <= n), digit by digit in
+// three histogram passes (12 + 12 + 8 bits); *k_eq receives how many keys
+// equal to it are among the k largest (the rest of them rank below).
 template <int NT, bool kVec>
-__device__ void topk_row(const float *row, int n, int k, int32_t *out, int *hist, int *scratch, int *sel)
+__device__ uint32_t kth_key(const float *row, int n, int k, int *hist, int *scratch, int *sel, int *k_eq)
 {
     // pass 1: top 12 bits
     for (int b = threadIdx.x; b < 4096; b += NT)
@@ -222,9 +225,17 @@ __device__ void topk_row(const float *row, int n, int k, int32_t *out, int *hist
     select_bin<NT>(hist, 256, k_rem, scratch, sel);
     const uint32_t tau = (p1 << 8) | static_cast<uint32_t>(sel[0]);
     k_rem -= sel[1];
-    // k_rem = how many keys equal to tau are kept (the first ones in index order)
-    const int need_eq = k_rem;
+    *k_eq = k_rem;
     __syncthreads();
+    return tau;
+}
+
+template <int NT, bool kVec>
+__device__ void topk_row(const float *row, int n, int k, int32_t *out, int *hist, int *scratch, int *sel)
+{
+    // k_rem = how many keys equal to tau are kept (the first ones in index order)
+    int need_eq;
+    const uint32_t tau = kth_key<NT, kVec>(row, n, k, hist, scratch, sel, &need_eq);
 
     // pass 4: ordered compaction.  Thread i handles elements [4i, 4i+4) of
     // each 4*NT chunk; gt/eq counts are packed (gt << 16 | eq).
@@ -386,19 +397,17 @@ __device__ __forceinline__ int cand_slot(const int *wc, int f)
     return w * kSeg + (f - wc[w]);
 }
 
-// Exact top-k of nc >= k candidates ck/ci listed in ascending index order (ck
-// holds the raw fp32 score bits; the keys are formed as they are read); writes
-// the kept indices to out in that order.
+// Key tau of the k-th largest of nc >= k candidates ck (raw fp32 score bits;
+// the keys are formed as they are read), in any order; *need_eq receives how
+// many candidates equal to tau are among the k largest.
 template <int NT>
-__device__ void select_candidates(const uint32_t *ck, const int32_t *ci, int nc, int k, int32_t *out, int *hist,
-                                  int *sel)
+__device__ uint32_t select_tau(const uint32_t *ck, int nc, int k, int *hist, int *sel, int *need_eq)
 {
     constexpr int NW = NT / 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // hist: two 1024-bin histograms that alternate between passes (the next one
-    // is cleared while warp 0 picks the bin in the current one), then the
-    // per-warp totals of the ordered output and the per-warp minima and maxima.
-    int *wsum = hist + 2048;
+    // is cleared while warp 0 picks the bin in the current one), then NW ints
+    // left to the caller and the per-warp minima and maxima.
     int *mm = hist + 2048 + NW;
     for (int q = threadIdx.x; q < 1024; q += NT)
         hist[q] = 0;
@@ -490,8 +499,20 @@ __device__ void select_candidates(const uint32_t *ck, const int32_t *ci, int nc,
         shift = shift > 10 ? shift - 10 : 0;
         nbins = 1 << (prev - shift);
     }
-    const uint32_t tau = kmin + prefix; // every bit of d fixed: the k-th largest candidate key
-    const int need_eq = k_rem;          // keys equal to tau to keep (the smallest indices)
+    *need_eq = k_rem; // keys equal to tau to keep (the smallest indices)
+    return kmin + prefix; // every bit of d fixed: the k-th largest candidate key
+}
+
+// Exact top-k of nc >= k candidates ck/ci listed in ascending index order (ck
+// holds the raw fp32 score bits); writes the kept indices to out in that order.
+template <int NT>
+__device__ void select_candidates(const uint32_t *ck, const int32_t *ci, int nc, int k, int32_t *out, int *hist,
+                                  int *sel)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int *wsum = hist + 2048; // per-warp totals of the ordered output
+    int need_eq;
+    const uint32_t tau = select_tau<NT>(ck, nc, k, hist, sel, &need_eq);
     // ordered output: thread t walks candidates [t * per, t * per + per); one
     // prefix count over threads of (#greater << 16 | #equal) gives its slots
     const int per = (nc + NT - 1) / NT;
@@ -727,7 +748,7 @@ __device__ bool topk_row_candidates(const float *row, int n, int k, int32_t *out
 
 __global__ void __launch_bounds__(kRowThreads, 4)
     topk_rows_kernel(const float *__restrict__ logits, int64_t ld, int T, const int32_t *__restrict__ valid_len, int k,
-                     int32_t *__restrict__ idx, unsigned *status)
+                     int32_t *__restrict__ idx, unsigned *status, const int32_t *__restrict__ row_flag)
 {
     extern __shared__ __align__(16) uint32_t dsm[];
     uint32_t *ck = dsm;
@@ -739,6 +760,8 @@ __global__ void __launch_bounds__(kRowThreads, 4)
     grid_dep_wait();
     grid_dep_launch();
     for (int row = blockIdx.x; row < T; row += gridDim.x) {
+        if (row_flag && !row_flag[row])
+            continue; // not one of the rows asked for (uniform)
         int n = valid_len[row];
         if (n < 0)
             n = 0;
@@ -762,6 +785,150 @@ __global__ void __launch_bounds__(kRowThreads, 4)
             else
                 topk_row<kRowThreads, false>(r, n, k, out, hist, scratch, sel);
         }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Top-k from the candidate lists of the fused indexer (no logits in memory).
+//
+// Threshold.  Row t holds n = min(q_pos[t] + 1, S) keys.  A row with n <= cap
+// keeps every key (threshold -inf).  Otherwise its m valid samples samp[t, 0, m)
+// (scores of keys at a fixed stride over the keys) give thr[t] = the r-th
+// largest sample, r = ceil(m * 2k / n): about 2k keys of the row score at or
+// above it, so its k largest are among them unless the row is far from what
+// its samples show (then its candidate count misses [k, cap] and the row is
+// redone from full logits; the result is the same).
+__global__ void __launch_bounds__(kRowThreads)
+    topk_threshold_kernel(const float *__restrict__ samp, int ld_s, int T, const int32_t *__restrict__ q_pos,
+                          const int32_t *__restrict__ qpos_s, int S, int k, int cap, float *__restrict__ thr)
+{
+    __shared__ __align__(16) int hist[4096];
+    __shared__ int scratch[kRowThreads / 32 + 1];
+    __shared__ int sel[2];
+    grid_dep_wait();
+    grid_dep_launch();
+    for (int row = blockIdx.x; row < T; row += gridDim.x) {
+        int64_t n = static_cast<int64_t>(q_pos[row]) + 1;
+        n = n < 0 ? 0 : (n > S ? S : n);
+        int m = qpos_s[row] + 1;
+        m = m < 0 ? 0 : (m > ld_s ? ld_s : m);
+        if (n <= cap || m == 0) {
+            if (threadIdx.x == 0)
+                thr[row] = -INFINITY;
+            continue;
+        }
+        int64_t r = (static_cast<int64_t>(m) * 2 * k + n - 1) / n;
+        r = r < 1 ? 1 : (r > m ? m : r);
+        const float *srow = samp + static_cast<int64_t>(row) * ld_s;
+        int k_eq;
+        const uint32_t tau = (reinterpret_cast<uintptr_t>(srow) & 15u) == 0
+                                 ? kth_key<kRowThreads, true>(srow, m, static_cast<int>(r), hist, scratch, sel, &k_eq)
+                                 : kth_key<kRowThreads, false>(srow, m, static_cast<int>(r), hist, scratch, sel, &k_eq);
+        if (threadIdx.x == 0)
+            thr[row] = key_float(tau);
+        __syncthreads();
+    }
+}
+
+// Select.  One CTA per row: a row with n <= k keeps keys 0 .. n-1; a row whose
+// candidate count c is in [k, cap] loads its candidates (any order), finds the
+// key tau of the k-th largest and how many keys equal to tau rank among the k
+// (select_tau), marks the keys above tau and those equal to it in two bitmaps
+// over the row's positions and walks the bitmaps in position order: every key
+// > tau is kept, and of the keys == tau the first need_eq; a block-wide
+// prefix count gives each kept position its output slot, so the output is in
+// ascending order and the tie rule is (score desc, position asc).  A row whose
+// count misses [k, cap] is flagged (flag[t] = 1) for the full path and left
+// untouched; every other row gets flag[t] = 0.
+constexpr int kCandHistInts = 2048 + 3 * (kRowThreads / 32); // select_tau's scratch
+constexpr int kCandSmemMax = 232448 - 1024;                  // dynamic bytes, beside the kernel's static ones
+
+__global__ void __launch_bounds__(kRowThreads)
+    topk_candidates_kernel(const uint32_t *__restrict__ cand_key, const int32_t *__restrict__ cand_idx,
+                           const int32_t *__restrict__ cand_cnt, int cap, int T, const int32_t *__restrict__ q_pos,
+                           int S, int k, int32_t *__restrict__ idx, int32_t *__restrict__ flag)
+{
+    extern __shared__ __align__(16) uint32_t dsm[];
+    const int nw_max = (S + 31) / 32;
+    uint32_t *ck = dsm;
+    int32_t *ci = reinterpret_cast<int32_t *>(dsm + cap);
+    int *hist = reinterpret_cast<int *>(dsm + 2 * cap);
+    uint32_t *bgt = dsm + 2 * cap + kCandHistInts;
+    uint32_t *beq = bgt + nw_max;
+    __shared__ int scratch[kRowThreads / 32 + 1];
+    __shared__ int sel[2];
+    grid_dep_wait();
+    grid_dep_launch();
+    for (int row = blockIdx.x; row < T; row += gridDim.x) {
+        int64_t n64 = static_cast<int64_t>(q_pos[row]) + 1;
+        const int n = static_cast<int>(n64 < 0 ? 0 : (n64 > S ? S : n64));
+        int32_t *out = idx + static_cast<int64_t>(row) * k;
+        if (n <= k) {
+            for (int j = threadIdx.x; j < k; j += kRowThreads)
+                out[j] = j < n ? j : -1;
+            if (threadIdx.x == 0)
+                flag[row] = 0;
+            continue;
+        }
+        const int c = cand_cnt[row];
+        if (c < k || c > cap) {
+            if (threadIdx.x == 0)
+                flag[row] = 1;
+            continue;
+        }
+        const int64_t base = static_cast<int64_t>(row) * cap;
+        for (int f = threadIdx.x; f < c; f += kRowThreads) {
+            ck[f] = __ldg(cand_key + base + f);
+            ci[f] = __ldg(cand_idx + base + f);
+        }
+        const int nw = (n + 31) / 32;
+        for (int w = threadIdx.x; w < nw; w += kRowThreads) {
+            bgt[w] = 0u;
+            beq[w] = 0u;
+        }
+        __syncthreads();
+        int need_eq;
+        const uint32_t tau = select_tau<kRowThreads>(ck, c, k, hist, sel, &need_eq);
+        for (int f = threadIdx.x; f < c; f += kRowThreads) {
+            const uint32_t key = order_key_bits(ck[f]);
+            const int i = ci[f];
+            if (key > tau)
+                atomicOr(&bgt[i >> 5], 1u << (i & 31));
+            else if (key == tau)
+                atomicOr(&beq[i >> 5], 1u << (i & 31));
+        }
+        __syncthreads();
+        const int per = (nw + kRowThreads - 1) / kRowThreads;
+        const int w0 = threadIdx.x * per < nw ? threadIdx.x * per : nw;
+        const int w1 = w0 + per < nw ? w0 + per : nw;
+        int gt = 0, eq = 0;
+        for (int w = w0; w < w1; ++w) {
+            gt += __popc(bgt[w]);
+            eq += __popc(beq[w]);
+        }
+        int total;
+        const int pre = block_exclusive_scan<kRowThreads>((gt << 16) | eq, scratch, &total);
+        int g_before = pre >> 16, e_before = pre & 0xFFFF;
+        for (int w = w0; w < w1; ++w) {
+            const uint32_t g = bgt[w];
+            uint32_t m = g | beq[w];
+            while (m) {
+                const int b = __ffs(m) - 1;
+                m &= m - 1u;
+                const int i = 32 * w + b;
+                if ((g >> b) & 1u) {
+                    out[g_before + (e_before < need_eq ? e_before : need_eq)] = i;
+                    ++g_before;
+                } else {
+                    if (e_before < need_eq)
+                        out[g_before + e_before] = i;
+                    ++e_before;
+                }
+            }
+        }
+        if (threadIdx.x == 0)
+            flag[row] = 0;
         __syncthreads();
     }
 }
@@ -865,7 +1032,7 @@ int launch_topk(const TopkArgs &a, cudaStream_t stream, char *err, size_t errlen
     }
     const int sms = num_sms();
     cudaError_t e;
-    if (a.T <= 2 * sms) {
+    if (a.T <= 2 * sms && !a.row_flag) {
         // Few rows (decode): each row's latency is the cost, so a row gets as
         // many CTAs as the SMs allow and is read once.  Many rows (prefill): one
         // small CTA per row keeps four rows in flight per SM.
@@ -889,10 +1056,56 @@ int launch_topk(const TopkArgs &a, cudaStream_t stream, char *err, size_t errlen
         }
         const int grid = a.T < 65535 * 4 ? a.T : 65535 * 4;
         e = launch_pdl(topk_rows_kernel, dim3(grid), dim3(kRowThreads), kRowSmem, stream, 1, a.logits, a.ld, a.T,
-                       a.valid_len, a.k, a.idx, status);
+                       a.valid_len, a.k, a.idx, status, a.row_flag);
     }
     if (e != cudaSuccess) {
         snprintf(err, errlen, "topk launch: %s", cudaGetErrorString(e));
+        return DSA_ERR_CUDA;
+    }
+    return DSA_OK;
+}
+
+
+size_t topk_candidates_smem(int S, int cap)
+{
+    return (static_cast<size_t>(2) * cap + kCandHistInts + 2 * static_cast<size_t>((S + 31) / 32)) * 4;
+}
+
+int launch_topk_threshold(const float *samp, int ld_s, int T, const int32_t *q_pos, const int32_t *qpos_s, int S,
+                          int k, int cap, float *thr, cudaStream_t stream, char *err, size_t errlen)
+{
+    const int grid = T < 4 * num_sms() ? T : 4 * num_sms();
+    cudaError_t e = launch_pdl(topk_threshold_kernel, dim3(grid), dim3(kRowThreads), 0, stream, 1, samp, ld_s, T,
+                               q_pos, qpos_s, S, k, cap, thr);
+    if (e != cudaSuccess) {
+        snprintf(err, errlen, "topk threshold launch: %s", cudaGetErrorString(e));
+        return DSA_ERR_CUDA;
+    }
+    return DSA_OK;
+}
+
+int launch_topk_candidates(const uint32_t *cand_key, const int32_t *cand_idx, const int32_t *cand_cnt, int cap,
+                           int T, const int32_t *q_pos, int S, int k, int32_t *idx, int32_t *flag,
+                           cudaStream_t stream, char *err, size_t errlen)
+{
+    const size_t smem = topk_candidates_smem(S, cap);
+    if (smem > kCandSmemMax) {
+        snprintf(err, errlen, "topk candidates: %zu bytes of shared memory needed", smem);
+        return DSA_ERR_UNSUPPORTED;
+    }
+    // the attribute is set once per device to the largest size any call may ask for
+    static std::atomic<bool> attr_set[64];
+    if (cudaError_t e_attr = raise_smem_limit_once(topk_candidates_kernel, kCandSmemMax, attr_set);
+        e_attr != cudaSuccess) {
+        snprintf(err, errlen, "cudaFuncSetAttribute(topk candidates): %s", cudaGetErrorString(e_attr));
+        return DSA_ERR_CUDA;
+    }
+    const int per_sm = smem <= 113 * 1024 ? 2 : 1;
+    const int grid = T < per_sm * num_sms() ? T : per_sm * num_sms();
+    cudaError_t e = launch_pdl(topk_candidates_kernel, dim3(grid), dim3(kRowThreads), smem, stream, 1, cand_key,
+                               cand_idx, cand_cnt, cap, T, q_pos, S, k, idx, flag);
+    if (e != cudaSuccess) {
+        snprintf(err, errlen, "topk candidates launch: %s", cudaGetErrorString(e));
         return DSA_ERR_CUDA;
     }
     return DSA_OK;

@@ -145,3 +145,31 @@ def test_every_declaration_is_documented_and_cites_its_page():
         if name in steps:
             flat = " ".join(comment.replace("*", " ").split())
             assert any(" ".join(pg.split()) in flat for pg in pages), f"{name}: no page cited"
+
+
+def test_fused_indexer_topk_validation(lib):
+    """dsa_indexer_topk's host checks and its workspace query (nothing reaches the device)."""
+    P = ctypes.c_void_p
+    fake = P(4096)
+    T, S, k = 8, 1000, 64
+    need = lib.dsa_indexer_topk_workspace_size(T, S, 64, 128, k)
+    # sampled keys, per-row positions and thresholds, T x max(4096, 4k) candidates of 8 bytes,
+    # T x S fp32 scores for rows redone from full scores
+    assert need >= T * 4096 * 8 + T * S * 4 + T * min(S, 2048) * 4
+    assert lib.dsa_indexer_topk_workspace_size(T, S, 64, 128, 2048) > need  # cap grows with k
+    assert lib.dsa_indexer_topk_workspace_size(T, S, 4, 32, k) == 0        # unsupported head shape
+    assert lib.dsa_indexer_topk_workspace_size(T, 262145, 64, 128, k) == 0  # past the key limit
+    assert lib.dsa_indexer_topk_workspace_size(T, S, 64, 128, 4097) == 0
+
+    def call(t=T, hi=64, di=128, s=S, kk=k, q8=fake, ws=P(1 << 20), ws_bytes=need):
+        return lib.dsa_indexer_topk(q8, fake, fake, t, hi, di, fake, fake, s, fake, kk, fake, ws, ws_bytes, None)
+
+    assert call(t=-1) == 1
+    assert call(t=0) == 0
+    assert call(hi=4, di=32) == 2
+    assert call(s=0) == 2 and call(s=262145) == 2
+    assert call(kk=0) == 2
+    assert call(q8=P(4097)) == 3
+    assert call(ws=P((1 << 20) + 64)) == 3
+    assert call(ws_bytes=need - 1) == 4
+    assert "workspace" in _err(lib)
