@@ -450,6 +450,35 @@ def time_calls(calls, steps, warmup, flush):
     return step_ms, per.mean(0)
 
 
+def fused_bench(dsa, x, b, cfg, steps, warmup, flush, dev, two_call_stages, chunk_rows=None):
+    """The same prefill with the indexer and top-k fused (dsa_indexer_topk: no index scores
+    in memory) in place of the two calls; the attention stage is unchanged.  The indices of
+    the last chunk (or the whole prefill) are compared byte for byte with the two-call path's."""
+    L, C = cfg.L, chunk_rows or cfg.L
+    ws = torch.empty(dsa.dsa_indexer_topk_workspace_size(C, L, cfg.HI, cfg.dI, cfg.k), dtype=torch.uint8, device=dev)
+    idx_f = torch.empty_like(b["idx"])
+    calls = []
+    for c in range(L // C):
+        r0, r1 = c * C, (c + 1) * C
+        calls.append((0, lambda r0=r0, r1=r1: dsa.dsa_indexer_topk(
+            x["q8"][r0:r1], x["qs"][r0:r1], x["w"][r0:r1], x["k8"][:r1], x["ks"][:r1], x["q_pos"][r0:r1], cfg.k,
+            idx_f, workspace=ws)))
+        calls.append((2, lambda r0=r0, r1=r1: dsa.dsa_sparse_mla_prefill(
+            x["q"][r0:r1], x["kv"][:r1], idx_f, cfg.sm_scale, b["out"][r0:r1], b["lse"][r0:r1])))
+    step_ms, stage_ms = time_calls(calls, steps, warmup, flush)
+    # b["idx"] holds the two-call path's indices of the same (last) chunk
+    same = bool(torch.equal(idx_f, b["idx"]))
+    two = two_call_stages["indexer"]["ms"] + two_call_stages["topk"]["ms"]
+    ms = float(step_ms.mean())
+    del ws
+    return {"ms_per_step": ms, "tokens_per_s": L / (ms / 1e3), "indexer_topk_ms": float(stage_ms[0]),
+            "sparse_mla_ms": float(stage_ms[2]), "two_call_indexer_plus_topk_ms": two,
+            "saved_ms": two - float(stage_ms[0]), "indices_match_two_call_path": same,
+            "launches_per_step": 8 * (L // C),
+            "what": "dsa_indexer_topk (sampled threshold, candidate-mode indexer, exact select; no scores "
+                    "written) then sparse MLA, per chunk"}
+
+
 def workload_bench(dsa, name, steps, warmup, flush, peaks, peaks_src, mm, dev):
     """One more configured prefill workload (tiny, L = 4096, or the chunked L = 131072):
     per-stage ms, tokens/s and roofline fractions, clocks sampled over its own timed region."""
@@ -480,6 +509,7 @@ def workload_bench(dsa, name, steps, warmup, flush, peaks, peaks_src, mm, dev):
         # the logits each chunk's indexer writes and its top-k reads back (causal part only)
         rec["logits_bytes_write_read"] = 8.0 * work["key_rows"]
         rec["logits_hbm_ms_at_peak"] = rec["logits_bytes_write_read"] / (pk["hbm"] * 1e9) * 1e3
+        rec["fused"] = fused_bench(dsa, x, b, cfg, steps, warmup, flush, dev, rec["stages"], chunk_rows=cfg.chunk)
     del x, b, calls
     torch.cuda.empty_cache()
     return rec
@@ -730,6 +760,7 @@ def main():
         "output_hash": out_hash,
         "timed_wall_s": t_wall1 - t_wall0,
     }
+    line["fused"] = fused_bench(dsa, x, b, cfg, max(3, min(args.steps, 10)), args.warmup, flush, dev, stages)
     if not args.no_e2e:
         line["e2e"] = e2e_bench(dsa, x, b, cfg, max(2, min(args.steps, 16)), dev)
         line["e2e"]["value"] *= world

@@ -185,12 +185,13 @@ int dsa_topk(const float *logits, int64_t ld, int T, const int32_t *valid_len,
  * attention drops from O(L^2) to O(Lk), which leaves the indexer's L x L
  * scores as the long-context cost; here they are neither written nor read).
  *
- * How: a per-row threshold from the scores of 2048 keys sampled at a fixed
- * stride (about 2k of the row's keys score at or above it; rows of at most
- * max(4096, 4k) keys take every key), then the indexer appends only the keys
- * at or above it to per-row lists, and an exact top-k runs over each list.  A
- * row whose list misses [k, max(4096, 4k)] (a row unlike its samples) is
- * redone from its full scores, so the result never depends on the sample.
+ * How: a per-row threshold from the scores of keys sampled at a fixed stride
+ * (2048 of them, or S/32 past 65536 keys), which about 1.25k + 256 of the
+ * row's keys reach (rows of at most max(4096, 2k) keys take every key); the
+ * indexer then appends only the keys at or above it to per-row lists, and an
+ * exact top-k runs over each list.  A row whose list misses
+ * [k, max(4096, 2k)] (a row unlike its samples) is redone from its full
+ * scores, so the result never depends on the sample.
  *
  *   q8, q_scale, w, q_pos, k8, k_scale, S: as for dsa_indexer_logits with
  *             contiguous keys ([S, d_I] codes, [S] scales); (H_I, d_I) =
@@ -200,7 +201,7 @@ int dsa_topk(const float *logits, int64_t ld, int T, const int32_t *valid_len,
  *             d_I, k) bytes, 256-byte aligned, owned by the caller, used only
  *             while the call's kernels run on `stream` (calls sharing one must
  *             be ordered).  It holds the sampled keys and scores, the per-row
- *             candidate lists (T x max(4096, 4k) entries of 8 bytes) and, for
+ *             candidate lists (T x max(4096, 2k) entries of 8 bytes) and, for
  *             the rows redone from full scores, T x S fp32 scores: most of it
  *             stays untouched; callers with long rows pass rows in chunks.
  * A position q_pos[r] >= S is clamped to S-1 and flagged DSA_DEV_BAD_POSITION.

@@ -41,6 +41,7 @@ namespace dsa {
 namespace {
 
 constexpr int kTileKeys = 128;
+constexpr int kCandRegions = 128; // candidate-mode regions per row: one per lane writing the row
 
 template <int HI, int DI, bool PAGED>
 struct IdxCfg {
@@ -105,25 +106,28 @@ struct Params {
     unsigned *status;
     // candidate mode and row filter (see IndexerArgs)
     const float *thr;
-    uint32_t *cand_key;
-    int32_t *cand_idx;
+    uint2 *cand;
     int32_t *cand_cnt;
     int cap;
     const int32_t *row_flag;
 };
 
 // FUSED: candidate mode.  Instead of writing logits, the epilogue appends
-// every key whose score is >= the row's threshold to the row's candidate list
-// (warp-aggregated slots from a shared-memory counter per row); the counts go
-// to cand_cnt when the CTA ends.  Same arithmetic, so the same fp32 scores.
+// every key whose score is >= the row's threshold to the row's candidate list.
+// A row is scored by 8 epilogue warps (TMEM lane quadrant x lane half) and, in
+// each, by the 16 lanes of one parity; its list is kCandRegions = 128 fixed
+// regions of p.cap entries, one per such lane, which counts its candidates in
+// a register: no atomics, no cross-lane step.  Each lane writes its count to
+// cand_cnt[row][region] when done.  Same arithmetic as the logits mode, so the
+// same fp32 scores.
 template <int HI, int DI, bool PAGED, bool FUSED = false>
 __global__ void __launch_bounds__(IdxCfg<HI, DI, PAGED>::THREADS, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k, Params p)
 {
     using C = IdxCfg<HI, DI, PAGED>;
-    static_assert(!FUSED || (C::FRAG && C::R <= 8), "candidate mode: fragment epilogue, at most 8 rows per CTA");
+    static_assert(!FUSED || (C::FRAG && C::R <= 8 && C::TPW >= 2 && C::NLH == 1 && 8 * C::NEPI == kCandRegions),
+                  "candidate mode: fragment epilogue (every lane stores), one lane half per warp, 8 rows or fewer");
     __shared__ float thr_s[FUSED ? C::R : 1];
-    __shared__ int cnt_s[FUSED ? C::R : 1];
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -172,7 +176,6 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI, PAGED>::THREADS, 1)
         pos_s[threadIdx.x] = pos;
         if constexpr (FUSED) {
             thr_s[threadIdx.x] = r < p.T ? p.thr[r] : INFINITY;
-            cnt_s[threadIdx.x] = 0;
         }
     }
     for (int i = threadIdx.x; i < C::R * HI; i += C::THREADS) {
@@ -209,8 +212,8 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI, PAGED>::THREADS, 1)
     const int kt0 = tiles_s[0], kt1 = tiles_s[1];
     if (kt1 <= kt0) {
         if constexpr (FUSED) {
-            if (threadIdx.x < C::R && r0 + threadIdx.x < p.T)
-                p.cand_cnt[r0 + threadIdx.x] = 0;
+            if (threadIdx.x < C::R * kCandRegions && r0 + threadIdx.x / kCandRegions < p.T)
+                p.cand_cnt[(int64_t)r0 * kCandRegions + threadIdx.x] = 0;
         }
         return; // uniform: nothing to score in this split
     }
@@ -345,6 +348,21 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI, PAGED>::THREADS, 1)
         const int lh0 = C::NLH == 1 ? (j & 1) : 0;
         const int cb = (C::NLH == 1 ? (j >> 1) : 0) * C::NCW;
         const int tb = cb / HI; // CTA-local row of the warp's first token
+        // candidate mode: this lane's region of each of its rows (the rows of its
+        // parity), its counters there and the rows' thresholds
+        constexpr int FH = C::TPW >= 2 ? C::TPW / 2 : 1;
+        const int region = (quad * 2 + lh0) * 16 + (lane >> 1);
+        int wcnt[FH];
+        float thr_r[FH];
+        uint2 *cbase[FH]; // this lane's region of each of its rows (null past T)
+#pragma unroll
+        for (int i = 0; i < FH; ++i) {
+            wcnt[i] = 0;
+            const int lr = tb + (C::TPW >= 2 ? (lane & 1) * FH : 0) + i;
+            thr_r[i] = FUSED ? thr_s[lr] : 0.f;
+            cbase[i] = (FUSED && r0 + lr < p.T) ? p.cand + ((int64_t)(r0 + lr) * kCandRegions + region) * p.cap
+                                                : nullptr;
+        }
         const int g = lane >> 2, tq = lane & 3;
         const int b1 = tq >> 1, b0 = tq & 1;
         uint64_t w2[C::REPS];
@@ -490,22 +508,10 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI, PAGED>::THREADS, 1)
                                 p.logits[(int64_t)rg * p.ld + s] = y[i] * ks[l];
                         } else {
                             const float v = y[i] * ks[l];
-                            const bool f = rg < p.T && s <= pos_s[lr] && v >= thr_s[lr];
-                            const unsigned fm = __ballot_sync(__activemask(), f);
-                            if (f) {
-                                // one shared-memory atomic per (warp, row): lanes of the same row
-                                // take consecutive slots
-                                const unsigned grp = __match_any_sync(fm, lr);
-                                const int leader = __ffs(grp) - 1;
-                                int base = 0;
-                                if (lane == leader)
-                                    base = atomicAdd(&cnt_s[lr], __popc(grp));
-                                base = __shfl_sync(grp, base, leader);
-                                const int slot = base + __popc(grp & ((1u << lane) - 1u));
-                                if (slot < p.cap) {
-                                    p.cand_key[(int64_t)rg * p.cap + slot] = __float_as_uint(v);
-                                    p.cand_idx[(int64_t)rg * p.cap + slot] = s;
-                                }
+                            if (s <= pos_s[lr] && v >= thr_r[i] && cbase[i]) {
+                                if (wcnt[i] < p.cap)
+                                    cbase[i][wcnt[i]] = make_uint2(__float_as_uint(v), static_cast<uint32_t>(s));
+                                ++wcnt[i];
                             }
                         }
                     }
@@ -520,6 +526,14 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI, PAGED>::THREADS, 1)
             }
         }
         tmem_ld_wait(); // no load of this warp outlives the loop
+        if constexpr (FUSED) {
+#pragma unroll
+            for (int i = 0; i < FH; ++i) {
+                const int rg = r0 + tb + (lane & 1) * FH + i;
+                if (rg < p.T)
+                    p.cand_cnt[(int64_t)rg * kCandRegions + region] = wcnt[i];
+            }
+        }
     } else {
         // --------------------------------------------------------- epilogue
         const int quad = warp & 3;
@@ -618,10 +632,6 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI, PAGED>::THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
-    if constexpr (FUSED) {
-        if (threadIdx.x < C::R && r0 + threadIdx.x < p.T)
-            p.cand_cnt[r0 + threadIdx.x] = cnt_s[threadIdx.x];
-    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
@@ -1010,8 +1020,7 @@ int launch_cfg(const IndexerArgs &a, cudaStream_t stream, char *err, size_t errl
     p.num_pages = a.num_pages;
     p.page_size = a.page_size;
     p.thr = a.thr;
-    p.cand_key = a.cand_key;
-    p.cand_idx = a.cand_idx;
+    p.cand = a.cand;
     p.cand_cnt = a.cand_cnt;
     p.cap = a.cap;
     p.row_flag = a.row_flag;
@@ -1060,7 +1069,7 @@ int launch_cfg(const IndexerArgs &a, cudaStream_t stream, char *err, size_t errl
     dim3 grid(groups, splits);
     cudaError_t e;
     if constexpr (C::FRAG && C::R <= 8) {
-        if (a.cand_key) {
+        if (a.cand) {
             static std::atomic<bool> fused_attr[64];
             if (cudaError_t e_attr = raise_smem_limit_once(indexer_kernel<HI, DI, PAGED, true>, C::SMEM, fused_attr);
                 e_attr != cudaSuccess) {
@@ -1075,7 +1084,7 @@ int launch_cfg(const IndexerArgs &a, cudaStream_t stream, char *err, size_t errl
             return DSA_OK;
         }
     }
-    if (a.cand_key) {
+    if (a.cand) {
         snprintf(err, errlen, "indexer: candidate mode needs contiguous keys and H_I in {32, 64}");
         return DSA_ERR_UNSUPPORTED;
     }

@@ -8,15 +8,15 @@
 // section "Computational Efficiency": attention cost goes from O(L^2) to
 // O(Lk), which at long context leaves the indexer's L^2 scores as the quadratic
 // part).  Written out, a row of L keys costs 4 L bytes of scores to write and
-// read back; the fused path keeps ~2k of them.
+// read back; the fused path keeps ~1.25k + 256 of them.
 //
 // Steps, all on the caller's stream:
-//   1. gather      the keys at a fixed stride over [0, S): nsamp = min(2048, S)
-//                  sample keys p_j = floor(j S / nsamp), and for every row the
-//                  last sample at or before its position;
+//   1. gather      the keys at a fixed stride over [0, S): nsamp sample keys
+//                  (sample_count) p_j = floor(j S / nsamp), and for every row
+//                  the last sample at or before its position;
 //   2. indexer     the rows' scores against the samples (the same kernel and
 //                  arithmetic as dsa_indexer_logits, samples as keys);
-//   3. threshold   per row, the score about 2k of the row's keys reach
+//   3. threshold   per row, a score about 1.25k + 256 of the row's keys reach
 //                  (topk_threshold_kernel); -inf for rows of at most cap keys;
 //   4. indexer     candidate mode: every key scoring at or above its row's
 //                  threshold is appended to the row's list (score, position);
@@ -36,19 +36,29 @@
 namespace dsa {
 namespace {
 
-constexpr int kSamples = 2048;
+// Sampled keys: 2048, or S / 32 for prefixes past 65536 keys (a row of n keys
+// then sees about 2048 n / S of them, and the rank its threshold sits at,
+// r ~ (1.25 k + 256) * samples / S, stays near 90 or more: the candidate count
+// misses [k, cap] for a row like its samples with a probability of the order
+// of 1e-2 at the smallest r and far less above; sampling costs ~3 % of the
+// indexer's work).
+int sample_count(int S) { return S <= 2048 ? S : (S / 32 > 2048 ? S / 32 : 2048); }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-int cap_for(int k) { return 4 * k > 4096 ? 4 * k : 4096; }
+// A row's candidate list holds at most cap_for(k) entries for the select; the
+// indexer writes it as 128 per-lane regions of cap_for(k) / 64 entries (about
+// three times what a lane finds at the threshold).
+int cap_for(int k) { return 2 * k > 4096 ? 2 * k : 4096; }
+constexpr int kLaneRegions = 128;
 
 struct Layout {
-    size_t k8s, kss, qpos_s, vlen, samp, thr, cand_key, cand_idx, cand_cnt, flag, fb_logits, total;
+    size_t k8s, kss, qpos_s, vlen, samp, thr, cand, cand_cnt, flag, fb_logits, total;
 };
 
 Layout layout(int T, int S, int dI, int k)
 {
-    const int nsamp = S < kSamples ? S : kSamples;
+    const int nsamp = sample_count(S);
     const size_t cap = static_cast<size_t>(cap_for(k));
     Layout l;
     size_t o = 0;
@@ -64,12 +74,10 @@ Layout layout(int T, int S, int dI, int k)
     o += align256(static_cast<size_t>(T) * nsamp * 4);
     l.thr = o;
     o += align256(static_cast<size_t>(T) * 4);
-    l.cand_key = o;
-    o += align256(static_cast<size_t>(T) * cap * 4);
-    l.cand_idx = o;
-    o += align256(static_cast<size_t>(T) * cap * 4);
+    l.cand = o;
+    o += align256(static_cast<size_t>(T) * kLaneRegions * (cap / 64) * 8);
     l.cand_cnt = o;
-    o += align256(static_cast<size_t>(T) * 4);
+    o += align256(static_cast<size_t>(T) * kLaneRegions * 4); // per row, one count per list region
     l.flag = o;
     o += align256(static_cast<size_t>(T) * 4);
     l.fb_logits = o;
@@ -126,7 +134,7 @@ int launch_indexer_topk(const IndexerTopkArgs &a, cudaStream_t stream, char *err
         return DSA_ERR_WORKSPACE;
     }
     const int cap = cap_for(a.k);
-    if (topk_candidates_smem(a.S, cap) > 232448 - 1024) {
+    if (topk_candidates_smem(a.S, cap) > 232448 - 2048) {
         snprintf(err, errlen, "fused indexer -> top-k: S = %d is beyond its shared-memory bitmaps", a.S);
         return DSA_ERR_UNSUPPORTED;
     }
@@ -137,12 +145,11 @@ int launch_indexer_topk(const IndexerTopkArgs &a, cudaStream_t stream, char *err
     int32_t *vlen = reinterpret_cast<int32_t *>(ws + l.vlen);
     float *samp = reinterpret_cast<float *>(ws + l.samp);
     float *thr = reinterpret_cast<float *>(ws + l.thr);
-    uint32_t *cand_key = reinterpret_cast<uint32_t *>(ws + l.cand_key);
-    int32_t *cand_idx = reinterpret_cast<int32_t *>(ws + l.cand_idx);
+    uint2 *cand = reinterpret_cast<uint2 *>(ws + l.cand);
     int32_t *cand_cnt = reinterpret_cast<int32_t *>(ws + l.cand_cnt);
     int32_t *flag = reinterpret_cast<int32_t *>(ws + l.flag);
     float *fb_logits = reinterpret_cast<float *>(ws + l.fb_logits);
-    const int nsamp = a.S < kSamples ? a.S : kSamples;
+    const int nsamp = sample_count(a.S);
 
     // 1. sample keys and per-row sample positions
     const int64_t items = static_cast<int64_t>(nsamp) * (a.dI / 16) + nsamp + a.T;
@@ -168,16 +175,14 @@ int launch_indexer_topk(const IndexerTopkArgs &a, cudaStream_t stream, char *err
     IndexerArgs ic{a.q8, a.q_scale, a.w, a.T, a.HI, a.dI, a.k8, a.k_scale, a.S, nullptr, 0, 0, 0, a.q_pos,
                    fb_logits, a.S};
     ic.thr = thr;
-    ic.cand_key = cand_key;
-    ic.cand_idx = cand_idx;
+    ic.cand = cand;
     ic.cand_cnt = cand_cnt;
-    ic.cap = cap;
+    ic.cap = cap / 64; // entries per lane region
     rc = launch_indexer(ic, stream, err, errlen);
     if (rc != DSA_OK)
         return rc;
     // 5. exact top-k of the candidates; rows whose count missed [k, cap] flagged
-    rc = launch_topk_candidates(cand_key, cand_idx, cand_cnt, cap, a.T, a.q_pos, a.S, a.k, a.idx, flag, stream, err,
-                                errlen);
+    rc = launch_topk_candidates(cand, cand_cnt, cap, a.T, a.q_pos, a.S, a.k, a.idx, flag, stream, err, errlen);
     if (rc != DSA_OK)
         return rc;
     // 6-7. the flagged rows from full scores

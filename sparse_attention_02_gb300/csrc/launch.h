@@ -36,6 +36,8 @@ cudaError_t raise_smem_limit_once(void (*kernel)(KArgs...), int bytes, std::atom
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e == cudaSuccess && dev < 64)
         done[dev].store(true, std::memory_order_release);
+    if (e != cudaSuccess)
+        cudaGetLastError(); // the failure is reported to the caller; leave no error behind for the next call
     return e;
 }
 
@@ -91,13 +93,13 @@ struct IndexerArgs {
     const int32_t *q_pos;
     float *logits;
     int64_t ld;
-    // Candidate mode (cand_key != nullptr; contiguous keys, H_I in {32, 64}):
-    // no logits are written; a key whose score is >= thr[r] is appended to
-    // row r's list as (raw fp32 score bits, position) in no particular order.
+    // Candidate mode (cand != nullptr; contiguous keys, H_I in {32, 64}): no
+    // logits are written; a key whose score is >= thr[r] is appended to row
+    // r's list as {raw fp32 score bits, position}, in no particular order.  The
+    // list is 128 regions of cap entries, one per epilogue lane scoring the row.
     const float *thr = nullptr;        // [T]
-    uint32_t *cand_key = nullptr;      // [T, cap]
-    int32_t *cand_idx = nullptr;       // [T, cap]
-    int32_t *cand_cnt = nullptr;       // [T] candidates found (only the first cap are stored)
+    uint2 *cand = nullptr;             // [T, 128, cap]
+    int32_t *cand_cnt = nullptr;       // [T, 128] candidates each region found (only cap are stored)
     int cap = 0;
     const int32_t *row_flag = nullptr; // score only rows with row_flag[r] != 0 (nullptr: all rows)
 };
@@ -119,9 +121,8 @@ int launch_topk(const TopkArgs &a, cudaStream_t stream, char *err, size_t errlen
 // scores, and the exact top-k over each row's candidate list.
 int launch_topk_threshold(const float *samp, int ld_s, int T, const int32_t *q_pos, const int32_t *qpos_s, int S,
                           int k, int cap, float *thr, cudaStream_t stream, char *err, size_t errlen);
-int launch_topk_candidates(const uint32_t *cand_key, const int32_t *cand_idx, const int32_t *cand_cnt, int cap,
-                           int T, const int32_t *q_pos, int S, int k, int32_t *idx, int32_t *flag,
-                           cudaStream_t stream, char *err, size_t errlen);
+int launch_topk_candidates(const uint2 *cand, const int32_t *cand_cnt, int cap, int T, const int32_t *q_pos, int S,
+                           int k, int32_t *idx, int32_t *flag, cudaStream_t stream, char *err, size_t errlen);
 size_t topk_candidates_smem(int S, int cap);
 
 struct IndexerTopkArgs {

@@ -794,11 +794,14 @@ __global__ void __launch_bounds__(kRowThreads, 4)
 //
 // Threshold.  Row t holds n = min(q_pos[t] + 1, S) keys.  A row with n <= cap
 // keeps every key (threshold -inf).  Otherwise its m valid samples samp[t, 0, m)
-// (scores of keys at a fixed stride over the keys) give thr[t] = the r-th
-// largest sample, r = ceil(m * 2k / n): about 2k keys of the row score at or
-// above it, so its k largest are among them unless the row is far from what
-// its samples show (then its candidate count misses [k, cap] and the row is
-// redone from full logits; the result is the same).
+// (scores of keys at a fixed stride over the keys) give thr[t] = the exact
+// r-th largest sample, r = ceil((1.25 k + 256) m / n), found digit by digit
+// (kth_key): about 1.25 k + 256 keys of the row score at or above it, so its k
+// largest are among them unless the row is far from what its samples show
+// (then its candidate count misses [k, cap] and the row is redone from full
+// logits; the result is the same).  A single coarse histogram over the
+// samples' whole key range is not enough here: near the threshold one of its
+// bins can span a score interval holding a thousand keys of a 32K-key row.
 __global__ void __launch_bounds__(kRowThreads)
     topk_threshold_kernel(const float *__restrict__ samp, int ld_s, int T, const int32_t *__restrict__ q_pos,
                           const int32_t *__restrict__ qpos_s, int S, int k, int cap, float *__restrict__ thr)
@@ -818,7 +821,7 @@ __global__ void __launch_bounds__(kRowThreads)
                 thr[row] = -INFINITY;
             continue;
         }
-        int64_t r = (static_cast<int64_t>(m) * 2 * k + n - 1) / n;
+        int64_t r = (static_cast<int64_t>(5 * k / 4 + 256) * m + n - 1) / n;
         r = r < 1 ? 1 : (r > m ? m : r);
         const float *srow = samp + static_cast<int64_t>(row) * ld_s;
         int k_eq;
@@ -832,22 +835,25 @@ __global__ void __launch_bounds__(kRowThreads)
 }
 
 // Select.  One CTA per row: a row with n <= k keeps keys 0 .. n-1; a row whose
-// candidate count c is in [k, cap] loads its candidates (any order), finds the
+// candidate count c is in [k, cap], with no region of its list overflowed (the
+// list is kCandRegions regions of cap / 64 entries, one per indexer epilogue
+// lane), loads its candidates (any order), finds the
 // key tau of the k-th largest and how many keys equal to tau rank among the k
 // (select_tau), marks the keys above tau and those equal to it in two bitmaps
 // over the row's positions and walks the bitmaps in position order: every key
 // > tau is kept, and of the keys == tau the first need_eq; a block-wide
 // prefix count gives each kept position its output slot, so the output is in
 // ascending order and the tie rule is (score desc, position asc).  A row whose
-// count misses [k, cap] is flagged (flag[t] = 1) for the full path and left
-// untouched; every other row gets flag[t] = 0.
+// count misses [k, cap] or overflowed a region is flagged (flag[t] = 1) for
+// the full path and left untouched; every other row gets flag[t] = 0.
 constexpr int kCandHistInts = 2048 + 3 * (kRowThreads / 32); // select_tau's scratch
-constexpr int kCandSmemMax = 232448 - 1024;                  // dynamic bytes, beside the kernel's static ones
+constexpr int kCandRegions = 128;                            // regions of a row's candidate list
+constexpr int kCandSmemMax = 232448 - 2048;                  // dynamic bytes, beside the kernel's static ones
 
 __global__ void __launch_bounds__(kRowThreads)
-    topk_candidates_kernel(const uint32_t *__restrict__ cand_key, const int32_t *__restrict__ cand_idx,
-                           const int32_t *__restrict__ cand_cnt, int cap, int T, const int32_t *__restrict__ q_pos,
-                           int S, int k, int32_t *__restrict__ idx, int32_t *__restrict__ flag)
+    topk_candidates_kernel(const uint2 *__restrict__ cand, const int32_t *__restrict__ cand_cnt, int cap, int T,
+                           const int32_t *__restrict__ q_pos, int S, int k, int32_t *__restrict__ idx,
+                           int32_t *__restrict__ flag)
 {
     extern __shared__ __align__(16) uint32_t dsm[];
     const int nw_max = (S + 31) / 32;
@@ -858,6 +864,7 @@ __global__ void __launch_bounds__(kRowThreads)
     uint32_t *beq = bgt + nw_max;
     __shared__ int scratch[kRowThreads / 32 + 1];
     __shared__ int sel[2];
+    __shared__ int reg_off[kCandRegions];
     grid_dep_wait();
     grid_dep_launch();
     for (int row = blockIdx.x; row < T; row += gridDim.x) {
@@ -871,16 +878,34 @@ __global__ void __launch_bounds__(kRowThreads)
                 flag[row] = 0;
             continue;
         }
-        const int c = cand_cnt[row];
-        if (c < k || c > cap) {
+        // the row's list: kCandRegions regions of rcap entries, region q holding cq
+        const int rcap = cap / 64;
+        const int q = threadIdx.x;
+        const int cq = q < kCandRegions ? __ldg(cand_cnt + static_cast<int64_t>(row) * kCandRegions + q) : 0;
+        int c;
+        const int off = block_exclusive_scan<kRowThreads>(cq, scratch, &c);
+        if (__syncthreads_or(cq > rcap) || c < k || c > cap) {
             if (threadIdx.x == 0)
                 flag[row] = 1;
             continue;
         }
-        const int64_t base = static_cast<int64_t>(row) * cap;
+        // entry f of the concatenated list lies in the last region whose offset is <= f
+        // (binary search over the offsets): every load is independent of the others
+        if (q < kCandRegions)
+            reg_off[q] = off;
+        __syncthreads();
         for (int f = threadIdx.x; f < c; f += kRowThreads) {
-            ck[f] = __ldg(cand_key + base + f);
-            ci[f] = __ldg(cand_idx + base + f);
+            int lo = 0, hi = kCandRegions - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (reg_off[mid] <= f)
+                    lo = mid;
+                else
+                    hi = mid - 1;
+            }
+            const uint2 v = __ldg(cand + (static_cast<int64_t>(row) * kCandRegions + lo) * rcap + (f - reg_off[lo]));
+            ck[f] = v.x;
+            ci[f] = static_cast<int32_t>(v.y);
         }
         const int nw = (n + 31) / 32;
         for (int w = threadIdx.x; w < nw; w += kRowThreads) {
@@ -1054,7 +1079,9 @@ int launch_topk(const TopkArgs &a, cudaStream_t stream, char *err, size_t errlen
             snprintf(err, errlen, "cudaFuncSetAttribute(topk rows): %s", cudaGetErrorString(e_attr));
             return DSA_ERR_CUDA;
         }
-        const int grid = a.T < 65535 * 4 ? a.T : 65535 * 4;
+        // (with a row filter, few rows are expected: one CTA per SM walks the flags)
+        const int cap_grid = a.row_flag ? sms : 65535 * 4;
+        const int grid = a.T < cap_grid ? a.T : cap_grid;
         e = launch_pdl(topk_rows_kernel, dim3(grid), dim3(kRowThreads), kRowSmem, stream, 1, a.logits, a.ld, a.T,
                        a.valid_len, a.k, a.idx, status, a.row_flag);
     }
@@ -1084,9 +1111,8 @@ int launch_topk_threshold(const float *samp, int ld_s, int T, const int32_t *q_p
     return DSA_OK;
 }
 
-int launch_topk_candidates(const uint32_t *cand_key, const int32_t *cand_idx, const int32_t *cand_cnt, int cap,
-                           int T, const int32_t *q_pos, int S, int k, int32_t *idx, int32_t *flag,
-                           cudaStream_t stream, char *err, size_t errlen)
+int launch_topk_candidates(const uint2 *cand, const int32_t *cand_cnt, int cap, int T, const int32_t *q_pos, int S,
+                           int k, int32_t *idx, int32_t *flag, cudaStream_t stream, char *err, size_t errlen)
 {
     const size_t smem = topk_candidates_smem(S, cap);
     if (smem > kCandSmemMax) {
@@ -1100,10 +1126,12 @@ int launch_topk_candidates(const uint32_t *cand_key, const int32_t *cand_idx, co
         snprintf(err, errlen, "cudaFuncSetAttribute(topk candidates): %s", cudaGetErrorString(e_attr));
         return DSA_ERR_CUDA;
     }
-    const int per_sm = smem <= 113 * 1024 ? 2 : 1;
+    // as many rows in flight per SM as shared memory allows (4 at most: the phases of a row end in barriers)
+    int per_sm = static_cast<int>(232448 / (smem + 2048));
+    per_sm = per_sm < 1 ? 1 : (per_sm > 4 ? 4 : per_sm);
     const int grid = T < per_sm * num_sms() ? T : per_sm * num_sms();
-    cudaError_t e = launch_pdl(topk_candidates_kernel, dim3(grid), dim3(kRowThreads), smem, stream, 1, cand_key,
-                               cand_idx, cand_cnt, cap, T, q_pos, S, k, idx, flag);
+    cudaError_t e = launch_pdl(topk_candidates_kernel, dim3(grid), dim3(kRowThreads), smem, stream, 1, cand, cand_cnt,
+                               cap, T, q_pos, S, k, idx, flag);
     if (e != cudaSuccess) {
         snprintf(err, errlen, "topk candidates launch: %s", cudaGetErrorString(e));
         return DSA_ERR_CUDA;

@@ -156,7 +156,7 @@ def test_fused_indexer_topk_validation(lib):
     # sampled keys, per-row positions and thresholds, T x max(4096, 4k) candidates of 8 bytes,
     # T x S fp32 scores for rows redone from full scores
     assert need >= T * 4096 * 8 + T * S * 4 + T * min(S, 2048) * 4
-    assert lib.dsa_indexer_topk_workspace_size(T, S, 64, 128, 2048) > need  # cap grows with k
+    assert lib.dsa_indexer_topk_workspace_size(T, S, 64, 128, 4096) > need  # the list cap grows with k past 2048
     assert lib.dsa_indexer_topk_workspace_size(T, S, 4, 32, k) == 0        # unsupported head shape
     assert lib.dsa_indexer_topk_workspace_size(T, 262145, 64, 128, k) == 0  # past the key limit
     assert lib.dsa_indexer_topk_workspace_size(T, S, 64, 128, 4097) == 0

@@ -54,7 +54,7 @@ def _check(x, k, q_pos, S, sample_rows=16, seed=0):
 
 @pytest.mark.parametrize("L", [1, 700, 5000, 9000, 20000])
 def test_fused_causal_prefill(L):
-    """Every row of a causal prefill: rows up to 8192 keys keep every key, longer rows
+    """Every row of a causal prefill: rows up to 4096 keys keep every key, longer rows
     take the sampled threshold."""
     x = W.prefill_inputs(W.CONFIGS["prefill_4k"], DEV, L=L, seed=L)
     _check(x, 2048, x["q_pos"], L, seed=L)
@@ -62,7 +62,7 @@ def test_fused_causal_prefill(L):
 
 @pytest.mark.parametrize("k", [64, 1000, 3000, 4096])
 def test_fused_k_range(k):
-    L = 20000  # rows past max(4096, 4k) keys take the threshold
+    L = 20000  # rows past max(4096, 2k) keys take the threshold
     x = W.prefill_inputs(W.CONFIGS["prefill_4k"], DEV, L=L, seed=k)
     _check(x, k, x["q_pos"], L, seed=k)
 
