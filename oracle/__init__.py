@@ -53,6 +53,8 @@ def _L():
         lib.dsa_oracle_topk.argtypes = [P, i64, i32, P, i32, P]
         lib.dsa_oracle_sparse_mla.argtypes = [P, P, i32, P, i32, i32, i32, i32, i32, f64, P, P]
         lib.dsa_oracle_sparse_mla_paged.argtypes = [P, P, i32, i32, P, i32, P, P, i32, i32, i32, i32, i32, f64, P, P]
+        lib.dsa_oracle_attn_target.argtypes = [P, P, i32, P, i32, i32, i32, f64, P, i64]
+        lib.dsa_oracle_indexer_kl.argtypes = [P, P, P, i32, i32, i32, P, i32, P, i64, P, P, P, P]
         _lib = lib
     return _lib
 
@@ -170,3 +172,36 @@ def sparse_mla_paged(q_bits, kv_pool_bits, block_table, ctx_len, idx, sm_scale: 
     _L().dsa_oracle_sparse_mla_paged(_p(q), _p(pool), num_pages, page_size, _p(bt), bt.shape[1], _p(cl),
                                      _p(ix), n, H, D, Dv, k, float(sm_scale), _p(out), _p(lse))
     return out, lse
+
+
+def attn_target(q_bits, kv_bits, q_pos, sm_scale: float, ld: int | None = None, fill=np.nan) -> np.ndarray:
+    """Warm-up target: the main attention's dense causal distribution over keys s <= q_pos[r],
+    averaged over heads.  q_bits uint16 [n, H, D], kv_bits uint16 [S, D].  Returns float64 [n, ld]."""
+    q = _c(q_bits, np.uint16)
+    n, H, D = q.shape
+    kv = _c(kv_bits, np.uint16)
+    S = kv.shape[0]
+    ld = S if ld is None else ld
+    out = np.full((n, ld), fill, dtype=np.float64)
+    qp = _c(q_pos, np.int32)
+    _L().dsa_oracle_attn_target(_p(q), _p(kv), S, _p(qp), n, H, D, float(sm_scale), _p(out), ld)
+    return out
+
+
+def indexer_kl(q, w, q_pos, k, p):
+    """Warm-up loss and gradients from dequantised fp64 q [n, HI, dI], k [S, dI], w [n, HI]
+    and the target p [n, >= S].  Returns (loss [n], dw [n, HI], dq [n, HI, dI], dk [S, dI])."""
+    q = _c(q, np.float64)
+    n, HI, dI = q.shape
+    k = _c(k, np.float64)
+    S = k.shape[0]
+    w = _c(w, np.float64)
+    pp = _c(p, np.float64)
+    qp = _c(q_pos, np.int32)
+    loss = np.empty(n, dtype=np.float64)
+    dw = np.empty((n, HI), dtype=np.float64)
+    dq = np.empty((n, HI, dI), dtype=np.float64)
+    dk = np.empty((S, dI), dtype=np.float64)
+    _L().dsa_oracle_indexer_kl(_p(q), _p(w), _p(qp), n, HI, dI, _p(k), S, _p(pp), pp.shape[1], _p(loss), _p(dw),
+                               _p(dq), _p(dk))
+    return loss, dw, dq, dk

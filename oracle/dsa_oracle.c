@@ -394,3 +394,155 @@ void dsa_oracle_sparse_mla_paged(const uint16_t *q, const uint16_t *kv_pool,
         }
     }
 }
+
+/* ------------------------------------------- indexer warm-up (training path)
+ * Release summary "DeepSeek-V3.2-Exp: Boosting Long-Context Efficiency with
+ * DeepSeek Sparse Attention", section "Method": before sparse training, a
+ * dense warm-up trains only the lightning indexer, against a
+ * KL-divergence-to-main-attention target.  Readings (the pages give no
+ * formula): the target of query token t is the main attention's dense causal
+ * distribution over its keys s <= t, averaged over the H query heads (the
+ * indexer has one distribution per token, shared by all heads in MQA mode);
+ * the indexer's distribution is softmax over s <= t of I[t,s]; the loss of
+ * row t is KL(target || indexer) = sum_s p (ln p - ln softmax(I)_s), 0 ln 0 = 0;
+ * gradients are those of the sum of the rows' losses with respect to w and to
+ * the dequantised indexer inputs q = code * q_scale, k = code * k_scale (the
+ * quantiser passes gradients straight through); ReLU'(0) = 0.
+ */
+
+/* p[r*ld + s] for s <= min(q_pos[r], S-1): the mean over heads h of
+ * softmax_s(sm_scale * <Q[r,h,:D], KV[s,:D]>) over s in [0, q_pos[r]]; entries
+ * past the row are left untouched. */
+void dsa_oracle_attn_target(const uint16_t *q, const uint16_t *kv, int S, const int32_t *q_pos, int n, int H, int D,
+                            double sm_scale, double *p, int64_t ld)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int r = 0; r < n; ++r) {
+        int last = q_pos[r];
+        if (last > S - 1)
+            last = S - 1;
+        if (last < 0)
+            continue;
+        const int cnt = last + 1;
+        double *sc = (double *)malloc(sizeof(double) * (size_t)cnt);
+        double *acc = p + (int64_t)r * ld;
+        for (int s = 0; s < cnt; ++s)
+            acc[s] = 0.0;
+        for (int h = 0; h < H; ++h) {
+            const uint16_t *qh = q + ((int64_t)r * H + h) * D;
+            double m = -INFINITY;
+            for (int s = 0; s < cnt; ++s) {
+                double dot = 0.0;
+                for (int d = 0; d < D; ++d)
+                    dot += dsa_oracle_bf16(qh[d]) * dsa_oracle_bf16(kv[(int64_t)s * D + d]);
+                sc[s] = sm_scale * dot;
+                if (sc[s] > m)
+                    m = sc[s];
+            }
+            double z = 0.0;
+            for (int s = 0; s < cnt; ++s)
+                z += exp(sc[s] - m);
+            for (int s = 0; s < cnt; ++s)
+                acc[s] += exp(sc[s] - m) / z / H;
+        }
+        free(sc);
+    }
+}
+
+/* The warm-up loss and its gradients for query rows r < n over keys s <= q_pos[r]
+ * (clamped to S-1), from dequantised fp64 inputs q[n,HI,dI], k[S,dI] and head
+ * weights w[n,HI], given the target p[r*ldp + s]:
+ *   a[r,j,s] = <q[r,j,:], k[s,:]>,  I[r,s] = sum_j w[r,j] max(a, 0)
+ *   L[r]     = sum_s p (ln p - (I - lse_r)),  lse_r = ln sum_s exp I[r,s]
+ *   g[r,s]   = softmax(I)_s - p[r,s]                       (dL/dI, rows of p sum to 1)
+ *   dw[r,j]  = sum_s g max(a, 0)
+ *   dq[r,j,:] = sum_s g w[r,j] [a > 0] k[s,:]
+ *   dk[s,:]  = sum_r sum_j g w[r,j] [a > 0] q[r,j,:]
+ * loss[n], dw[n,HI], dq[n,HI,dI] are written; dk[S,dI] is zeroed and then
+ * accumulated over the rows. */
+void dsa_oracle_indexer_kl(const double *q, const double *w, const int32_t *q_pos, int n, int HI, int dI,
+                           const double *k, int S, const double *p, int64_t ldp, double *loss, double *dw, double *dq,
+                           double *dk)
+{
+    for (int64_t i = 0; i < (int64_t)S * dI; ++i)
+        dk[i] = 0.0;
+    /* per row: I, softmax, loss, g; then dw, dq (rows in parallel) */
+    double *g_all = (double *)malloc(sizeof(double) * (size_t)n * (size_t)(S > 0 ? S : 1));
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int r = 0; r < n; ++r) {
+        int last = q_pos[r];
+        if (last > S - 1)
+            last = S - 1;
+        double *g = g_all + (int64_t)r * S;
+        const double *qr = q + (int64_t)r * HI * dI;
+        const double *wr = w + (int64_t)r * HI;
+        for (int j = 0; j < HI; ++j)
+            dw[(int64_t)r * HI + j] = 0.0;
+        for (int64_t i = 0; i < (int64_t)HI * dI; ++i)
+            dq[(int64_t)r * HI * dI + i] = 0.0;
+        if (last < 0) {
+            loss[r] = 0.0;
+            continue;
+        }
+        const int cnt = last + 1;
+        double m = -INFINITY;
+        for (int s = 0; s < cnt; ++s) {
+            double I = 0.0;
+            for (int j = 0; j < HI; ++j) {
+                double a = 0.0;
+                for (int d = 0; d < dI; ++d)
+                    a += qr[(int64_t)j * dI + d] * k[(int64_t)s * dI + d];
+                I += wr[j] * (a > 0.0 ? a : 0.0);
+            }
+            g[s] = I; /* holds I for now */
+            if (I > m)
+                m = I;
+        }
+        double z = 0.0;
+        for (int s = 0; s < cnt; ++s)
+            z += exp(g[s] - m);
+        const double lse = m + log(z);
+        double L = 0.0;
+        for (int s = 0; s < cnt; ++s) {
+            const double ps = p[(int64_t)r * ldp + s];
+            if (ps > 0.0)
+                L += ps * (log(ps) - (g[s] - lse));
+            g[s] = exp(g[s] - lse) - ps;
+        }
+        loss[r] = L;
+        for (int s = 0; s < cnt; ++s) {
+            for (int j = 0; j < HI; ++j) {
+                double a = 0.0;
+                for (int d = 0; d < dI; ++d)
+                    a += qr[(int64_t)j * dI + d] * k[(int64_t)s * dI + d];
+                if (a > 0.0) {
+                    dw[(int64_t)r * HI + j] += g[s] * a;
+                    for (int d = 0; d < dI; ++d)
+                        dq[((int64_t)r * HI + j) * dI + d] += g[s] * wr[j] * k[(int64_t)s * dI + d];
+                }
+            }
+        }
+    }
+    /* dk: keys in parallel, each summing over the rows that see it */
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int s = 0; s < S; ++s) {
+        for (int r = 0; r < n; ++r) {
+            int last = q_pos[r];
+            if (last > S - 1)
+                last = S - 1;
+            if (s > last)
+                continue;
+            const double gs = g_all[(int64_t)r * S + s];
+            const double *qr = q + (int64_t)r * HI * dI;
+            for (int j = 0; j < HI; ++j) {
+                double a = 0.0;
+                for (int d = 0; d < dI; ++d)
+                    a += qr[(int64_t)j * dI + d] * k[(int64_t)s * dI + d];
+                if (a > 0.0)
+                    for (int d = 0; d < dI; ++d)
+                        dk[(int64_t)s * dI + d] += gs * w[(int64_t)r * HI + j] * qr[(int64_t)j * dI + d];
+            }
+        }
+    }
+    free(g_all);
+}

@@ -13,6 +13,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_pins as pins
+from tests import test_oracle_training as tpins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "dsa_oracle.c")
 
@@ -54,6 +55,16 @@ MUTANTS = {
     "quant_amax_signed": ("const float m = fabsf(xr[c]);", "const float m = xr[c];"),
     "quant_zero_row_scale": ("        float s = 1.f;\n", "        float s = 0.5f;\n"),
     "ue8m0_rounds_down": ("ldexp(1.0, e)", "ldexp(1.0, e - 1)"),
+    # indexer warm-up (training path)
+    "kl_grad_sign": ("g[s] = exp(g[s] - lse) - ps;", "g[s] = ps - exp(g[s] - lse);"),
+    "kl_lse_dropped": ("L += ps * (log(ps) - (g[s] - lse));", "L += ps * (log(ps) - g[s]);"),
+    "kl_dq_relu_mask_dropped": ("                if (a > 0.0) {", "                if (1) {"),
+    "kl_dw_relu_dropped": ("dw[(int64_t)r * HI + j] += g[s] * a;", "dw[(int64_t)r * HI + j] += g[s];"),
+    "kl_dk_weight_dropped": ("dk[(int64_t)s * dI + d] += gs * w[(int64_t)r * HI + j] * qr[(int64_t)j * dI + d];",
+                             "dk[(int64_t)s * dI + d] += gs * qr[(int64_t)j * dI + d];"),
+    "target_not_head_mean": ("acc[s] += exp(sc[s] - m) / z / H;", "acc[s] += exp(sc[s] - m) / z;"),
+    "target_causal_exclusive": ("const int cnt = last + 1;\n        double *sc", "const int cnt = last;\n        double *sc"),
+    "target_scale_dropped": ("sc[s] = sm_scale * dot;", "sc[s] = dot;"),
 }
 
 PINS = [
@@ -78,6 +89,11 @@ PINS = [
     lambda: pins.test_e4m3_encoder_ties_to_even_and_saturates(),
     lambda: pins.test_e4m3_encoder_matches_torch_cast(),
     lambda: pins.test_quantize_matches_torch_per_row_and_scale_modes(),
+    lambda: tpins.test_gradients_match_central_differences(),
+    lambda: tpins.test_minimum_at_the_indexers_own_distribution(),
+    lambda: tpins.test_uniform_indexer_closed_form(),
+    lambda: tpins.test_target_one_head_is_the_library_softmax(),
+    lambda: tpins.test_target_is_the_head_mean_and_sums_to_one(),
 ]
 
 
