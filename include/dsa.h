@@ -215,6 +215,42 @@ int dsa_indexer_topk(const void *q8, const float *q_scale, const float *w, int T
 size_t dsa_indexer_topk_workspace_size(int T, int S, int H_I, int d_I, int k);
 
 /*
+ * dsa_indexer_warmup: the indexer's dense warm-up step, loss and gradients.
+ *
+ * Release summary "DeepSeek-V3.2-Exp: Boosting Long-Context Efficiency with
+ * DeepSeek Sparse Attention", section "Method": before sparse training a dense
+ * warm-up trains only the lightning indexer, against a KL-divergence-to-main-
+ * attention target.  Readings (the pages give no formula): for query row t at
+ * position q_pos[t] (clamped to S-1) over keys s <= q_pos[t]
+ *   p[t,s]   = mean over the H heads of softmax_s(sm_scale * <q[t,h,:576], kv[s,:576]>)
+ *              (the main attention's dense causal distribution, MQA mode)
+ *   I[t,s]   = the index score of dsa_indexer_logits, a[t,j,s] = <q8[t,j]*q_scale[t], k8[s]*k_scale[s]>
+ *   loss[t]  = sum_s p (ln p - ln softmax_s I[t,:])
+ *   dw[t,j]  = d(sum loss)/dw = sum_s g ReLU(a),      g = softmax(I) - p
+ *   dq[t,j,:] = sum_s g w[t,j] [a > 0] k[s,:] * k_scale[s]      (w.r.t. the dequantised q)
+ *   dk[s,:]  = sum_t sum_j g w[t,j] [a > 0] q[t,j,:] * q_scale[t] (w.r.t. the dequantised k)
+ * (the FP8 quantiser passes gradients straight through; ReLU'(0) = 0).
+ *
+ *   q [T, H, 576] bf16, kv [S, 576] bf16, 1 <= H <= 128, sm_scale > 0;
+ *   q8, q_scale, w, q_pos, k8, k_scale: as for dsa_indexer_logits with
+ *   contiguous keys, (H_I, d_I) = (64, 128) or (32, 128);
+ *   outputs fp32: loss [T], dw [T, H_I], dq [T, H_I, d_I], dk [S, d_I].
+ *   workspace: dsa_indexer_warmup_workspace_size(T, S, H_I, d_I) bytes, 256-byte
+ *   aligned, owned by the caller (it holds p, I and then g, and the per-(t, j, s)
+ *   coefficients of dk: about 4 (2 + H_I) T S bytes).
+ * Precision: the target's scores on BF16 tensor cores with fp32 accumulation,
+ * the index scores as dsa_indexer_logits, everything after in fp32.
+ */
+int dsa_indexer_warmup(const void *q, const void *kv, int H, float sm_scale,
+                       const void *q8, const float *q_scale, const float *w, int H_I, int d_I,
+                       const void *k8, const float *k_scale, const int32_t *q_pos, int T, int S,
+                       float *loss, float *dw, float *dq, float *dk,
+                       void *workspace, size_t workspace_bytes, dsa_stream_t stream);
+
+/* Bytes of workspace dsa_indexer_warmup needs (0 on unsupported sizes). */
+size_t dsa_indexer_warmup_workspace_size(int T, int S, int H_I, int d_I);
+
+/*
  * dsa_sparse_mla_prefill: MQA-mode sparse MLA over the selected rows (stage 3).
  *
  * For query row t, head h and its valid selected rows s_i = idx[t*k + i]

@@ -459,10 +459,31 @@ void dsa_oracle_attn_target(const uint16_t *q, const uint16_t *kv, int S, const 
  *   dq[r,j,:] = sum_s g w[r,j] [a > 0] k[s,:]
  *   dk[s,:]  = sum_r sum_j g w[r,j] [a > 0] q[r,j,:]
  * loss[n], dw[n,HI], dq[n,HI,dI] are written; dk[S,dI] is zeroed and then
- * accumulated over the rows. */
+ * accumulated over the rows.
+ *
+ * mask_fp32: the ReLU decision [a > 0] is a discrete one that rounding can flip
+ * when a is within a few fp32 ulps of 0, and it moves the gradient by a whole
+ * g w k term.  With mask_fp32 != 0 the decision is taken on a computed the way
+ * the GPU kernel computes it (fp32 values of q and k, fp32 fused multiply-adds
+ * over d in groups of four, within a group from d + 3 down to d); every value
+ * stays fp64.  With 0 (the default of the pins) the decision is exact. */
+static int relu_on(const double *qv, const double *kv, int dI, double a, int mask_fp32)
+{
+    if (!mask_fp32)
+        return a > 0.0;
+    float acc = 0.f;
+    for (int d = 0; d < dI; d += 4) {
+        float t = acc;
+        for (int e = 3; e >= 0; --e)
+            t = fmaf((float)qv[d + e], (float)kv[d + e], t);
+        acc = t;
+    }
+    return acc > 0.f;
+}
+
 void dsa_oracle_indexer_kl(const double *q, const double *w, const int32_t *q_pos, int n, int HI, int dI,
                            const double *k, int S, const double *p, int64_t ldp, double *loss, double *dw, double *dq,
-                           double *dk)
+                           double *dk, int mask_fp32)
 {
     for (int64_t i = 0; i < (int64_t)S * dI; ++i)
         dk[i] = 0.0;
@@ -515,7 +536,7 @@ void dsa_oracle_indexer_kl(const double *q, const double *w, const int32_t *q_po
                 double a = 0.0;
                 for (int d = 0; d < dI; ++d)
                     a += qr[(int64_t)j * dI + d] * k[(int64_t)s * dI + d];
-                if (a > 0.0) {
+                if (relu_on(qr + (int64_t)j * dI, k + (int64_t)s * dI, dI, a, mask_fp32)) {
                     dw[(int64_t)r * HI + j] += g[s] * a;
                     for (int d = 0; d < dI; ++d)
                         dq[((int64_t)r * HI + j) * dI + d] += g[s] * wr[j] * k[(int64_t)s * dI + d];
@@ -538,7 +559,7 @@ void dsa_oracle_indexer_kl(const double *q, const double *w, const int32_t *q_po
                 double a = 0.0;
                 for (int d = 0; d < dI; ++d)
                     a += qr[(int64_t)j * dI + d] * k[(int64_t)s * dI + d];
-                if (a > 0.0)
+                if (relu_on(qr + (int64_t)j * dI, k + (int64_t)s * dI, dI, a, mask_fp32))
                     for (int d = 0; d < dI; ++d)
                         dk[(int64_t)s * dI + d] += gs * w[(int64_t)r * HI + j] * qr[(int64_t)j * dI + d];
             }

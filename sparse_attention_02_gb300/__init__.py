@@ -61,9 +61,13 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.dsa_sparse_mla_decode_workspace_size.restype = sz
     lib.dsa_sparse_mla_decode_workspace_size.argtypes = [i32, i32, i32]
     lib.dsa_indexer_topk.argtypes = [P, P, P, i32, i32, i32, P, P, i32, P, i32, P, P, sz, P]
+    lib.dsa_indexer_warmup.argtypes = [P, P, i32, f32, P, P, P, i32, i32, P, P, P, i32, i32, P, P, P, P, P, sz, P]
+    lib.dsa_indexer_warmup_workspace_size.restype = sz
+    lib.dsa_indexer_warmup_workspace_size.argtypes = [i32, i32, i32, i32]
     lib.dsa_indexer_topk_workspace_size.restype = sz
     lib.dsa_indexer_topk_workspace_size.argtypes = [i32, i32, i32, i32, i32]
-    for name in ("dsa_quantize_fp8", "dsa_indexer_logits", "dsa_topk", "dsa_indexer_topk", "dsa_sparse_mla_prefill",
+    for name in ("dsa_quantize_fp8", "dsa_indexer_logits", "dsa_topk", "dsa_indexer_topk", "dsa_indexer_warmup",
+                 "dsa_sparse_mla_prefill",
                  "dsa_sparse_mla_decode_paged",
                  "dsa_sparse_mla_decode_paged_noalloc", "dsa_prefill_host", "dsa_get_device_status"):
         getattr(lib, name).restype = i32
@@ -221,6 +225,48 @@ def dsa_indexer_topk(q8, q_scale, w, k8, k_scale, q_pos, k: int, idx, workspace=
                                            _ptr(q_pos), k, _ptr(idx), _ptr(workspace),
                                            workspace.numel() * workspace.element_size(), _stream(stream)))
     return idx
+
+
+def dsa_indexer_warmup_workspace_size(T: int, S: int, H_I: int, d_I: int) -> int:
+    return int(load_library().dsa_indexer_warmup_workspace_size(T, S, H_I, d_I))
+
+
+def dsa_indexer_warmup(q, kv, sm_scale: float, q8, q_scale, w, k8, k_scale, q_pos, loss, dw, dq, dk,
+                       workspace=None, stream=None):
+    """Indexer warm-up: the KL loss of the index scores' softmax against the main attention's
+    head-averaged dense distribution, and its gradients.  q bf16 [T, H, 576], kv bf16 [S, 576];
+    indexer inputs as for dsa_indexer_logits (contiguous keys); outputs fp32 loss [T],
+    dw [T, H_I], dq [T, H_I, d_I], dk [S, d_I].  ``workspace``: a uint8 CUDA tensor of at least
+    dsa_indexer_warmup_workspace_size(T, S, H_I, d_I) bytes; taken from PyTorch when None."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(kv, torch.bfloat16, "kv", 2)
+    _need(q8, torch.uint8, "q8", 3)
+    _need(q_scale, torch.float32, "q_scale", 1)
+    _need(w, torch.float32, "w", 2)
+    _need(k8, torch.uint8, "k8", 2)
+    _need(k_scale, torch.float32, "k_scale", 1)
+    _need(q_pos, torch.int32, "q_pos", 1)
+    for t, name, dim in ((loss, "loss", 1), (dw, "dw", 2), (dq, "dq", 3), (dk, "dk", 2)):
+        _need(t, torch.float32, name, dim)
+    T, H, D = q.shape
+    S = kv.shape[0]
+    _, HI, dI = q8.shape
+    if D != 576 or kv.shape[1] != 576 or q8.shape[0] != T or q_scale.shape[0] != T or tuple(w.shape) != (T, HI) \
+            or tuple(k8.shape) != (S, dI) or k_scale.shape[0] != S or q_pos.shape[0] != T \
+            or loss.shape[0] != T or tuple(dw.shape) != (T, HI) or tuple(dq.shape) != (T, HI, dI) \
+            or tuple(dk.shape) != (S, dI):
+        raise ValueError("inconsistent shapes")
+    if workspace is None:
+        need = dsa_indexer_warmup_workspace_size(T, S, HI, dI)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    _same_device(workspace, "workspace")
+    _check(load_library().dsa_indexer_warmup(_ptr(q), _ptr(kv), H, float(sm_scale), _ptr(q8), _ptr(q_scale),
+                                             _ptr(w), HI, dI, _ptr(k8), _ptr(k_scale), _ptr(q_pos), T, S, _ptr(loss),
+                                             _ptr(dw), _ptr(dq), _ptr(dk), _ptr(workspace),
+                                             workspace.numel() * workspace.element_size(), _stream(stream)))
+    return loss, dw, dq, dk
 
 
 def dsa_sparse_mla_prefill(q, kv, idx, sm_scale: float, out, lse, stream=None):

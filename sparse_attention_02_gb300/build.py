@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_objs")
 LIB = os.path.join(HERE, "libdsa.so")
-SOURCES = ["api.cu", "quantize.cu", "indexer.cu", "topk.cu", "indexer_topk.cu", "sparse_mla.cu", "prefill_host.cu"]
+SOURCES = ["api.cu", "quantize.cu", "indexer.cu", "topk.cu", "indexer_topk.cu", "warmup.cu", "sparse_mla.cu", "prefill_host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

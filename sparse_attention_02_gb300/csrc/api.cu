@@ -222,6 +222,42 @@ int dsa_indexer_topk(const void *q8, const float *q_scale, const float *w, int T
     return rc == DSA_OK ? ok() : rc;
 }
 
+size_t dsa_indexer_warmup_workspace_size(int T, int S, int H_I, int d_I)
+{
+    if (T < 0 || S < 1 || d_I != 128 || (H_I != 64 && H_I != 32))
+        return 0;
+    return warmup_workspace_bytes(T, S, H_I);
+}
+
+int dsa_indexer_warmup(const void *q, const void *kv, int H, float sm_scale, const void *q8, const float *q_scale,
+                       const float *w, int H_I, int d_I, const void *k8, const float *k_scale, const int32_t *q_pos,
+                       int T, int S, float *loss, float *dw, float *dq, float *dk, void *workspace,
+                       size_t workspace_bytes, dsa_stream_t stream)
+{
+    if (T < 0 || S < 1)
+        return fail(DSA_ERR_INVALID_ARG, "T < 0 or S < 1");
+    if (T == 0)
+        return ok();
+    if (!q || !kv || !q8 || !q_scale || !w || !k8 || !k_scale || !q_pos || !loss || !dw || !dq || !dk)
+        return fail(DSA_ERR_INVALID_ARG, "null pointer argument");
+    if (H < 1 || H > 128)
+        return fail(DSA_ERR_UNSUPPORTED, "H must be in [1, 128]");
+    if (d_I != 128 || (H_I != 64 && H_I != 32))
+        return fail(DSA_ERR_UNSUPPORTED, "warm-up: (H_I, d_I) must be (64, 128) or (32, 128)");
+    if (!(sm_scale > 0.f) || sm_scale > 1e30f)
+        return fail(DSA_ERR_INVALID_ARG, "sm_scale must be positive and finite");
+    if (!aligned16(q) || !aligned16(kv) || !aligned16(q8) || !aligned16(k8) || !aligned16(dq))
+        return fail(DSA_ERR_ALIGNMENT, "q, kv, q8, k8 and dq must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(DSA_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+    if (!workspace || workspace_bytes < warmup_workspace_bytes(T, S, H_I))
+        return fail(DSA_ERR_WORKSPACE, "workspace missing or smaller than dsa_indexer_warmup_workspace_size");
+    WarmupArgs a{q, kv, H, sm_scale, q8, q_scale, w, H_I, d_I, k8, k_scale, q_pos, T, S, loss, dw, dq, dk,
+                 workspace, workspace_bytes};
+    int rc = launch_warmup(a, reinterpret_cast<cudaStream_t>(stream), t_err, sizeof t_err);
+    return rc == DSA_OK ? ok() : rc;
+}
+
 int dsa_quantize_fp8(const float *x, int64_t rows, int64_t cols, int scale_mode, void *codes, float *scale,
                      dsa_stream_t stream)
 {

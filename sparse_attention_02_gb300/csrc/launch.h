@@ -142,6 +142,29 @@ struct IndexerTopkArgs {
 int launch_indexer_topk(const IndexerTopkArgs &a, cudaStream_t stream, char *err, size_t errlen);
 size_t indexer_topk_workspace_bytes(int T, int S, int dI, int k);
 
+struct WarmupArgs {
+    const void *q;       // [T, H, 576] bf16: main-attention queries
+    const void *kv;      // [S, 576] bf16
+    int H;
+    float sm_scale;
+    const void *q8;      // indexer inputs as for dsa_indexer_logits (contiguous keys)
+    const float *q_scale;
+    const float *w;
+    int HI, dI;
+    const void *k8;
+    const float *k_scale;
+    const int32_t *q_pos;
+    int T, S;
+    float *loss;         // [T]
+    float *dw;           // [T, HI]
+    float *dq;           // [T, HI, dI]
+    float *dk;           // [S, dI]
+    void *workspace;
+    size_t workspace_bytes;
+};
+int launch_warmup(const WarmupArgs &a, cudaStream_t stream, char *err, size_t errlen);
+size_t warmup_workspace_bytes(int T, int S, int HI);
+
 struct MlaArgs {
     const void *q;      // [T, H, 576] bf16
     const void *kv;     // [S, 576] bf16, or pool [num_pages, page_size, 576]

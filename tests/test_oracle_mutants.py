@@ -58,7 +58,7 @@ MUTANTS = {
     # indexer warm-up (training path)
     "kl_grad_sign": ("g[s] = exp(g[s] - lse) - ps;", "g[s] = ps - exp(g[s] - lse);"),
     "kl_lse_dropped": ("L += ps * (log(ps) - (g[s] - lse));", "L += ps * (log(ps) - g[s]);"),
-    "kl_dq_relu_mask_dropped": ("                if (a > 0.0) {", "                if (1) {"),
+    "kl_grad_relu_mask_dropped": ("        return a > 0.0;", "        return 1;"),
     "kl_dw_relu_dropped": ("dw[(int64_t)r * HI + j] += g[s] * a;", "dw[(int64_t)r * HI + j] += g[s];"),
     "kl_dk_weight_dropped": ("dk[(int64_t)s * dI + d] += gs * w[(int64_t)r * HI + j] * qr[(int64_t)j * dI + d];",
                              "dk[(int64_t)s * dI + d] += gs * qr[(int64_t)j * dI + d];"),

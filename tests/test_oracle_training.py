@@ -124,3 +124,15 @@ def test_target_is_the_head_mean_and_sums_to_one():
     assert np.allclose(oracle.attn_target(qb[:, perm], kvb, qp, 1 / 24), p, rtol=1e-12, equal_nan=True)
     heads = [oracle.attn_target(qb[:, h:h + 1], kvb, qp, 1 / 24) for h in range(H)]
     assert np.allclose(np.mean(heads, axis=0), p, rtol=1e-12, equal_nan=True)
+
+
+def test_fp32_mask_changes_only_decisions_near_the_kink():
+    """The fp32 ReLU decision (the kernel's precision) agrees with the exact one away from
+    a = 0: on inputs with no dot product near 0 both options give the same gradients."""
+    q, w, qp, k, p = _case(6)
+    exact = oracle.indexer_kl(q, w, qp, k, p)
+    f32 = oracle.indexer_kl(q, w, qp, k, p, mask_fp32=True)
+    a = np.einsum("rjd,sd->rjs", q, k)
+    assert np.abs(a).min() > 1e-3  # no decision near the kink in this case
+    for x, y in zip(exact, f32):
+        assert np.array_equal(x, y)
