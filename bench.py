@@ -38,6 +38,7 @@ WORKLOAD = "prefill_32k"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s): the derived FP8 peak, a side column
 OTHER_WORKLOADS = ("tiny", "prefill_4k", "chunked_128k")
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # CUDA-core FP32 FMA rate: SMs x lanes x 2 FLOP x max clock
 NOMINAL = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0, "fp8_tflops": 4500.0}  # GB300 datasheet, dense
 PROFILES = os.path.join(ROOT, "profiles")
 
@@ -479,6 +480,50 @@ def fused_bench(dsa, x, b, cfg, steps, warmup, flush, dev, two_call_stages, chun
                     "written) then sparse MLA, per chunk"}
 
 
+def warmup_bench(dsa, steps, warmup, flush, peaks, peaks_src, mm, dev, name="prefill_4k"):
+    """The indexer's warm-up step (dsa_indexer_warmup: target, loss, gradients) on the L = 4096
+    prefill shapes.  Work counted once per step: the target's QK^T (one pass; the kernel takes
+    two, one for the per-head LSE and one for the probabilities), the FP8 index scores, and the
+    backward's three contractions (a, then dq and dk), 2 x H_I x d_I FLOP per (row, key) each."""
+    cfg = W.CONFIGS[name]
+    L = cfg.L
+    x = W.prefill_inputs(cfg, dev)
+    loss = torch.empty((L,), device=dev)
+    dw = torch.empty((L, cfg.HI), device=dev)
+    dq = torch.empty((L, cfg.HI, cfg.dI), device=dev)
+    dk = torch.empty((L, cfg.dI), device=dev)
+    ws = torch.empty(dsa.dsa_indexer_warmup_workspace_size(L, L, cfg.HI, cfg.dI), dtype=torch.uint8, device=dev)
+
+    def call():
+        dsa.dsa_indexer_warmup(x["q"], x["kv"], cfg.sm_scale, x["q8"], x["qs"], x["w"], x["k8"], x["ks"], x["q_pos"],
+                               loss, dw, dq, dk, workspace=ws)
+
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    step_ms, _ = time_calls([(0, call)], steps, warmup, flush)
+    clk = clocks.stop()
+    pk = run_peaks(peaks, peaks_src, clk, mm)
+    pairs = L * (L + 1) / 2
+    f_target = 2.0 * cfg.H * cfg.D * pairs
+    f_index = 2.0 * cfg.HI * cfg.dI * pairs
+    f_bwd = 3 * 2.0 * cfg.HI * cfg.dI * pairs
+    ms = float(step_ms.mean())
+    total = f_target + f_index + f_bwd
+    lower_ms = (f_target / (pk["bf16"] * 1e12) + f_index / (pk["fp8"] * 1e12) + f_bwd / (FP32_ALU_TFLOPS * 1e12)) * 1e3
+    finite = bool(torch.isfinite(loss).all() and torch.isfinite(dq).all() and torch.isfinite(dk).all())
+    del ws, x
+    torch.cuda.empty_cache()
+    return {"workload": f"{name}: L={L} causal, H={cfg.H} D={cfg.D} bf16 target, indexer H_I={cfg.HI} d_I={cfg.dI} FP8",
+            "ms_per_step": ms, "tokens_per_s": L / (ms / 1e3), "steps": steps,
+            "flop": {"target_qk": f_target, "indexer": f_index, "backward": f_bwd},
+            "achieved_tflops": total / (ms / 1e3) / 1e12,
+            "roofline_ms": lower_ms, "frac": lower_ms / ms,
+            "bound": "target on BF16 tensor cores, index scores on FP8, backward on the CUDA cores (fp32 FMA)",
+            "peak_source": {"bf16": pk["bf16_how"], "fp8": pk["fp8_how"],
+                            "fp32_alu": f"{FP32_ALU_TFLOPS:.1f} TFLOP/s (152 SMs x 128 FMA/clk x 2 x 2.07 GHz)"},
+            "outputs_finite": finite, "clocks": clk}
+
+
 def workload_bench(dsa, name, steps, warmup, flush, peaks, peaks_src, mm, dev):
     """One more configured prefill workload (tiny, L = 4096, or the chunked L = 131072):
     per-stage ms, tokens/s and roofline fractions, clocks sampled over its own timed region."""
@@ -780,6 +825,7 @@ def main():
             n_steps = 3 if W.CONFIGS[name].chunk else max(3, min(args.steps, 10))
             line["workloads"][name] = workload_bench(dsa, name, n_steps, args.warmup, flush, peaks, peaks_src, mm,
                                                      dev)
+        line["workloads"]["warmup_4k"] = warmup_bench(dsa, 5, args.warmup, flush, peaks, peaks_src, mm, dev)
     if dist:
         dist.barrier()
         dist.destroy_process_group()
