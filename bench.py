@@ -660,6 +660,37 @@ def decode_bench(dsa, steps, warmup, flush, peaks, dev):
                                "sparse_mla": attn_bytes / (st[2] / 1e3) / 1e9 / hbm}}
 
 
+def e2e_timeline(dsa, step, steps, max_chunks_per_call=64):
+    """After the timed steps, the same number of steps again with dsa_prefill_host's per-chunk
+    timeline on (outside the timed region): per call, its span from the first input copy to the
+    last output copy, the time its three streams were busy, and how long the stages' stream sat
+    waiting between chunks (for copies).  A slow step shows up on the stream whose time grew."""
+    cap = steps * max_chunks_per_call
+    dsa.dsa_prefill_host_trace(cap)
+    try:
+        for _ in range(steps):
+            step()
+        torch.cuda.synchronize()
+        t, call, rows = dsa.dsa_prefill_host_trace_read(cap)
+    finally:
+        dsa.dsa_prefill_host_trace(0)
+    out = {"span_ms": [], "h2d_busy_ms": [], "stages_busy_ms": [], "stages_wait_ms": [], "d2h_busy_ms": [],
+           "chunks_per_call": 0}
+    for c in range(steps):
+        m = t[call == c].astype(np.float64)
+        if not len(m):
+            continue
+        out["chunks_per_call"] = int(len(m))
+        busy = lambda a, b: float(np.sum(m[:, b] - m[:, a]))
+        stages = busy(2, 3)
+        out["span_ms"].append(round(float(m[:, 5].max() - m[:, 0].min()), 3))
+        out["h2d_busy_ms"].append(round(busy(0, 1), 3))
+        out["stages_busy_ms"].append(round(stages, 3))
+        out["stages_wait_ms"].append(round(float(m[:, 3].max() - m[:, 2].min()) - stages, 3))
+        out["d2h_busy_ms"].append(round(busy(4, 5), 3))
+    return out
+
+
 def e2e_bench(dsa, x, b, cfg, steps, dev, chunk_rows=2048):
     """The same step through the public C ABI on pinned HOST buffers: dsa_prefill_host copies the
     inputs in, runs the three stages chunk by chunk (copies of one chunk overlap the kernels of
@@ -694,12 +725,14 @@ def e2e_bench(dsa, x, b, cfg, steps, dev, chunk_rows=2048):
     torch.cuda.synchronize()
     each = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
     ms = ev[0].elapsed_time(ev[steps]) / steps
+    trace = e2e_timeline(dsa, step, steps)
     # the host outputs are the device path's outputs (same kernels, same rows)
     same = bool(torch.equal(out_h.view(torch.int16), b["out"].cpu().view(torch.int16)))
     del ws, host
     return {"value": cfg.L / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": ms, "ms_each_step": [round(x, 3) for x in each],
             "median_ms_per_step": float(np.median(each)),
+            "timeline": trace,
             "api": "dsa_prefill_host",
             "chunk_rows": chunk_rows, "matches_device_path": same}
 

@@ -362,6 +362,35 @@ int dsa_prefill_host(const void *q8, const float *q_scale, const float *w, const
 size_t dsa_prefill_host_workspace_size(int T, int S, int H_I, int d_I, int H, int k, int chunk_rows);
 
 /*
+ * dsa_prefill_host_trace: a per-chunk timeline of dsa_prefill_host calls on
+ * the current device, to see which stream a slow call spent its time on (a
+ * debugging record with no counterpart on the pages; off unless turned on).
+ * max_chunks > 0 creates 6 * max_chunks + 1 timing events and starts an empty
+ * record; every later call then records, for each of its chunks while the
+ * record has room, an event on the input-copy stream before and after the
+ * chunk's input copies, on `stream` before and after its three stages, and on
+ * the output-copy stream before and after its output copies.  Each "before"
+ * event follows the chunk's waits, so it marks when that stream began the
+ * chunk.  max_chunks = 0 ends the record and destroys its events.  Returns
+ * DSA_ERR_INVALID_ARG for max_chunks outside [0, 2^20], DSA_ERR_CUDA if the
+ * events cannot be created (recording is then off).
+ */
+int dsa_prefill_host_trace(int max_chunks);
+
+/*
+ * dsa_prefill_host_trace_read: the record of dsa_prefill_host_trace.  Waits
+ * for the recorded events and writes, for the first min(recorded, max_chunks)
+ * chunks in enqueue order (HOST arrays): ms[6 j + e] = milliseconds from the
+ * start of the first recorded call to event e of chunk j (0/1 input copies
+ * begin/end, 2/3 stages begin/end, 4/5 output copies begin/end; NaN for an
+ * event a failed call never reached), call[j] = the call the chunk belongs to
+ * (0 = first recorded call), rows[j] = its query rows; *n_out = the chunks
+ * written.  The record stays as it is. Returns DSA_ERR_INVALID_ARG for a null
+ * pointer or max_chunks < 0.
+ */
+int dsa_prefill_host_trace_read(float *ms, int32_t *call, int32_t *rows, int max_chunks, int *n_out);
+
+/*
  * dsa_sparse_mla_decode_paged_noalloc: dsa_sparse_mla_decode_paged without a
  * caller-provided workspace.  The pages have no counterpart to this entry
  * point: it is for callers that cannot allocate device memory while they

@@ -14,6 +14,7 @@ from __future__ import annotations
 import ctypes
 import os
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -56,6 +57,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.dsa_prefill_host.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, P, P, i32, P, sz, P]
     lib.dsa_prefill_host_workspace_size.restype = sz
     lib.dsa_prefill_host_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    lib.dsa_prefill_host_trace.argtypes = [i32]
+    lib.dsa_prefill_host_trace_read.argtypes = [P, P, P, i32, ctypes.POINTER(i32)]
     lib.dsa_selftest_wait_timeout.argtypes = [ctypes.c_uint32, P]
     lib.dsa_selftest_wait_timeout.restype = i32
     lib.dsa_sparse_mla_decode_workspace_size.restype = sz
@@ -69,7 +72,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     for name in ("dsa_quantize_fp8", "dsa_indexer_logits", "dsa_topk", "dsa_indexer_topk", "dsa_indexer_warmup",
                  "dsa_sparse_mla_prefill",
                  "dsa_sparse_mla_decode_paged",
-                 "dsa_sparse_mla_decode_paged_noalloc", "dsa_prefill_host", "dsa_get_device_status"):
+                 "dsa_sparse_mla_decode_paged_noalloc", "dsa_prefill_host", "dsa_prefill_host_trace",
+                 "dsa_prefill_host_trace_read", "dsa_get_device_status"):
         getattr(lib, name).restype = i32
     if path is None:
         _lib = lib
@@ -388,6 +392,23 @@ def dsa_prefill_host(q8, q_scale, w, q_pos, k8, k_scale, q, kv, sm_scale: float,
                                            _ptr(q), _ptr(kv), T, S, H_I, d_I, H, k, float(sm_scale), _ptr(out),
                                            _ptr(lse), chunk_rows, _ptr(workspace), ws_bytes, _stream(stream)))
     return out, lse
+
+
+def dsa_prefill_host_trace(max_chunks: int):
+    """Start (max_chunks > 0) or end (0) the per-chunk timeline record of dsa_prefill_host calls."""
+    _check(load_library().dsa_prefill_host_trace(int(max_chunks)))
+
+
+def dsa_prefill_host_trace_read(max_chunks: int):
+    """The recorded timeline: (ms [n, 6] float32 from the first recorded call's start to each chunk's
+    input-copy begin/end, stages begin/end, output-copy begin/end; call [n]; rows [n])."""
+    ms = np.full((max_chunks, 6), np.nan, dtype=np.float32)
+    call = np.zeros(max_chunks, dtype=np.int32)
+    rows = np.zeros(max_chunks, dtype=np.int32)
+    n = ctypes.c_int(0)
+    _check(load_library().dsa_prefill_host_trace_read(ms.ctypes.data, call.ctypes.data, rows.ctypes.data,
+                                                       int(max_chunks), ctypes.byref(n)))
+    return ms[:n.value], call[:n.value], rows[:n.value]
 
 
 def dsa_selftest_wait_timeout(limit_us: int, stream=None):

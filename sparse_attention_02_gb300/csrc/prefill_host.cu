@@ -13,6 +13,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <limits>
 #include <mutex>
 #include <vector>
 #include <stdio.h>
@@ -37,12 +38,20 @@ __global__ void pos_to_len_kernel(const int32_t *__restrict__ q_pos, int n, int3
         len[i] = q_pos[i] + 1;
 }
 
-// Copy streams and events of one device, created on its first call and kept.
+// Events of a chunk's timeline (dsa_prefill_host_trace), in this order.
+enum { kInBegin, kInEnd, kKernBegin, kKernEnd, kOutBegin, kOutEnd, kTraceEvents };
+
+// Copy streams and events of one device, created on its first call and kept;
+// the timeline record only while dsa_prefill_host_trace has it on.
 struct HostPipe {
     bool ready = false;
     cudaStream_t h2d = nullptr, d2h = nullptr;
     cudaEvent_t start = nullptr, end = nullptr;
     cudaEvent_t in_ready[kSlots] = {}, slot_done[kSlots] = {}, out_copied[kSlots] = {};
+    int trace_cap = 0, trace_n = 0, trace_calls = 0; // chunks the record holds, has, calls recorded
+    cudaEvent_t trace_t0 = nullptr;                  // start of the first recorded call
+    std::vector<cudaEvent_t> trace_ev;               // kTraceEvents per chunk
+    std::vector<int32_t> trace_call, trace_rows;     // per chunk: call number, query rows
 };
 HostPipe g_pipe[kMaxDev];
 std::mutex g_pipe_mu[kMaxDev];
@@ -60,6 +69,19 @@ bool make_pipe(HostPipe &p)
             return false;
     p.ready = true;
     return true;
+}
+
+void free_trace(HostPipe &p)
+{
+    for (cudaEvent_t e : p.trace_ev)
+        cudaEventDestroy(e);
+    if (p.trace_t0)
+        cudaEventDestroy(p.trace_t0);
+    p.trace_ev.clear();
+    p.trace_call.clear();
+    p.trace_rows.clear();
+    p.trace_t0 = nullptr;
+    p.trace_cap = p.trace_n = p.trace_calls = 0;
 }
 
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -184,9 +206,16 @@ extern "C" int dsa_prefill_host(const void *q8, const float *q_scale, const floa
             e = x;
     };
     // the workspace may still be in use by earlier work on the caller's stream
+    if (P.trace_cap > 0 && P.trace_calls == 0)
+        chk(cudaEventRecord(P.trace_t0, cs)); // before the copy streams are released
     chk(cudaEventRecord(P.start, cs));
     chk(cudaStreamWaitEvent(P.h2d, P.start, 0));
     chk(cudaStreamWaitEvent(P.d2h, P.start, 0));
+    // the chunk's timeline events while the record has room, else none
+    auto mark = [&](int j, int which, cudaStream_t st) {
+        if (j >= 0)
+            chk(cudaEventRecord(P.trace_ev[static_cast<size_t>(j) * kTraceEvents + which], st));
+    };
 
     int keys_in = 0; // key rows [0, keys_in) already on the device
     const std::vector<int> starts = chunk_starts(T, C);
@@ -198,9 +227,16 @@ extern "C" int dsa_prefill_host(const void *q8, const float *q_scale, const floa
         int kmax = 0;
         for (int r = r0; r < r0 + n; ++r)
             kmax = std::max(kmax, q_pos[r] + 1);
+        int tj = -1; // this chunk's slot in the timeline record
+        if (P.trace_n < P.trace_cap) {
+            tj = P.trace_n++;
+            P.trace_call[tj] = P.trace_calls;
+            P.trace_rows[tj] = n;
+        }
         // ---- inputs (the slot's previous chunk must be done with them)
         if (c >= kSlots)
             chk(cudaStreamWaitEvent(P.h2d, P.slot_done[s], 0));
+        mark(tj, kInBegin, P.h2d);
         if (kmax > keys_in) {
             const size_t a = keys_in, b = kmax;
             chk(cudaMemcpyAsync(ws + L.k8 + a * d_I, hk8 + a * d_I, (b - a) * d_I, cudaMemcpyHostToDevice, P.h2d));
@@ -216,11 +252,13 @@ extern "C" int dsa_prefill_host(const void *q8, const float *q_scale, const floa
         chk(cudaMemcpyAsync(ws + L.qpos[s], q_pos + r0, (size_t)n * 4, cudaMemcpyHostToDevice, P.h2d));
         chk(cudaMemcpyAsync(ws + L.q[s], hq + (size_t)r0 * H * 1152, (size_t)n * H * 1152, cudaMemcpyHostToDevice,
                             P.h2d));
+        mark(tj, kInEnd, P.h2d);
         chk(cudaEventRecord(P.in_ready[s], P.h2d));
         // ---- kernels (the slot's previous outputs must have been copied out)
         chk(cudaStreamWaitEvent(cs, P.in_ready[s], 0));
         if (c >= kSlots)
             chk(cudaStreamWaitEvent(cs, P.out_copied[s], 0));
+        mark(tj, kKernBegin, cs);
         if (e != cudaSuccess)
             break;
         const int32_t *qpos_d = reinterpret_cast<const int32_t *>(ws + L.qpos[s]);
@@ -239,14 +277,19 @@ extern "C" int dsa_prefill_host(const void *q8, const float *q_scale, const floa
                                         reinterpret_cast<float *>(ws + L.lse[s]), stream);
         if (rc != DSA_OK)
             break;
+        mark(tj, kKernEnd, cs);
         chk(cudaEventRecord(P.slot_done[s], cs));
         // ---- outputs
         chk(cudaStreamWaitEvent(P.d2h, P.slot_done[s], 0));
+        mark(tj, kOutBegin, P.d2h);
         chk(cudaMemcpyAsync(hout + (size_t)r0 * H * 1024, ws + L.out[s], (size_t)n * H * 1024,
                             cudaMemcpyDeviceToHost, P.d2h));
         chk(cudaMemcpyAsync(lse + (size_t)r0 * H, ws + L.lse[s], (size_t)n * H * 4, cudaMemcpyDeviceToHost, P.d2h));
+        mark(tj, kOutEnd, P.d2h);
         chk(cudaEventRecord(P.out_copied[s], P.d2h));
     }
+    if (P.trace_cap > 0)
+        ++P.trace_calls;
     // the call is complete on the caller's stream once every copy has landed
     chk(cudaEventRecord(P.end, P.d2h));
     chk(cudaEventRecord(P.start, P.h2d));
@@ -256,5 +299,59 @@ extern "C" int dsa_prefill_host(const void *q8, const float *q_scale, const floa
         return rc;
     if (e != cudaSuccess)
         return report_error(DSA_ERR_CUDA, "host prefill: %s", cudaGetErrorString(e));
+    return DSA_OK;
+}
+
+extern "C" int dsa_prefill_host_trace(int max_chunks)
+{
+    if (max_chunks < 0 || max_chunks > (1 << 20))
+        return report_error(DSA_ERR_INVALID_ARG, "max_chunks = %d outside [0, 2^20]", max_chunks);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev)
+        return report_error(DSA_ERR_CUDA, "no current device");
+    std::lock_guard<std::mutex> lk(g_pipe_mu[dev]);
+    HostPipe &P = g_pipe[dev];
+    free_trace(P);
+    if (max_chunks == 0)
+        return DSA_OK;
+    bool ok = cudaEventCreate(&P.trace_t0) == cudaSuccess;
+    P.trace_ev.assign(static_cast<size_t>(max_chunks) * kTraceEvents, nullptr);
+    for (size_t i = 0; ok && i < P.trace_ev.size(); ++i)
+        ok = cudaEventCreate(&P.trace_ev[i]) == cudaSuccess;
+    if (!ok) {
+        free_trace(P);
+        return report_error(DSA_ERR_CUDA, "creating the timeline events failed");
+    }
+    P.trace_call.assign(max_chunks, 0);
+    P.trace_rows.assign(max_chunks, 0);
+    P.trace_cap = max_chunks;
+    return DSA_OK;
+}
+
+extern "C" int dsa_prefill_host_trace_read(float *ms, int32_t *call, int32_t *rows, int max_chunks, int *n_out)
+{
+    if (!ms || !call || !rows || !n_out || max_chunks < 0)
+        return report_error(DSA_ERR_INVALID_ARG, "null pointer or max_chunks < 0");
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev)
+        return report_error(DSA_ERR_CUDA, "no current device");
+    std::lock_guard<std::mutex> lk(g_pipe_mu[dev]);
+    HostPipe &P = g_pipe[dev];
+    const int n = std::min(P.trace_n, max_chunks);
+    for (int j = 0; j < n; ++j) {
+        for (int ev = 0; ev < kTraceEvents; ++ev) {
+            cudaEvent_t x = P.trace_ev[static_cast<size_t>(j) * kTraceEvents + ev];
+            float t = 0.f;
+            // an event a failed call never recorded reads as NaN
+            if (cudaEventSynchronize(x) != cudaSuccess || cudaEventElapsedTime(&t, P.trace_t0, x) != cudaSuccess) {
+                cudaGetLastError();
+                t = std::numeric_limits<float>::quiet_NaN();
+            }
+            ms[static_cast<size_t>(j) * kTraceEvents + ev] = t;
+        }
+        call[j] = P.trace_call[j];
+        rows[j] = P.trace_rows[j];
+    }
+    *n_out = n;
     return DSA_OK;
 }

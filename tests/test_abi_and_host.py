@@ -120,6 +120,22 @@ def test_host_prefill_validation(lib):
     assert "q_pos[2]" in _err(lib)
 
 
+def test_host_prefill_timeline_validation(lib):
+    """The timeline calls' argument checks, taken before any CUDA call."""
+    import numpy as np
+
+    P = ctypes.c_void_p
+    assert lib.dsa_prefill_host_trace(-1) == 1
+    assert lib.dsa_prefill_host_trace((1 << 20) + 1) == 1
+    n = ctypes.c_int(0)
+    buf = np.zeros(6, dtype=np.float32)
+    ib = np.zeros(1, dtype=np.int32)
+    assert lib.dsa_prefill_host_trace_read(None, P(ib.ctypes.data), P(ib.ctypes.data), 1, ctypes.byref(n)) == 1
+    assert lib.dsa_prefill_host_trace_read(P(buf.ctypes.data), P(ib.ctypes.data), P(ib.ctypes.data), -1,
+                                           ctypes.byref(n)) == 1
+    assert lib.dsa_prefill_host_trace_read(P(buf.ctypes.data), P(ib.ctypes.data), P(ib.ctypes.data), 1, None) == 1
+
+
 def test_binding_raises_without_the_library(tmp_path):
     import sparse_attention_02_gb300 as dsa
 

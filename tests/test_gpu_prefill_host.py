@@ -79,3 +79,36 @@ def test_prefill_host_two_calls_back_to_back():
     for out, lse in outs:
         assert torch.equal(out.view(torch.int16), o_ref.view(torch.int16))
         assert torch.equal(lse, l_ref)
+
+
+def test_prefill_host_timeline():
+    """The per-chunk timeline of two calls: one entry per chunk in enqueue order, rows that
+    add up to the calls' rows, each chunk's input copies before its stages before its
+    output copies, the stages of successive chunks in stream order, and outputs unchanged
+    by the recording; a record of fewer chunks keeps the first ones."""
+    dsa = lib()
+    cfg = W.CONFIGS["tiny"]
+    x = W.prefill_inputs(cfg, DEV)
+    o_ref, l_ref = _device_path(dsa, x, slice(None), cfg)
+    dsa.dsa_prefill_host_trace(64)
+    try:
+        outs = [_host_path(dsa, x, slice(None), cfg, 64) for _ in range(2)]
+        t, call, rows = dsa.dsa_prefill_host_trace_read(64)
+    finally:
+        dsa.dsa_prefill_host_trace(0)
+    for o, l in outs:
+        assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16)) and torch.equal(l, l_ref)
+    # 256 rows in chunks of at most 64: 16, 32, 64, 64, 64, 16
+    per_call = [16, 32, 64, 64, 64, 16]
+    assert call.tolist() == [0] * 6 + [1] * 6 and rows.tolist() == per_call * 2
+    assert np.all(np.isfinite(t)) and np.all(t >= 0)
+    assert np.all(np.diff(t, axis=1) >= 0)               # in begin <= in end <= stages ... <= out end
+    assert np.all(t[1:, 2] >= t[:-1, 3])                 # stages of successive chunks in order
+    assert t[6, 0] >= t[5, 5]                            # the second call starts after the first ends
+    dsa.dsa_prefill_host_trace(3)
+    try:
+        _host_path(dsa, x, slice(None), cfg, 64)
+        t, call, rows = dsa.dsa_prefill_host_trace_read(64)
+    finally:
+        dsa.dsa_prefill_host_trace(0)
+    assert rows.tolist() == per_call[:3] and call.tolist() == [0, 0, 0]
