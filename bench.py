@@ -737,6 +737,89 @@ def e2e_bench(dsa, x, b, cfg, steps, dev, chunk_rows=2048):
             "chunk_rows": chunk_rows, "matches_device_path": same}
 
 
+def case_setup(dsa, name, dev):
+    """One entry point on a small input, for narrow profiler captures of its kernels: returns
+    (description, call).  Inputs are built once; the call does only the entry point's work."""
+    if name in ("indexer_4k", "topk_4k", "mla_4k", "warmup_4k"):
+        cfg = W.CONFIGS["prefill_4k"]
+        L = cfg.L
+        x = W.prefill_inputs(cfg, dev)
+        logits = torch.empty((L, L), dtype=torch.float32, device=dev)
+        vlen = x["q_pos"] + 1
+        idx = torch.empty((L, cfg.k), dtype=torch.int32, device=dev)
+        if name == "indexer_4k":
+            return (f"dsa_indexer_logits, L={L} causal, H_I={cfg.HI}, d_I={cfg.dI}",
+                    lambda: dsa.dsa_indexer_logits(x["q8"], x["qs"], x["w"], x["k8"], x["ks"], x["q_pos"], logits))
+        dsa.dsa_indexer_logits(x["q8"], x["qs"], x["w"], x["k8"], x["ks"], x["q_pos"], logits)
+        if name == "topk_4k":
+            return f"dsa_topk, {L} rows of the causal L={L} scores, k={cfg.k}", lambda: dsa.dsa_topk(logits, vlen, cfg.k, idx)
+        if name == "mla_4k":
+            dsa.dsa_topk(logits, vlen, cfg.k, idx)
+            out = torch.empty((L, cfg.H, cfg.Dv), dtype=torch.bfloat16, device=dev)
+            lse = torch.empty((L, cfg.H), dtype=torch.float32, device=dev)
+            return (f"dsa_sparse_mla_prefill, L={L}, k={cfg.k}, H={cfg.H}",
+                    lambda: dsa.dsa_sparse_mla_prefill(x["q"], x["kv"], idx, cfg.sm_scale, out, lse))
+        del logits
+        loss = torch.empty((L,), device=dev)
+        dw = torch.empty((L, cfg.HI), device=dev)
+        dq = torch.empty((L, cfg.HI, cfg.dI), device=dev)
+        dk = torch.empty((L, cfg.dI), device=dev)
+        ws = torch.empty(dsa.dsa_indexer_warmup_workspace_size(L, L, cfg.HI, cfg.dI), dtype=torch.uint8, device=dev)
+        return (f"dsa_indexer_warmup, L={L} causal, H={cfg.H}, H_I={cfg.HI}",
+                lambda: dsa.dsa_indexer_warmup(x["q"], x["kv"], cfg.sm_scale, x["q8"], x["qs"], x["w"], x["k8"],
+                                               x["ks"], x["q_pos"], loss, dw, dq, dk, workspace=ws))
+    if name == "fused_rows_32k":
+        cfg = W.CONFIGS["prefill_32k"]
+        rows = np.arange(cfg.L - 2048, cfg.L)
+        x = W.prefill_rows(cfg, dev, rows)
+        idx = torch.empty((len(rows), cfg.k), dtype=torch.int32, device=dev)
+        ws = torch.empty(dsa.dsa_indexer_topk_workspace_size(len(rows), cfg.L, cfg.HI, cfg.dI, cfg.k),
+                         dtype=torch.uint8, device=dev)
+        return (f"dsa_indexer_topk, query rows [{cfg.L - 2048}, {cfg.L}) over {cfg.L} keys, k={cfg.k}",
+                lambda: dsa.dsa_indexer_topk(x["q8"], x["qs"], x["w"], x["k8"], x["ks"], x["q_pos"], cfg.k, idx,
+                                             workspace=ws))
+    if name == "decode":
+        cfg = W.CONFIGS["decode_paged"]
+        d = W.decode_inputs(cfg, dev)
+        B = int(d["ctx"].shape[0])
+        logits = torch.empty((B, int(d["ctx"].max())), dtype=torch.float32, device=dev)
+        idx = torch.empty((B, cfg.k), dtype=torch.int32, device=dev)
+        out = torch.empty((B, cfg.H, 512), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((B, cfg.H), dtype=torch.float32, device=dev)
+        ws_n = dsa.dsa_sparse_mla_decode_workspace_size(B, cfg.H, cfg.k)
+        ws = torch.empty(ws_n, dtype=torch.uint8, device=dev) if ws_n else None
+
+        def step():
+            dsa.dsa_indexer_logits(d["q8"], d["qs"], d["w"], d["k8_pool"], d["ks_pool"], d["q_pos"], logits,
+                                   block_table=d["block_table"])
+            dsa.dsa_topk(logits, d["ctx"], cfg.k, idx)
+            dsa.dsa_sparse_mla_decode_paged(d["q"], d["kv_pool"], d["block_table"], d["ctx"], idx, cfg.sm_scale,
+                                            out, lse, workspace=ws)
+        return (f"decode step: B={B}, ctx U[{cfg.ctx_lo},{cfg.ctx_hi}], page {cfg.page_size}, k={cfg.k}", step)
+    raise ValueError(name)
+
+
+PROFILE_CASES = ("indexer_4k", "topk_4k", "mla_4k", "warmup_4k", "fused_rows_32k", "decode")
+
+
+def run_case(dsa, name, steps, warmup, dev):
+    """--case: `warmup` calls, then `steps` calls of one entry point between two events.  The
+    line is for locating launches in a profiler capture, not a measurement of the method."""
+    what, call = case_setup(dsa, name, dev)
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"case": name, "what": what, "warmup_calls": warmup, "calls": steps,
+                      "ms_per_call": e0.elapsed_time(e1) / max(steps, 1),
+                      "device_status": dsa.dsa_get_device_status()}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -748,8 +831,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-workloads", action="store_true", help="skip tiny, L=4096 and the chunked L=131072")
+    ap.add_argument("--case", choices=PROFILE_CASES,
+                    help="only run one entry point on a small input (--warmup then --steps calls), for profiling")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.case:
+        import sparse_attention_02_gb300 as dsa
+
+        dsa.load_library()
+        run_case(dsa, args.case, args.steps, args.warmup, torch.device("cuda", 0))
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
