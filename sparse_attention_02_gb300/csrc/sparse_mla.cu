@@ -20,21 +20,24 @@
 //   add the same two halves in the same way, so they hold bit-identical
 //   scores, run the same softmax (identical P, m and l) and each applies P to
 //   its own V quarter.  Stages of 36 KB leave room for four in flight; the last
-//   96 of this CTA's Q columns live in TMEM (the score MMA reads them as a TMEM
-//   A operand), the first 192 in shared memory.
+//   160 of this CTA's Q columns live in TMEM (the score MMA reads them as a TMEM
+//   A operand), the first 128 in shared memory.
 
 // The swap carries the raw fp32 partial scores (32 KB per 64-key block).  The
-// sender warps add the peer's partials to their own in fp32 and apply the log2
+// sender warps stage them in shared memory and the copy engine moves them
+// (cp.async.bulk into the peer's shared memory, 4 KB per warp and 32-key
+// plane): remote stores issued by the warps themselves moved a third of that
+// rate, the issue of 2048 16-byte stores per block competing with the gathers.
+// The sender warps add the peer's partials to their own in fp32 and apply the log2
 // softmax scale, (own + peer) * scale, written back over the block's S buffer:
 // the add commutes, so both CTAs hold bit-identical scores whose error is that
 // of the fp32 accumulation alone, a few fp32 ulps of |S| at any score
 // magnitude (a sharp, one-key softmax with scores of tens of nats included).
-// Partials rounded to fp16 would halve the swap, which bounds the rate (the
-// pair's link carries ~16 KB per 0.4 us), but put an error of ~|S| * 2^-11 on
-// every score and hence on LSE.
+// Partials rounded to fp16 would halve the swap, but put an error of
+// ~|S| * 2^-11 on every score and hence on LSE.
 //
-// Per 64-key block j (double-buffered S and P buffers, one swap buffer, four
-// KV stages):
+// Per 64-key block j (double-buffered S buffers, one P buffer, one swap buffer,
+// four KV stages):
 //   producer warps  four warps cp.async the 64 selected rows x 576 B into the
 //                   SW128 / SW64 K-major layouts (one 128-byte line per 8
 //                   lanes), zero-fill invalid entries, and arrive on the
@@ -50,12 +53,11 @@
 //                   per instruction whatever N is, so the N=64 score MMAs need
 //                   two issuing warps to keep the tensor pipe fed;
 //   sender warps    thread = head, one warp per TMEM lane quadrant: the
-//                   block's 64 partial scores from TMEM, st.async to the peer
-//                   in fp32 (completion counted in bytes on the peer's
-//                   mbarrier) as soon as the peer has read the previous
-//                   block's, so the swap of one block overlaps the softmax of
-//                   the previous one and the softmax warps never issue the
-//                   slow DSMEM stores themselves;
+//                   block's 64 partial scores from TMEM into shared memory,
+//                   then a bulk copy per 32-key plane to the peer (completion
+//                   counted in bytes on the peer's mbarrier) as soon as the
+//                   peer has read the previous block's, so the swap of one
+//                   block overlaps the softmax of the previous one;
 //   softmax warps   thread = head, two warps per TMEM lane quadrant, each with
 //                   32 of the block's keys: own partial from the S buffer
 //                   (then free for the next score MMAs once the senders have
@@ -82,14 +84,14 @@ constexpr int kDv = 512;
 constexpr int kBN = 64;                  // keys per block
 constexpr int kVAtoms = 4;               // 64-column atoms of this CTA's V quarter per stage
 constexpr int kQAtom = 128 * 128;        // bytes of one full Q atom (128 rows x 128 B, SW128)
-constexpr int kQSmemAtoms = 3;           // Q atoms in shared memory; the 4th and the RoPE half sit in TMEM
+constexpr int kQSmemAtoms = 2;           // Q atoms in shared memory; atoms 2, 3 and the RoPE half sit in TMEM
 constexpr int kKVAtom = kBN * 128;       // bytes of one KV atom (64 rows x 128 B, SW128)
 constexpr int kKVHalf = kBN * 64;        // bytes of the RoPE half atom (64 rows x 64 B, SW64)
 constexpr int kStage = kVAtoms * kKVAtom + kKVHalf; // 36 KB
 constexpr int kNStage = 4;
 constexpr int kPf = 3;                   // paged: blocks ahead whose latent rows the producers resolve
 constexpr int kXBuf = 128 * kBN * 4;     // one swap buffer: 128 heads x 64 fp32 partial scores
-constexpr int kNX = 1; // swap buffers (32 KB each): one beside four stages; a second with three stages measured no faster
+constexpr int kNX = 1; // swap buffers (32 KB each): one beside four stages; a second with three stages measured slower
 constexpr int kProdWarps = 4;
 constexpr int kPvWarp = kProdWarps;      // all PV MMAs (fixed accumulation order) + TMEM owner
 constexpr int kQkWarp0 = kProdWarps + 1; // score MMAs of even blocks; kQkWarp0 + 1: odd blocks
@@ -103,7 +105,8 @@ constexpr float kRescaleLog2 = 8.f;      // move the running max only when excee
 constexpr int OFF_Q = 0;                                  // 3 full atoms
 constexpr int OFF_KV = OFF_Q + kQSmemAtoms * kQAtom;     // 48 KB
 constexpr int OFF_X = OFF_KV + kNStage * kStage;         // 192 KB
-constexpr int OFF_BAR = OFF_X + kNX * kXBuf;             // 224 KB
+constexpr int OFF_STG = OFF_X + kNX * kXBuf;             // one 32-key plane of this CTA's partials, staged
+constexpr int OFF_BAR = OFF_STG + kXBuf / 2;             // 224 KB
 constexpr int NBAR = 40;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int kSmem = OFF_MISC + 64 + 1024;
@@ -111,7 +114,7 @@ static_assert(kSmem <= 232448, "dynamic shared memory above the 227 KB a CTA may
 
 // barrier slots
 // [J & 1] for S buffers, [J % kNX] for swap buffers, [J % kNP] for P buffers
-constexpr int kNP = 2; // P buffers in TMEM
+constexpr int kNP = 1; // P buffers in TMEM (one: its TMEM columns hold a Q atom instead)
 constexpr int B_KVF = 0, B_KVE = 4, B_SF = 8, B_SE = 10, B_XF = 12, B_XE = 14, B_PF = 16, B_PE = 18,
               B_ST = 20, // [J & 1]: the senders wrote the block's scaled total scores over its S buffer
               B_QF = 22, B_QE = 23, B_QA = 24, B_OF = 25, B_OE = 26, B_DONE = 27,
@@ -122,7 +125,7 @@ constexpr int B_KVF = 0, B_KVE = 4, B_SF = 8, B_SE = 10, B_XF = 12, B_XE = 14, B
 constexpr uint32_t TM_O = 0;
 constexpr uint32_t TM_S = 256;  // two buffers of 64 fp32 partial scores
 constexpr uint32_t TM_P = 384;  // kNP buffers of 32 (bf16 pairs)
-constexpr uint32_t TM_QT = 448; // Q: the 4th atom (32 columns of bf16 pairs) and the RoPE half (16)
+constexpr uint32_t TM_QT = 416; // Q: atoms 2 and 3 (32 columns of bf16 pairs each) and the RoPE half (16)
 constexpr uint32_t TM_RED = 496; // per-head values swapped between the two softmax warps of a quadrant
 constexpr uint32_t kTmemCols = 512;
 
@@ -242,6 +245,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
+
+// Copy engine: `bytes` of this CTA's shared memory into a peer's (both 16-byte
+// aligned, a multiple of 16 bytes), completion counted on the peer's mbarrier.
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes, uint32_t bar_cluster)
+{
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst_cluster),
+                 "r"(src_cta), "r"(bytes), "r"(bar_cluster)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 template <bool PAGED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -397,41 +412,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 __syncwarp();
             }
             if (nb > 0) {
-                // TMEM part of Q for heads 32 pw .. 32 pw + 31 (lane = head): the 4th
-                // atom of the V quarter (64 columns) and the RoPE half (32 columns),
-                // as bf16 pairs, the A-operand layout of a TMEM-sourced MMA
+                // TMEM part of Q for heads 32 pw .. 32 pw + 31 (lane = head): atoms 2 and 3
+                // of the V quarter (128 columns) and the RoPE half (32 columns), as bf16
+                // pairs, the A-operand layout of a TMEM-sourced MMA
                 const int h = 32 * pw + lane;
-                uint32_t qa[32], qr[16];
-                if (h < p.H) {
-                    const uint4 *src = reinterpret_cast<const uint4 *>(p.q + ((int64_t)t * p.H + h) * kD + 256 * rank + 192);
-                    const uint4 *srr = reinterpret_cast<const uint4 *>(p.q + ((int64_t)t * p.H + h) * kD + 512 + 32 * rank);
+                const uint32_t tq = tmem + (static_cast<uint32_t>(32 * pw) << 16) + TM_QT;
+                const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q + ((int64_t)t * p.H + (h < p.H ? h : 0)) * kD);
+#pragma unroll 1
+                for (int a = 0; a < 2; ++a) {
+                    uint32_t qa[32];
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
-                        const uint4 v = __ldg(src + c);
+                        const uint4 v = h < p.H ? __ldg(qrow + (256 * rank + 128 + 64 * a) / 8 + c) : make_uint4(0, 0, 0, 0);
                         qa[4 * c] = v.x;
                         qa[4 * c + 1] = v.y;
                         qa[4 * c + 2] = v.z;
                         qa[4 * c + 3] = v.w;
                     }
+                    tmem_st32(tq + 32 * a, qa);
+                    tmem_st_wait();
+                }
+                {
+                    uint32_t qr[16];
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        const uint4 v = __ldg(srr + c);
+                        const uint4 v = h < p.H ? __ldg(qrow + (512 + 32 * rank) / 8 + c) : make_uint4(0, 0, 0, 0);
                         qr[4 * c] = v.x;
                         qr[4 * c + 1] = v.y;
                         qr[4 * c + 2] = v.z;
                         qr[4 * c + 3] = v.w;
                     }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        qa[c] = 0u;
-#pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        qr[c] = 0u;
+                    tmem_st16(tq + 64, qr);
                 }
-                const uint32_t tq = tmem + (static_cast<uint32_t>(32 * pw) << 16) + TM_QT;
-                tmem_st32(tq, qa);
-                tmem_st16(tq + 32, qr);
                 tmem_st_wait();
                 tc_fence_before();
             }
@@ -602,16 +614,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bool ok = true;
         // This CTA's 288 score columns: its V quarter [256 r, 256 r + 256) (16
         // k-steps of 16 columns) and its half of the RoPE columns [512 + 32 r,
-        // +32) (2 k-steps).  A operand: k-steps 0..11 from the three Q atoms in
-        // shared memory, k-steps 12..17 from TMEM (the 4th atom, then the RoPE
+        // +32) (2 k-steps).  A operand: k-steps 0..7 from the two Q atoms in
+        // shared memory, k-steps 8..17 from TMEM (atoms 2 and 3, then the RoPE
         // half).  B operand: the stage's four SW128 atoms, then its SW64 RoPE
         // half atom.  Descriptors are precomputed: the issue loop is one add and
         // one tcgen05.mma per k-step.
-        uint64_t qd[12];
+        uint64_t qd[4 * kQSmemAtoms];
         uint32_t bofs[16]; // B offset of k-step s < 16 within a KV stage, 16-byte units
 #pragma unroll
         for (int s = 0; s < 16; ++s) {
-            if (s < 12)
+            if (s < 4 * kQSmemAtoms)
                 qd[s] = sdesc(sbase + OFF_Q + (s >> 2) * kQAtom + (s & 3) * 32, 16, 1024, 2);
             bofs[s] = static_cast<uint32_t>(((s >> 2) * kKVAtom + (s & 3) * 32) >> 4);
         }
@@ -643,15 +655,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint32_t d_tmem = tmem + TM_S + 64 * b;
                     umma_f16_ss(d_tmem, qd[0], sd + bofs[0], idesc_qk, 0u);
 #pragma unroll
-                    for (int s = 1; s < 12; ++s)
+                    for (int s = 1; s < 4 * kQSmemAtoms; ++s)
                         umma_f16_ss(d_tmem, qd[s], sd + bofs[s], idesc_qk, 1u);
 #pragma unroll
-                    for (int s = 12; s < 16; ++s)
-                        umma_f16_ts(d_tmem, tmem + TM_QT + 8 * (s - 12), sd + bofs[s], idesc_qk, 1u);
+                    for (int s = 4 * kQSmemAtoms; s < 16; ++s)
+                        umma_f16_ts(d_tmem, tmem + TM_QT + 8 * (s - 4 * kQSmemAtoms), sd + bofs[s], idesc_qk, 1u);
 #pragma unroll
                     for (int s = 16; s < 18; ++s)
-                        umma_f16_ts(d_tmem, tmem + TM_QT + 8 * (s - 12), sdh + static_cast<uint64_t>(2 * (s - 16)),
-                                    idesc_qk, 1u);
+                        umma_f16_ts(d_tmem, tmem + TM_QT + 8 * (s - 4 * kQSmemAtoms),
+                                    sdh + static_cast<uint64_t>(2 * (s - 16)), idesc_qk, 1u);
                     umma_commit(bar(B_SF + b));
                 }
                 __syncwarp();
@@ -669,22 +681,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp < kSoftWarp0) {
         // -------------------------------- score senders
         // Thread = head (TMEM lane), all 64 keys of each block.  This CTA's fp32
-        // partial scores go to the peer by st.async (completion counted in bytes
-        // on the peer's mbarrier); once the peer's partials have landed here,
-        // the same warp writes (own + peer) * scale over the block's S buffer
-        // (fp32: the add commutes, so both CTAs hold the same bits) and frees
-        // the swap buffer at once, so the next block's swap never waits for the
-        // softmax.  The row of head h in the swap buffer is 16 chunks of 16
-        // bytes, chunk c stored at c ^ (h & 7): eight consecutive heads reading
-        // the same chunk hit eight different banks.
+        // partial scores go to the peer one 32-key plane at a time: staged in
+        // shared memory, then a bulk copy of the warp's 32 head rows (completion
+        // counted in bytes on the peer's mbarrier); once the peer's partials
+        // have landed here, the same warp writes (own + peer) * scale over the
+        // block's S buffer (fp32: the add commutes, so both CTAs hold the same
+        // bits) and frees the swap buffer at once, so the next block's swap
+        // never waits for the softmax.  Swap buffer and staging hold [plane]
+        // [head][32 keys] rows of 128 bytes, chunk c of head h's row stored at
+        // c ^ (h & 7): eight consecutive heads reading the same chunk hit eight
+        // different banks.
         const int quad = warp & 3;
         const int h = quad * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t hsw = static_cast<uint32_t>(h & 7);
-        const uint32_t x_remote0 = mapa_shared(sbase + OFF_X + h * (kBN * 4), peer);
         const uint32_t xf_remote0 = mapa_shared(bar(B_XF), peer);
         const uint32_t xe_remote0 = mapa_shared(bar(B_XE), peer);
-        const uint8_t *xrow = smem + OFF_X + h * (kBN * 4);
+        // swap buffer: two planes of 32 keys, [plane][head][32 fp32], chunk c of a row at c ^ (h & 7)
+        const uint8_t *xrow = smem + OFF_X + h * 128;
+        uint8_t *stg_row = smem + OFF_STG + h * 128;
+        const uint32_t stg_q = sbase + OFF_STG + quad * 32 * 128;
+        const uint32_t x_remote_q = mapa_shared(sbase + OFF_X + quad * 32 * 128, peer);
         uint32_t J = 0;
         int u = 0;
         bool ok = true;
@@ -715,16 +732,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t xr = x_remote0 + xb * kXBuf, xfr = xf_remote0 + 8u * xb;
+                const uint32_t xfr = xf_remote0 + 8u * xb;
 #pragma unroll 1
-                for (int qq = 0; qq < 4; ++qq) {
-                    uint32_t r[16];
-                    tmem_ld16(s_cols + 16 * qq, r);
-                    tmem_ld_wait();
+                for (int pl = 0; pl < 2; ++pl) {
+                    // the staging rows are free once the previous copy has read them
+                    if (lane == 0)
+                        bulk_wait_read0();
+                    __syncwarp();
+#pragma unroll 1
+                    for (int qh = 0; qh < 2; ++qh) {
+                        uint32_t r[16];
+                        tmem_ld16(s_cols + 32 * pl + 16 * qh, r);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc)
-                        st_async_v4_b32(xr + ((static_cast<uint32_t>(4 * qq + cc) ^ hsw) << 4), r[4 * cc],
-                                        r[4 * cc + 1], r[4 * cc + 2], r[4 * cc + 3], xfr);
+                        for (int cc = 0; cc < 4; ++cc)
+                            *reinterpret_cast<uint4 *>(stg_row + ((static_cast<uint32_t>(4 * qh + cc) ^ hsw) << 4)) =
+                                make_uint4(r[4 * cc], r[4 * cc + 1], r[4 * cc + 2], r[4 * cc + 3]);
+                    }
+                    fence_proxy_async_smem(); // the copy engine reads what the generic stores wrote
+                    __syncwarp();
+                    if (lane == 0) {
+                        // this warp's 32 head rows of the plane (4 KB, contiguous in both buffers)
+                        bulk_s2cluster(x_remote_q + xb * kXBuf + pl * (kXBuf / 2), stg_q, 32 * 128, xfr);
+                        bulk_commit();
+                    }
                 }
                 if (!mbar_wait_warp<true>(bar(B_XF + xb), (J / kNX) & 1, abort_flag, p.status)) {
                     ok = false;
@@ -738,7 +769,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const uint4 pw = *reinterpret_cast<const uint4 *>(
-                            xrow + xb * kXBuf + ((static_cast<uint32_t>(4 * qq + c) ^ hsw) << 4));
+                            xrow + xb * kXBuf + (qq >> 1) * (kXBuf / 2) +
+                            ((static_cast<uint32_t>(4 * (qq & 1) + c) ^ hsw) << 4));
                         const uint32_t pws[4] = {pw.x, pw.y, pw.z, pw.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
@@ -756,6 +788,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        if (lane == 0)
+            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); // this warp's copies are complete
+        __syncwarp();
     } else {
         // ------------------------------------------------ softmax + epilogue
         // Warp half hf of a lane quadrant owns keys [32 hf, 32 hf + 32) of every
