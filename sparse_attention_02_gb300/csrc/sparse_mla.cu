@@ -25,14 +25,17 @@
 
 // The swap carries the raw fp32 partial scores (32 KB per 64-key block).  The
 // sender warps stage them in shared memory and the copy engine moves them
-// (cp.async.bulk into the peer's shared memory, 4 KB per warp and 32-key
-// plane): remote stores issued by the warps themselves moved a third of that
-// rate, the issue of 2048 16-byte stores per block competing with the gathers.
-// The sender warps add the peer's partials to their own in fp32 and apply the log2
-// softmax scale, (own + peer) * scale, written back over the block's S buffer:
-// the add commutes, so both CTAs hold bit-identical scores whose error is that
-// of the fp32 accumulation alone, a few fp32 ulps of |S| at any score
-// magnitude (a sharp, one-key softmax with scores of tens of nats included).
+// (cp.async.bulk into the peer's shared memory, 2 KB per warp and 16-key
+// quarter, two staging slots per warp so staging overlaps the copies, one
+// arrival barrier per quarter so the add starts with the first): remote stores
+// issued by the warps themselves moved a third of that rate, the issue of 2048
+// 16-byte stores per block competing with the gathers.
+// The softmax warps add the peer's partials to their own in fp32 and apply the
+// log2 softmax scale, (own + peer) * scale: the add commutes, so both CTAs hold
+// bit-identical scores whose error is that of the fp32 accumulation alone, a
+// few fp32 ulps of |S| at any score magnitude (a sharp, one-key softmax with
+// scores of tens of nats included).  With the add in the sender warps the
+// senders carried the whole swap and set the block rate.
 // Partials rounded to fp16 would halve the swap, but put an error of
 // ~|S| * 2^-11 on every score and hence on LSE.
 //
@@ -54,14 +57,15 @@
 //                   two issuing warps to keep the tensor pipe fed;
 //   sender warps    thread = head, one warp per TMEM lane quadrant: the
 //                   block's 64 partial scores from TMEM into shared memory,
-//                   then a bulk copy per 32-key plane to the peer (completion
-//                   counted in bytes on the peer's mbarrier) as soon as the
-//                   peer has read the previous block's, so the swap of one
-//                   block overlaps the softmax of the previous one;
+//                   then a bulk copy per 16-key quarter to the peer (completion
+//                   counted in bytes on the peer's per-quarter mbarrier) as
+//                   soon as the peer's softmax warps have read the previous
+//                   block's;
 //   softmax warps   thread = head, two warps per TMEM lane quadrant, each with
 //                   32 of the block's keys: own partial from the S buffer
 //                   (then free for the next score MMAs once the senders have
-//                   read it too), peer partial from the swap buffer, sum,
+//                   read it too), peer partial from the swap buffer as its two
+//                   quarters land (then free for the peer's next block), sum,
 //                   scale, mask, max (agreed with the sibling warp through a
 //                   spare TMEM column), exp2, running sum; P (bf16) into the
 //                   block's P buffer once its previous PV is done.  The
@@ -105,9 +109,9 @@ constexpr float kRescaleLog2 = 8.f;      // move the running max only when excee
 constexpr int OFF_Q = 0;                                  // 3 full atoms
 constexpr int OFF_KV = OFF_Q + kQSmemAtoms * kQAtom;     // 48 KB
 constexpr int OFF_X = OFF_KV + kNStage * kStage;         // 192 KB
-constexpr int OFF_STG = OFF_X + kNX * kXBuf;             // one 32-key plane of this CTA's partials, staged
+constexpr int OFF_STG = OFF_X + kNX * kXBuf;             // two 16-key quarters of this CTA's partials, staged
 constexpr int OFF_BAR = OFF_STG + kXBuf / 2;             // 224 KB
-constexpr int NBAR = 40;
+constexpr int NBAR = 44;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int kSmem = OFF_MISC + 64 + 1024;
 static_assert(kSmem <= 232448, "dynamic shared memory above the 227 KB a CTA may hold");
@@ -115,11 +119,11 @@ static_assert(kSmem <= 232448, "dynamic shared memory above the 227 KB a CTA may
 // barrier slots
 // [J & 1] for S buffers, [J % kNX] for swap buffers, [J % kNP] for P buffers
 constexpr int kNP = 1; // P buffers in TMEM (one: its TMEM columns hold a Q atom instead)
-constexpr int B_KVF = 0, B_KVE = 4, B_SF = 8, B_SE = 10, B_XF = 12, B_XE = 14, B_PF = 16, B_PE = 18,
-              B_ST = 20, // [J & 1]: the senders wrote the block's scaled total scores over its S buffer
+constexpr int B_KVF = 0, B_KVE = 4, B_SF = 8, B_SE = 10, B_XE = 14, B_PF = 16, B_PE = 18,
               B_QF = 22, B_QE = 23, B_QA = 24, B_OF = 25, B_OE = 26, B_DONE = 27,
               B_RB = 28,  // [quad][parity]: sibling softmax warps swapped their block max
-              B_RL = 36;  // [quad]: sibling softmax warps swapped their row sums
+              B_RL = 36,  // [quad]: sibling softmax warps swapped their row sums
+              B_XQ = 40;  // [q]: the peer's partials of keys [16 q, 16 q + 16) landed
 
 // TMEM columns
 constexpr uint32_t TM_O = 0;
@@ -256,7 +260,7 @@ __device__ __forceinline__ void bulk_s2cluster(uint32_t dst_cluster, uint32_t sr
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 
 template <bool PAGED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -285,16 +289,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_SF + i), 1);
-            mbar_init(bar(B_ST + i), kSendWarps);
-            mbar_init(bar(B_SE + i), kSoftWarps);
+            mbar_init(bar(B_SE + i), kSoftWarps + kSendWarps);
         }
         for (int i = 0; i < kNX; ++i) {
-            mbar_init(bar(B_XF + i), 1);
-            mbar_init(bar(B_XE + i), kSendWarps); // the peer's senders have added its contents
+            mbar_init(bar(B_XE + i), kSoftWarps); // the peer's softmax warps have read its contents
         }
         for (int i = 0; i < kNP; ++i) {
             mbar_init(bar(B_PF + i), kSoftWarps);
             mbar_init(bar(B_PE + i), 1);
+        }
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(bar(B_XQ + i), 1);
+            mbar_arrive_expect_tx(bar(B_XQ + i), kXBuf / 4); // armed for block 0
         }
         mbar_init(bar(B_QF), 1 + kProdWarps); // the Q TMA (expect_tx) + each producer's TMEM part
         mbar_init(bar(B_QE), 2);
@@ -681,27 +687,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp < kSoftWarp0) {
         // -------------------------------- score senders
         // Thread = head (TMEM lane), all 64 keys of each block.  This CTA's fp32
-        // partial scores go to the peer one 32-key plane at a time: staged in
-        // shared memory, then a bulk copy of the warp's 32 head rows (completion
-        // counted in bytes on the peer's mbarrier); once the peer's partials
-        // have landed here, the same warp writes (own + peer) * scale over the
-        // block's S buffer (fp32: the add commutes, so both CTAs hold the same
-        // bits) and frees the swap buffer at once, so the next block's swap
-        // never waits for the softmax.  Swap buffer and staging hold [plane]
-        // [head][32 keys] rows of 128 bytes, chunk c of head h's row stored at
-        // c ^ (h & 7): eight consecutive heads reading the same chunk hit eight
-        // different banks.
+        // partial scores go to the peer one 16-key quarter at a time: staged in
+        // shared memory (two slots per warp), then a bulk copy of the warp's 32
+        // head rows (completion counted in bytes on the peer's per-quarter
+        // mbarrier, which the peer's softmax warps wait on and re-arm).  The
+        // next block's copies wait until the peer's softmax warps have read this
+        // one's.  Per-warp handshakes per quarter measured slower (the waits
+        // inside the copy loop cost more than the coupling they remove).
         const int quad = warp & 3;
         const int h = quad * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t hsw = static_cast<uint32_t>(h & 7);
-        const uint32_t xf_remote0 = mapa_shared(bar(B_XF), peer);
         const uint32_t xe_remote0 = mapa_shared(bar(B_XE), peer);
-        // swap buffer: two planes of 32 keys, [plane][head][32 fp32], chunk c of a row at c ^ (h & 7)
-        const uint8_t *xrow = smem + OFF_X + h * 128;
-        uint8_t *stg_row = smem + OFF_STG + h * 128;
-        const uint32_t stg_q = sbase + OFF_STG + quad * 32 * 128;
-        const uint32_t x_remote_q = mapa_shared(sbase + OFF_X + quad * 32 * 128, peer);
+        // swap buffer: four quarters of 16 keys
+        // ([q][head][16 fp32], 64-byte rows, chunk c of head h's row at c ^ ((h >> 1) & 3): eight
+        // consecutive heads storing or reading the same chunk hit eight different banks; staging: two
+        // 2 KB slots per warp, one quarter of its 32 head rows each)
+        const uint32_t qsw = static_cast<uint32_t>((h >> 1) & 3);
+        uint8_t *stg_row = smem + OFF_STG + quad * 4096 + lane * 64;
+        const uint32_t stg_q = sbase + OFF_STG + quad * 4096;
+        const uint32_t x_remote_q = mapa_shared(sbase + OFF_X + quad * 32 * 64, peer);
+        const uint32_t xq_remote0 = mapa_shared(bar(B_XQ), peer);
         uint32_t J = 0;
         int u = 0;
         bool ok = true;
@@ -722,8 +727,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const uint32_t s_cols = tmem + lane_off + TM_S + 64 * b;
                 // arm this CTA's swap buffer for the peer's half of block J (its bytes may
                 // already be landing; this thread saw the buffer's phase of block J - kNX complete)
-                if (quad == 0 && lane == 0)
-                    mbar_arrive_expect_tx(bar(B_XF + xb), kXBuf);
                 // the peer's swap buffer must be free (its senders have added block J - kNX)
                 if (!mbar_wait_warp(bar(B_SF + b), (J >> 1) & 1, abort_flag, p.status) ||
                     (J >= kNX &&
@@ -732,60 +735,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t xfr = xf_remote0 + 8u * xb;
-#pragma unroll 1
-                for (int pl = 0; pl < 2; ++pl) {
-                    // the staging rows are free once the previous copy has read them
-                    if (lane == 0)
-                        bulk_wait_read0();
-                    __syncwarp();
-#pragma unroll 1
-                    for (int qh = 0; qh < 2; ++qh) {
-                        uint32_t r[16];
-                        tmem_ld16(s_cols + 32 * pl + 16 * qh, r);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int cc = 0; cc < 4; ++cc)
-                            *reinterpret_cast<uint4 *>(stg_row + ((static_cast<uint32_t>(4 * qh + cc) ^ hsw) << 4)) =
-                                make_uint4(r[4 * cc], r[4 * cc + 1], r[4 * cc + 2], r[4 * cc + 3]);
-                    }
-                    fence_proxy_async_smem(); // the copy engine reads what the generic stores wrote
-                    __syncwarp();
-                    if (lane == 0) {
-                        // this warp's 32 head rows of the plane (4 KB, contiguous in both buffers)
-                        bulk_s2cluster(x_remote_q + xb * kXBuf + pl * (kXBuf / 2), stg_q, 32 * 128, xfr);
-                        bulk_commit();
-                    }
-                }
-                if (!mbar_wait_warp<true>(bar(B_XF + xb), (J / kNX) & 1, abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
 #pragma unroll 1
                 for (int qq = 0; qq < 4; ++qq) {
+                    // slot qq & 1 is free once the copy issued two quarters ago has read it
+                    if (lane == 0)
+                        bulk_wait_read1();
+                    __syncwarp();
                     uint32_t r[16];
                     tmem_ld16(s_cols + 16 * qq, r);
                     tmem_ld_wait();
+                    uint8_t *srow = stg_row + (qq & 1) * 2048;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint4 pw = *reinterpret_cast<const uint4 *>(
-                            xrow + xb * kXBuf + (qq >> 1) * (kXBuf / 2) +
-                            ((static_cast<uint32_t>(4 * (qq & 1) + c) ^ hsw) << 4));
-                        const uint32_t pws[4] = {pw.x, pw.y, pw.z, pw.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            r[4 * c + e] = __float_as_uint((__uint_as_float(r[4 * c + e]) + __uint_as_float(pws[e])) *
-                                                           p.scale_log2);
+                    for (int cc = 0; cc < 4; ++cc)
+                        *reinterpret_cast<uint4 *>(srow + ((static_cast<uint32_t>(cc) ^ qsw) << 4)) =
+                            make_uint4(r[4 * cc], r[4 * cc + 1], r[4 * cc + 2], r[4 * cc + 3]);
+                    fence_proxy_async_smem(); // the copy engine reads what the generic stores wrote
+                    __syncwarp();
+                    if (lane == 0) {
+                        // this warp's 32 head rows of the quarter (2 KB, contiguous in both buffers)
+                        bulk_s2cluster(x_remote_q + qq * (kXBuf / 4), stg_q + (qq & 1) * 2048, 32 * 64,
+                                       xq_remote0 + 8u * qq);
+                        bulk_commit();
                     }
-                    tmem_st16(s_cols + 16 * qq, r);
                 }
-                tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(bar(B_ST + b));                      // totals of block J ready
-                    mbar_arrive_remote_relaxed(xe_remote0 + 8u * xb); // this CTA's swap buffer is free again
-                }
+                if (lane == 0)
+                    mbar_arrive(bar(B_SE + b)); // this warp has read the block's partials
             }
         }
         if (lane == 0)
@@ -802,6 +778,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int h = quad * 32 + lane;                  // head = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t red = tmem + lane_off + TM_RED;
+        const uint8_t *xq_row = smem + OFF_X + h * 64;
+        const uint32_t xqsw = static_cast<uint32_t>((h >> 1) & 3);
+        const uint32_t xe_remote_sm = mapa_shared(bar(B_XE), peer);
         uint32_t J = 0;
         int u = 0, v = 0;
         bool ok = true;
@@ -856,7 +835,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 // 1. the block's scaled total scores of this warp's 32 keys, written over the S
                 //    buffer by the senders; then the buffer is free for block J + 2
                 const int pb = J % kNP;
-                if (!mbar_wait_warp(bar(B_ST + b), (J >> 1) & 1, abort_flag, p.status)) {
+                if (!mbar_wait_warp(bar(B_SF + b), (J >> 1) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
@@ -874,6 +853,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(bar(B_SE + b));
+                // the peer's partials of this warp's two quarters: (own + peer) * scale in fp32
+                // (the add commutes: both CTAs hold the same bits)
+                if (!mbar_wait_warp<true>(bar(B_XQ + 2 * hf), J & 1, abort_flag, p.status) ||
+                    !mbar_wait_warp<true>(bar(B_XQ + 2 * hf + 1), J & 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int qh = 0; qh < 2; ++qh) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const float4 pv = *reinterpret_cast<const float4 *>(
+                            xq_row + (2 * hf + qh) * (kXBuf / 4) + ((static_cast<uint32_t>(c) ^ xqsw) << 4));
+                        const int e0 = 16 * qh + 4 * c;
+                        sc[e0] = (sc[e0] + pv.x) * p.scale_log2;
+                        sc[e0 + 1] = (sc[e0 + 1] + pv.y) * p.scale_log2;
+                        sc[e0 + 2] = (sc[e0 + 2] + pv.z) * p.scale_log2;
+                        sc[e0 + 3] = (sc[e0 + 3] + pv.w) * p.scale_log2;
+                    }
+                }
+                __syncwarp(); // every lane has read its rows of the two quarters
+                if (lane == 0) {
+                    if (quad == 0) // both quarters' phases of block J are complete: arm them for block J + 1
+                        for (int q = 2 * hf; q < 2 * hf + 2; ++q)
+                            mbar_arrive_expect_tx(bar(B_XQ + q), kXBuf / 4);
+                    mbar_arrive_remote_relaxed(xe_remote_sm); // the peer may send its next partials
+                }
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
