@@ -19,7 +19,7 @@
 //   partial-score tiles through distributed shared memory.  Both CTAs then
 //   add the same two halves in the same way, so they hold bit-identical
 //   scores, run the same softmax (identical P, m and l) and each applies P to
-//   its own V quarter.  Stages of 36 KB leave room for four in flight; the last
+//   its own V quarter.  Stages are 36 KB (three or four in flight); the last
 //   160 of this CTA's Q columns live in TMEM (the score MMA reads them as a TMEM
 //   A operand), the first 128 in shared memory.
 
@@ -39,8 +39,8 @@
 // Partials rounded to fp16 would halve the swap, but put an error of
 // ~|S| * 2^-11 on every score and hence on LSE.
 //
-// Per 64-key block j (double-buffered S buffers, one P buffer, one swap buffer,
-// four KV stages):
+// Per 64-key block j (double-buffered S buffers, one P buffer; prefill: two
+// swap buffers and three KV stages, decode: one and four):
 //   producer warps  four warps cp.async the 64 selected rows x 576 B into the
 //                   SW128 / SW64 K-major layouts (one 128-byte line per 8
 //                   lanes), zero-fill invalid entries, and arrive on the
@@ -92,10 +92,8 @@ constexpr int kQSmemAtoms = 2;           // Q atoms in shared memory; atoms 2, 3
 constexpr int kKVAtom = kBN * 128;       // bytes of one KV atom (64 rows x 128 B, SW128)
 constexpr int kKVHalf = kBN * 64;        // bytes of the RoPE half atom (64 rows x 64 B, SW64)
 constexpr int kStage = kVAtoms * kKVAtom + kKVHalf; // 36 KB
-constexpr int kNStage = 4;
 constexpr int kPf = 3;                   // paged: blocks ahead whose latent rows the producers resolve
 constexpr int kXBuf = 128 * kBN * 4;     // one swap buffer: 128 heads x 64 fp32 partial scores
-constexpr int kNX = 1; // swap buffers (32 KB each): one beside four stages; a second with three stages measured slower
 constexpr int kProdWarps = 4;
 constexpr int kPvWarp = kProdWarps;      // all PV MMAs (fixed accumulation order) + TMEM owner
 constexpr int kQkWarp0 = kProdWarps + 1; // score MMAs of even blocks; kQkWarp0 + 1: odd blocks
@@ -106,15 +104,25 @@ constexpr int kSoftWarps = 8;            // two per TMEM lane quadrant, 32 keys 
 constexpr int kThreads = 32 * (kSoftWarp0 + kSoftWarps);
 constexpr float kRescaleLog2 = 8.f;      // move the running max only when exceeded by this
 
-constexpr int OFF_Q = 0;                                  // 3 full atoms
-constexpr int OFF_KV = OFF_Q + kQSmemAtoms * kQAtom;     // 48 KB
-constexpr int OFF_X = OFF_KV + kNStage * kStage;         // 192 KB
-constexpr int OFF_STG = OFF_X + kNX * kXBuf;             // two 16-key quarters of this CTA's partials, staged
-constexpr int OFF_BAR = OFF_STG + kXBuf / 2;             // 224 KB
-constexpr int NBAR = 44;
-constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-constexpr int kSmem = OFF_MISC + 64 + 1024;
-static_assert(kSmem <= 232448, "dynamic shared memory above the 227 KB a CTA may hold");
+constexpr int NBAR = 48;
+
+// Shared-memory layout.  Prefill: three KV stages and two swap buffers (the
+// peer's next block may land while this one's is read: 23.0 ms against 23.5 ms
+// with four stages and one buffer at L = 32768).  Decode: four stages and one
+// swap buffer (its rows come from HBM, so the deeper gather ring matters more:
+// 78 us against 85 us at B = 64).
+template <bool PAGED> struct Layout {
+    static constexpr int kNStage = PAGED ? 4 : 3;
+    static constexpr int kNX = PAGED ? 1 : 2;                // swap buffers, 32 KB each
+    static constexpr int OFF_Q = 0;                          // two full Q atoms
+    static constexpr int OFF_KV = OFF_Q + kQSmemAtoms * kQAtom;
+    static constexpr int OFF_X = OFF_KV + kNStage * kStage;
+    static constexpr int OFF_STG = OFF_X + kNX * kXBuf;      // two 16-key quarters of this CTA's partials, staged
+    static constexpr int OFF_BAR = OFF_STG + kXBuf / 2;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int kSmem = OFF_MISC + 64 + 1024;
+    static_assert(kSmem <= 232448, "dynamic shared memory above the 227 KB a CTA may hold");
+};
 
 // barrier slots
 // [J & 1] for S buffers, [J % kNX] for swap buffers, [J % kNP] for P buffers
@@ -123,7 +131,7 @@ constexpr int B_KVF = 0, B_KVE = 4, B_SF = 8, B_SE = 10, B_XE = 14, B_PF = 16, B
               B_QF = 22, B_QE = 23, B_QA = 24, B_OF = 25, B_OE = 26, B_DONE = 27,
               B_RB = 28,  // [quad][parity]: sibling softmax warps swapped their block max
               B_RL = 36,  // [quad]: sibling softmax warps swapped their row sums
-              B_XQ = 40;  // [q]: the peer's partials of keys [16 q, 16 q + 16) landed
+              B_XQ = 40;  // [xb][q]: the peer's partials of keys [16 q, 16 q + 16) landed in swap buffer xb
 
 // TMEM columns
 constexpr uint32_t TM_O = 0;
@@ -266,6 +274,10 @@ template <bool PAGED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_q, Params p)
 {
+    using Lay = Layout<PAGED>;
+    constexpr int kNStage = Lay::kNStage, kNX = Lay::kNX;
+    constexpr int OFF_Q = Lay::OFF_Q, OFF_KV = Lay::OFF_KV, OFF_X = Lay::OFF_X, OFF_STG = Lay::OFF_STG,
+                  OFF_BAR = Lay::OFF_BAR, OFF_MISC = Lay::OFF_MISC;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -298,9 +310,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(bar(B_PF + i), kSoftWarps);
             mbar_init(bar(B_PE + i), 1);
         }
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 4 * kNX; ++i) {
             mbar_init(bar(B_XQ + i), 1);
-            mbar_arrive_expect_tx(bar(B_XQ + i), kXBuf / 4); // armed for block 0
+            mbar_arrive_expect_tx(bar(B_XQ + i), kXBuf / 4); // armed for blocks 0 .. kNX - 1
         }
         mbar_init(bar(B_QF), 1 + kProdWarps); // the Q TMA (expect_tx) + each producer's TMEM part
         mbar_init(bar(B_QE), 2);
@@ -725,9 +737,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const int b = J & 1;
                 const int xb = J % kNX;
                 const uint32_t s_cols = tmem + lane_off + TM_S + 64 * b;
-                // arm this CTA's swap buffer for the peer's half of block J (its bytes may
-                // already be landing; this thread saw the buffer's phase of block J - kNX complete)
-                // the peer's swap buffer must be free (its senders have added block J - kNX)
+                // the peer's swap buffer xb must be free (its softmax warps have read block J - kNX)
                 if (!mbar_wait_warp(bar(B_SF + b), (J >> 1) & 1, abort_flag, p.status) ||
                     (J >= kNX &&
                      !mbar_wait_warp<true>(bar(B_XE + xb), ((J / kNX) - 1) & 1, abort_flag, p.status))) {
@@ -753,8 +763,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) {
                         // this warp's 32 head rows of the quarter (2 KB, contiguous in both buffers)
-                        bulk_s2cluster(x_remote_q + qq * (kXBuf / 4), stg_q + (qq & 1) * 2048, 32 * 64,
-                                       xq_remote0 + 8u * qq);
+                        bulk_s2cluster(x_remote_q + xb * kXBuf + qq * (kXBuf / 4), stg_q + (qq & 1) * 2048, 32 * 64,
+                                       xq_remote0 + 8u * (4 * xb + qq));
                         bulk_commit();
                     }
                 }
@@ -855,8 +865,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     mbar_arrive(bar(B_SE + b));
                 // the peer's partials of this warp's two quarters: (own + peer) * scale in fp32
                 // (the add commutes: both CTAs hold the same bits)
-                if (!mbar_wait_warp<true>(bar(B_XQ + 2 * hf), J & 1, abort_flag, p.status) ||
-                    !mbar_wait_warp<true>(bar(B_XQ + 2 * hf + 1), J & 1, abort_flag, p.status)) {
+                const int xb = J % kNX;
+                if (!mbar_wait_warp<true>(bar(B_XQ + 4 * xb + 2 * hf), (J / kNX) & 1, abort_flag, p.status) ||
+                    !mbar_wait_warp<true>(bar(B_XQ + 4 * xb + 2 * hf + 1), (J / kNX) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
@@ -865,7 +876,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const float4 pv = *reinterpret_cast<const float4 *>(
-                            xq_row + (2 * hf + qh) * (kXBuf / 4) + ((static_cast<uint32_t>(c) ^ xqsw) << 4));
+                            xq_row + xb * kXBuf + (2 * hf + qh) * (kXBuf / 4) + ((static_cast<uint32_t>(c) ^ xqsw) << 4));
                         const int e0 = 16 * qh + 4 * c;
                         sc[e0] = (sc[e0] + pv.x) * p.scale_log2;
                         sc[e0 + 1] = (sc[e0 + 1] + pv.y) * p.scale_log2;
@@ -875,10 +886,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp(); // every lane has read its rows of the two quarters
                 if (lane == 0) {
-                    if (quad == 0) // both quarters' phases of block J are complete: arm them for block J + 1
+                    if (quad == 0) // both quarters' phases of block J are complete: arm them for block J + kNX
                         for (int q = 2 * hf; q < 2 * hf + 2; ++q)
-                            mbar_arrive_expect_tx(bar(B_XQ + q), kXBuf / 4);
-                    mbar_arrive_remote_relaxed(xe_remote_sm); // the peer may send its next partials
+                            mbar_arrive_expect_tx(bar(B_XQ + 4 * xb + q), kXBuf / 4);
+                    mbar_arrive_remote_relaxed(xe_remote_sm + 8u * xb); // the peer may send into buffer xb again
                 }
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -1148,6 +1159,7 @@ template <bool PAGED>
 int launch(const MlaArgs &a, cudaStream_t stream, char *err, size_t errlen)
 {
     static std::atomic<bool> attr_set[64];
+    constexpr int kSmem = Layout<PAGED>::kSmem;
     if (cudaError_t e_attr = raise_smem_limit_once(sparse_mla_kernel<PAGED>, kSmem, attr_set);
         e_attr != cudaSuccess) {
         snprintf(err, errlen, "cudaFuncSetAttribute(sparse_mla): %s", cudaGetErrorString(e_attr));
