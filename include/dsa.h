@@ -338,11 +338,14 @@ int dsa_sparse_mla_decode_paged(const void *q, const void *kv_pool, int num_page
  *         256-byte aligned, owned by the caller.
  *
  * Query rows go in chunks of at most chunk_rows (C): C/4 and C/2 rows first,
- * so the kernels start after a short copy, then C, and a last chunk of C/4,
- * so little is left to copy out after the last kernels.  The inputs of a chunk
+ * then C, and a last chunk of C/4, processed from the last chunk to the first
+ * (short chunks at both ends: the kernels start after a short copy and little
+ * is left to copy out after the last kernels; the first chunk processed brings
+ * in the keys of every row, and the long rows' chunks, whose kernels outlast
+ * their copies, come first).  The inputs of a chunk
  * are copied in on a copy stream, its kernels run on `stream`, its outputs are copied out on
- * a second copy stream, and two buffer slots let the copies of neighbouring
- * chunks overlap the kernels.  The keys stay on the device for the call and are
+ * a second copy stream, and four buffer slots let the copies run up to three
+ * chunks ahead of the kernels.  The keys stay on the device for the call and are
  * copied in as far as each chunk's positions need them.  Host buffers should be
  * page-locked (cudaHostAlloc or cudaHostRegister) for the copies to overlap;
  * pageable memory gives the same results more slowly.  The call returns once

@@ -98,8 +98,8 @@ def test_prefill_host_timeline():
         dsa.dsa_prefill_host_trace(0)
     for o, l in outs:
         assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16)) and torch.equal(l, l_ref)
-    # 256 rows in chunks of at most 64: 16, 32, 64, 64, 64, 16
-    per_call = [16, 32, 64, 64, 64, 16]
+    # 256 rows in chunks of at most 64 (16, 32, 64, 64, 64, 16), processed last rows first
+    per_call = [16, 64, 64, 64, 32, 16]
     assert call.tolist() == [0] * 6 + [1] * 6 and rows.tolist() == per_call * 2
     assert np.all(np.isfinite(t)) and np.all(t >= 0)
     assert np.all(np.diff(t, axis=1) >= 0)               # in begin <= in end <= stages ... <= out end
