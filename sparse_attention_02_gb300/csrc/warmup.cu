@@ -332,9 +332,13 @@ __device__ __forceinline__ float e4m3_to_float(uint32_t c)
 // ---------------------------------------------------------- backward: rows
 // One CTA of 256 threads per query row t.  Per 64-key tile: the tile's
 // dequantised keys kd[64][128] and g; a[j][s] for the 64 heads x 64 keys
-// (thread: 4 heads x 4 keys, float4 loads along d); dw partials; c = g w [a>0]
-// into shared memory and to the global c[t][j][s]; then dq[j][d] += sum_s
-// c[j][s] kd[s][d] (thread: 4 heads x 8 columns).
+// (thread: 4 heads x keys sg, sg + 16, sg + 32, sg + 48, float4 loads along d);
+// dw partials; c = g w [a>0] into shared memory and to the global c[t][j][s];
+// then dq[j][d] += sum_s c[j][s] kd[s][d] (thread: 4 heads x columns
+// 4 dd .. +4 and 64 + 4 dd .. +4).  Neighbouring threads read neighbouring key
+// rows and neighbouring column groups: with keys 4 rows apart (4 x 132 floats
+// = 16 banks) sixteen threads' rows fell on two bank groups, and 8-column
+// groups on four, and the kernel ran at the shared-memory pipe's limit.
 constexpr int kBTile = 64;
 constexpr int kBD = 128;
 constexpr int kBKdPitch = kBD + 4;   // floats per key row in shared memory (16-byte aligned, banks spread)
@@ -366,9 +370,9 @@ __global__ void __launch_bounds__(256)
         qd[i] = e4m3_to_float(q8[(int64_t)t * HI * kBD + i]) * qs;
     for (int i = threadIdx.x; i < HI; i += 256)
         dws[i] = 0.f;
-    // a phase: thread (jg, sg) = heads jg * JT .. +JT, keys sg * 4 .. +4
+    // a phase: thread (jg, sg) = heads jg * JT .. +JT, keys sg + 16 e (e < 4)
     const int jg = threadIdx.x >> 4, sg = threadIdx.x & 15;
-    // dq phase: thread (jd, dd) = heads jd * JD .. +JD, columns dd * 8 .. +8
+    // dq phase: thread (jd, dd) = heads jd * JD .. +JD, columns 4 dd .. +4 and 64 + 4 dd .. +4
     constexpr int JD = HI / 16;
     const int jd = threadIdx.x >> 4, dd = threadIdx.x & 15;
     float acc_dq[JD][8];
@@ -411,7 +415,7 @@ __global__ void __launch_bounds__(256)
                 qv[i] = *reinterpret_cast<const float4 *>(qd + (jg * JT + i) * kBD + d);
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-                kv[e] = *reinterpret_cast<const float4 *>(kd + (sg * 4 + e) * kBKdPitch + d);
+                kv[e] = *reinterpret_cast<const float4 *>(kd + (sg + 16 * e) * kBKdPitch + d);
 #pragma unroll
             for (int i = 0; i < JT; ++i)
 #pragma unroll
@@ -422,27 +426,23 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
         for (int i = 0; i < JT; ++i) {
             const int j = jg * JT + i;
-            float4 cv;
-            float *cp = reinterpret_cast<float *>(&cv);
+            float *crow = cbuf + ((int64_t)t * HI + j) * ldc + s0;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float ge = gt[sg * 4 + e];
+                const int sl = sg + 16 * e;
+                const float ge = gt[sl];
                 acc_dw[i] += a[i][e] > 0.f ? ge * a[i][e] : 0.f;
-                cp[e] = a[i][e] > 0.f ? ge * wj[i] : 0.f;
+                const float c = a[i][e] > 0.f ? ge * wj[i] : 0.f;
+                cs[j * kBCPitch + sl] = c;
+                if (s0 + sl < S)
+                    crow[sl] = c; // sixteen threads: 64 contiguous bytes
             }
-            *reinterpret_cast<float4 *>(cs + j * kBCPitch + sg * 4) = cv;
-            if (s0 + sg * 4 + 3 < S) // ldc is a multiple of 4: 16-byte aligned
-                *reinterpret_cast<float4 *>(cbuf + ((int64_t)t * HI + j) * ldc + s0 + sg * 4) = cv;
-            else
-                for (int e = 0; e < 4; ++e)
-                    if (s0 + sg * 4 + e < S)
-                        cbuf[((int64_t)t * HI + j) * ldc + s0 + sg * 4 + e] = cp[e];
         }
         __syncthreads();
 #pragma unroll 4
         for (int s = 0; s < kBTile; ++s) {
-            const float4 k0 = *reinterpret_cast<const float4 *>(kd + s * kBKdPitch + dd * 8);
-            const float4 k1 = *reinterpret_cast<const float4 *>(kd + s * kBKdPitch + dd * 8 + 4);
+            const float4 k0 = *reinterpret_cast<const float4 *>(kd + s * kBKdPitch + dd * 4);
+            const float4 k1 = *reinterpret_cast<const float4 *>(kd + s * kBKdPitch + 64 + dd * 4);
 #pragma unroll
             for (int i = 0; i < JD; ++i) {
                 const float c = cs[(jd * JD + i) * kBCPitch + s];
@@ -466,9 +466,9 @@ __global__ void __launch_bounds__(256)
         dw[(int64_t)t * HI + i] = dws[i];
 #pragma unroll
     for (int i = 0; i < JD; ++i) {
-        float *dst = dq + ((int64_t)t * HI + jd * JD + i) * kBD + dd * 8;
+        float *dst = dq + ((int64_t)t * HI + jd * JD + i) * kBD + dd * 4;
         *reinterpret_cast<float4 *>(dst) = make_float4(acc_dq[i][0], acc_dq[i][1], acc_dq[i][2], acc_dq[i][3]);
-        *reinterpret_cast<float4 *>(dst + 4) = make_float4(acc_dq[i][4], acc_dq[i][5], acc_dq[i][6], acc_dq[i][7]);
+        *reinterpret_cast<float4 *>(dst + 64) = make_float4(acc_dq[i][4], acc_dq[i][5], acc_dq[i][6], acc_dq[i][7]);
     }
 }
 
@@ -481,8 +481,9 @@ size_t bwd_rows_smem()
 // ---------------------------------------------------------- backward: keys
 // One CTA of 256 threads per (64-key tile kt, chunk of 256 query rows): for
 // each row t of the chunk that sees the tile, dk[s][d] += sum_j c[t][j][s]
-// q[t][j][d] (thread: 4 keys x 8 columns); the partial sums are added to dk
-// with atomics.
+// q[t][j][d] (thread: 4 keys x columns 4 dd .. +4 and 64 + 4 dd .. +4, so the
+// sixteen column groups of a row are 256 contiguous bytes); the partial sums
+// are added to dk with atomics.
 constexpr int kBRowChunk = 256;
 
 template <int HI>
@@ -499,7 +500,7 @@ __global__ void __launch_bounds__(256)
     const int s0 = blockIdx.x * kBTile;
     const int t0 = blockIdx.y * kBRowChunk;
     const int t1 = t0 + kBRowChunk < T ? t0 + kBRowChunk : T;
-    const int sg = threadIdx.x >> 4, dd = threadIdx.x & 15; // keys sg * 4 .. +4, columns dd * 8 .. +8
+    const int sg = threadIdx.x >> 4, dd = threadIdx.x & 15; // keys sg * 4 .. +4, columns 4 dd .. +4, 64 + 4 dd .. +4
     float acc[4][8];
 #pragma unroll
     for (int e = 0; e < 4; ++e)
@@ -525,8 +526,8 @@ __global__ void __launch_bounds__(256)
         __syncthreads();
 #pragma unroll 2
         for (int j = 0; j < HI; ++j) {
-            const float4 q0 = *reinterpret_cast<const float4 *>(qd + j * kBD + dd * 8);
-            const float4 q1 = *reinterpret_cast<const float4 *>(qd + j * kBD + dd * 8 + 4);
+            const float4 q0 = *reinterpret_cast<const float4 *>(qd + j * kBD + dd * 4);
+            const float4 q1 = *reinterpret_cast<const float4 *>(qd + j * kBD + 64 + dd * 4);
             const float4 cv = *reinterpret_cast<const float4 *>(ct + j * kBCPitch + sg * 4);
             const float cc[4] = {cv.x, cv.y, cv.z, cv.w};
 #pragma unroll
@@ -550,7 +551,7 @@ __global__ void __launch_bounds__(256)
         if (s < S)
 #pragma unroll
             for (int c = 0; c < 8; ++c)
-                atomicAdd(dk + (int64_t)s * kBD + dd * 8 + c, acc[e][c]);
+                atomicAdd(dk + (int64_t)s * kBD + (c < 4 ? dd * 4 + c : 64 + dd * 4 + c - 4), acc[e][c]);
     }
 }
 
