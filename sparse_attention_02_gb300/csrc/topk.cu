@@ -473,17 +473,22 @@ __device__ uint32_t select_tau(const uint32_t *ck, int nc, int k, int *hist, int
             }
             const int excl = incl - sum;
             const unsigned m = __ballot_sync(0xffffffffu, excl < k_rem && incl >= k_rem);
-            if (lane == (m ? __ffs(m) - 1 : 0)) {
-                int above = excl;
-                for (int j = 31; j >= 0; --j) {
-                    const int c = cur[32 * lane + j];
-                    if (above + c >= k_rem) {
-                        sel[0] = 32 * lane + j;
-                        sel[1] = above;
-                        break;
-                    }
-                    above += c;
-                }
+            // within the chosen lane's 32 bins, highest first: lane i takes bin
+            // 32 L + 31 - i, a prefix count over the lanes finds the bin
+            const int L = m ? __ffs(m) - 1 : 0;
+            const int above_L = __shfl_sync(0xffffffffu, excl, L);
+            const int c = cur[32 * L + 31 - lane];
+            int pre = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, pre, o);
+                if (lane >= o)
+                    pre += y;
+            }
+            const unsigned m2 = __ballot_sync(0xffffffffu, above_L + pre >= k_rem);
+            if (m2 && lane == __ffs(m2) - 1) {
+                sel[0] = 32 * L + 31 - lane;
+                sel[1] = above_L + pre - c;
             }
         } else {
             for (int q = threadIdx.x - 32; q < 1024; q += NT - 32)
