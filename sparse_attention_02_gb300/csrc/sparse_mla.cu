@@ -842,8 +842,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int n0 = (un.jb + j + 1) * kBN + 32 * hf + lane;
                     raw = n0 < p.k ? idx_row[n0] : -1;
                 }
-                // 1. the block's scaled total scores of this warp's 32 keys, written over the S
-                //    buffer by the senders; then the buffer is free for block J + 2
+                // 1. this CTA's partial scores of the warp's 32 keys from the S buffer (free for
+                //    block J + 2 once the senders have read it too)
                 const int pb = J % kNP;
                 if (!mbar_wait_warp(bar(B_SF + b), (J >> 1) & 1, abort_flag, p.status)) {
                     ok = false;
