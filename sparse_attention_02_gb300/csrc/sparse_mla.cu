@@ -367,24 +367,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int32_t *idx_row = p.idx + (int64_t)t * p.k;
             const int ctx = PAGED ? p.ctx_len[t] : 0;
             // the unit's blocks up to its last in-range entry.  Paged (decode: the
-            // scan sits before the unit's first gather, nothing hides it): 16-byte
-            // loads, a unit holds at most 64 blocks = 4096 entries = 32 loads per
-            // lane; prefill overlaps the scan with the previous token's blocks
+            // scan sits before the unit's first gather, nothing hides it):
+            // backwards, 128 entries (one 16-byte load per lane) at a time, so a
+            // row whose last block holds an in-range entry (every row whose
+            // context reaches k) takes one round (all 2048 entries read forwards
+            // cost ~7 us); prefill overlaps the scan with the previous token's blocks
             int last = -1;
             const int i_beg = un.jb * kBN;
             const int i_end = un.je * kBN < p.k ? un.je * kBN : p.k;
             if (PAGED && (p.k & 3) == 0 && (reinterpret_cast<uintptr_t>(p.idx) & 15u) == 0) {
                 const int4 *q4 = reinterpret_cast<const int4 *>(idx_row);
-#pragma unroll 16
-                for (int m = 0; m < 32; ++m) {
-                    const int i = i_beg + 4 * (lane + 32 * m);
-                    if (i < i_end) {
+                for (int c1 = i_end; c1 > i_beg && last < 0; c1 -= 128) {
+                    // i_beg, i_end and i are multiples of 4: a load is wholly inside or
+                    // wholly before [i_beg, c1)
+                    const int i = c1 - 128 + 4 * lane;
+                    if (i >= i_beg) {
                         const int4 v = __ldg(q4 + (i >> 2));
                         const int vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            if (i + e < i_end && in_range<PAGED>(p, vv[e], ctx))
+                            if (in_range<PAGED>(p, vv[e], ctx))
                                 last = i + e;
+                    }
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const int y = __shfl_xor_sync(0xffffffffu, last, o);
+                        last = y > last ? y : last;
                     }
                 }
             } else {
