@@ -54,7 +54,7 @@ def _L():
         lib.dsa_oracle_sparse_mla.argtypes = [P, P, i32, P, i32, i32, i32, i32, i32, f64, P, P]
         lib.dsa_oracle_sparse_mla_paged.argtypes = [P, P, i32, i32, P, i32, P, P, i32, i32, i32, i32, i32, f64, P, P]
         lib.dsa_oracle_attn_target.argtypes = [P, P, i32, P, i32, i32, i32, f64, P, i64]
-        lib.dsa_oracle_indexer_kl.argtypes = [P, P, P, i32, i32, i32, P, i32, P, i64, P, P, P, P, i32]
+        lib.dsa_oracle_indexer_kl.argtypes = [P, P, P, i32, i32, i32, P, i32, P, i64, P, P, P, P]
         _lib = lib
     return _lib
 
@@ -188,11 +188,10 @@ def attn_target(q_bits, kv_bits, q_pos, sm_scale: float, ld: int | None = None, 
     return out
 
 
-def indexer_kl(q, w, q_pos, k, p, mask_fp32: bool = False):
+def indexer_kl(q, w, q_pos, k, p):
     """Warm-up loss and gradients from dequantised fp64 q [n, HI, dI], k [S, dI], w [n, HI]
     and the target p [n, >= S].  Returns (loss [n], dw [n, HI], dq [n, HI, dI], dk [S, dI]).
-    mask_fp32: take the ReLU decisions of the gradients on the dot products computed the way
-    the GPU kernel computes them (see the C source); values stay fp64."""
+    The gradients' ReLU decisions are taken on the fp64 dot products (ReLU'(0) = 0)."""
     q = _c(q, np.float64)
     n, HI, dI = q.shape
     k = _c(k, np.float64)
@@ -205,5 +204,5 @@ def indexer_kl(q, w, q_pos, k, p, mask_fp32: bool = False):
     dq = np.empty((n, HI, dI), dtype=np.float64)
     dk = np.empty((S, dI), dtype=np.float64)
     _L().dsa_oracle_indexer_kl(_p(q), _p(w), _p(qp), n, HI, dI, _p(k), S, _p(pp), pp.shape[1], _p(loss), _p(dw),
-                               _p(dq), _p(dk), int(bool(mask_fp32)))
+                               _p(dq), _p(dk))
     return loss, dw, dq, dk

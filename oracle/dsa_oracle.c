@@ -460,30 +460,29 @@ void dsa_oracle_attn_target(const uint16_t *q, const uint16_t *kv, int S, const 
  *   dk[s,:]  = sum_r sum_j g w[r,j] [a > 0] q[r,j,:]
  * loss[n], dw[n,HI], dq[n,HI,dI] are written; dk[S,dI] is zeroed and then
  * accumulated over the rows.
- *
- * mask_fp32: the ReLU decision [a > 0] is a discrete one that rounding can flip
- * when a is within a few fp32 ulps of 0, and it moves the gradient by a whole
- * g w k term.  With mask_fp32 != 0 the decision is taken on a computed the way
- * the GPU kernel computes it (fp32 values of q and k, fp32 fused multiply-adds
- * over d in groups of four, within a group from d + 3 down to d); every value
- * stays fp64.  With 0 (the default of the pins) the decision is exact. */
-static int relu_on(const double *qv, const double *kv, int dI, double a, int mask_fp32)
+ * ReLU'(0) = 0, and the decision [a > 0] is taken on the exact a: see relu_on. */
+
+/* [a > 0] for a = <qv, kv> of dI terms, given the fp64 sum a and sabs = sum |q_d k_d|.
+ * The fp64 sum is off by at most 2 dI 2^-53 sabs (products and additions each
+ * rounded once), so its sign stands beyond dI 2^-50 sabs.  Below that the sum is
+ * formed again in binary128, where for FP8-dequantised inputs it is exact: every
+ * product of (code x scale) values has at most 2 x 28 significant bits, all of
+ * them share the factor of the two scales, and their exponents span the codes'
+ * 36 bits, so dI = 128 terms fit in 56 + 36 + 7 < 113 bits.  (A sum that cancels
+ * to exactly 0 can come out of fp64 as a tiny nonzero value.) */
+static int relu_on(const double *qv, const double *kv, int dI, double a, double sabs)
 {
-    if (!mask_fp32)
+    if (fabs(a) > (double)dI * 0x1p-50 * sabs)
         return a > 0.0;
-    float acc = 0.f;
-    for (int d = 0; d < dI; d += 4) {
-        float t = acc;
-        for (int e = 3; e >= 0; --e)
-            t = fmaf((float)qv[d + e], (float)kv[d + e], t);
-        acc = t;
-    }
-    return acc > 0.f;
+    _Float128 acc = 0;
+    for (int d = 0; d < dI; ++d)
+        acc += (_Float128)qv[d] * (_Float128)kv[d];
+    return acc > 0;
 }
 
 void dsa_oracle_indexer_kl(const double *q, const double *w, const int32_t *q_pos, int n, int HI, int dI,
                            const double *k, int S, const double *p, int64_t ldp, double *loss, double *dw, double *dq,
-                           double *dk, int mask_fp32)
+                           double *dk)
 {
     for (int64_t i = 0; i < (int64_t)S * dI; ++i)
         dk[i] = 0.0;
@@ -533,10 +532,13 @@ void dsa_oracle_indexer_kl(const double *q, const double *w, const int32_t *q_po
         loss[r] = L;
         for (int s = 0; s < cnt; ++s) {
             for (int j = 0; j < HI; ++j) {
-                double a = 0.0;
-                for (int d = 0; d < dI; ++d)
-                    a += qr[(int64_t)j * dI + d] * k[(int64_t)s * dI + d];
-                if (relu_on(qr + (int64_t)j * dI, k + (int64_t)s * dI, dI, a, mask_fp32)) {
+                double a = 0.0, sabs = 0.0;
+                for (int d = 0; d < dI; ++d) {
+                    const double t = qr[(int64_t)j * dI + d] * k[(int64_t)s * dI + d];
+                    a += t;
+                    sabs += fabs(t);
+                }
+                if (relu_on(qr + (int64_t)j * dI, k + (int64_t)s * dI, dI, a, sabs)) {
                     dw[(int64_t)r * HI + j] += g[s] * a;
                     for (int d = 0; d < dI; ++d)
                         dq[((int64_t)r * HI + j) * dI + d] += g[s] * wr[j] * k[(int64_t)s * dI + d];
@@ -556,10 +558,13 @@ void dsa_oracle_indexer_kl(const double *q, const double *w, const int32_t *q_po
             const double gs = g_all[(int64_t)r * S + s];
             const double *qr = q + (int64_t)r * HI * dI;
             for (int j = 0; j < HI; ++j) {
-                double a = 0.0;
-                for (int d = 0; d < dI; ++d)
-                    a += qr[(int64_t)j * dI + d] * k[(int64_t)s * dI + d];
-                if (relu_on(qr + (int64_t)j * dI, k + (int64_t)s * dI, dI, a, mask_fp32))
+                double a = 0.0, sabs = 0.0;
+                for (int d = 0; d < dI; ++d) {
+                    const double t = qr[(int64_t)j * dI + d] * k[(int64_t)s * dI + d];
+                    a += t;
+                    sabs += fabs(t);
+                }
+                if (relu_on(qr + (int64_t)j * dI, k + (int64_t)s * dI, dI, a, sabs))
                     for (int d = 0; d < dI; ++d)
                         dk[(int64_t)s * dI + d] += gs * w[(int64_t)r * HI + j] * qr[(int64_t)j * dI + d];
             }

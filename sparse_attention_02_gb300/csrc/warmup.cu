@@ -25,11 +25,13 @@
 //                       exp(S - LSE) / H -> p.
 //   (the FP8 indexer)   I, as dsa_indexer_logits computes it.
 //   kl_grad_kernel      one CTA per row: LSE of I, the loss, g over I in place.
-//   bwd_rows_kernel     one CTA per query row, FP32 on the CUDA cores, 64-key
-//                       tiles in shared memory: a, dw, dq, and the coefficients
-//                       c[t,j,s] = g w [a > 0] for dk.
-//   bwd_keys_kernel     one CTA per (64-key tile, 256-row chunk): dk from c and
-//                       q, added to dk with atomics (dk is zeroed first).
+//   codes_kernel        the FP8 codes as bf16 (exact) and the bounds of the
+//                       exact ReLU decision.
+//   bwd_tc_kernel<0>    tcgen05 BF16, one CTA per tile of 128 (t, j) rows:
+//                       a = Q K^T per 128-key tile, c = g ks [a > 0] as a bf16
+//                       hi + lo pair in TMEM, dq += C K; dw on the way.
+//   bwd_tc_kernel<1>    the same per (128-key tile, chunk of row tiles) with
+//                       the roles swapped: dk += C^T Q, chunks meeting in atomics.
 #include "common.cuh"
 #include "launch.h"
 
@@ -329,243 +331,519 @@ __device__ __forceinline__ float e4m3_to_float(uint32_t c)
     return __uint_as_float(sign | ((e + 120u) << 23) | (man << 20));
 }
 
-// ---------------------------------------------------------- backward: rows
-// One CTA of 256 threads per query row t.  Per 64-key tile: the tile's
-// dequantised keys kd[64][128] and g; a[j][s] for the 64 heads x 64 keys
-// (thread: 4 heads x keys sg, sg + 16, sg + 32, sg + 48, float4 loads along d);
-// dw partials; c = g w [a>0] into shared memory and to the global c[t][j][s];
-// then dq[j][d] += sum_s c[j][s] kd[s][d] (thread: 4 heads x columns
-// 4 dd .. +4 and 64 + 4 dd .. +4).  Neighbouring threads read neighbouring key
-// rows and neighbouring column groups: with keys 4 rows apart (4 x 132 floats
-// = 16 banks) sixteen threads' rows fell on two bank groups, and 8-column
-// groups on four, and the kernel ran at the shared-memory pipe's limit.
-constexpr int kBTile = 64;
-constexpr int kBD = 128;
-constexpr int kBKdPitch = kBD + 4;   // floats per key row in shared memory (16-byte aligned, banks spread)
-constexpr int kBCPitch = kBTile + 4; // floats per head row of c
+// ------------------------------------------------- backward on tensor cores
+// Both gradient contractions run on BF16 tensor cores, in two kernels of one
+// shape.  The operands are the FP8 codes as bf16 (exact); the scales are
+// positive, so they multiply out of a and of the ReLU decision:
+//   rows (KEYS = false): one CTA per tile of 128 (t, j) rows, walking the key
+//     tiles its rows see.  D1 = Qc Kc^T (rows x keys, fp32 in TMEM); per
+//     element c = g ks [a > 0] and dw += g ks a; D2 += C Kc.  Then
+//     dq[t,j,:] = w[t,j] D2 and dw[t,j] = q_scale[t] sum.
+//   keys (KEYS = true): one CTA per (128-key tile, chunk of row tiles).
+//     D1 = Kc Qc^T (keys x rows); c = g w q_scale [a > 0]; D2 += C Qc, and D2
+//     is added to dk (chunks meet in the atomics; dk is zeroed first).
+// C reaches the tensor cores as a bf16 pair hi + lo (c to ~2^-17 relative), so
+// D2 is an fp32 sum of exact products.  The streamed code tile serves both
+// MMAs: K-major as D1's B operand, MN-major as D2's.
+// ReLU decision, exact: the tensor cores sum exact products in fp32, whose
+// error is below 2^-16 sum_d |q_d k_d| for 128 terms (127 additions at most
+// 2^-23 relative each); that sum is bounded by the q row's L1 norm times the
+// key row's largest code.  Where |a| is within that bound (and the element
+// contributes), the warp forms the exact sum of the code products as a 64-bit
+// integer (codes times 2^9 are integers, products below 2^36, 128 of them
+// below 2^43) and takes its sign.
+constexpr int kGThreads = 192;             // producer, MMA issuer, four epilogue warps
+constexpr int kGStages = 3;                // streamed code tiles
+constexpr int kGAtom = 128 * 128;          // one 64-column SW128 atom of a 128-row bf16 tile
+constexpr int kGTileBytes = 2 * kGAtom;    // 128 rows x 128 codes
+constexpr int kGAux = 6 * 128 * 4;         // per-stage column data (floats)
+constexpr int kGRowChunk = 64;             // row tiles per CTA of the keys kernel
+constexpr int kGOffRes = 0;                                   // the CTA's own tile
+constexpr int kGOffSt = kGOffRes + kGTileBytes;               // streamed tiles
+constexpr int kGOffAux = kGOffSt + kGStages * kGTileBytes;
+constexpr int kGOffList = kGOffAux + kGStages * kGAux;        // active row tiles (keys kernel)
+constexpr int kGOffBar = kGOffList + kGRowChunk * 4;
+constexpr int kGNBar = 17;
+constexpr int kGOffMisc = kGOffBar + kGNBar * 8;
+constexpr int kGSmem = kGOffMisc + 64 + 1024;
+static_assert(kGSmem <= 232448, "backward kernel shared memory");
+// barriers
+constexpr int G_RES = 0, G_SF = 1, G_SE = 4, G_DF = 7, G_DE = 9, G_CF = 11, G_CE = 13, G_D2 = 15, G_DONE = 16;
+// TMEM columns: D1 (two buffers), D2, C (two slots of 64 keys: hi then lo bf16 pairs)
+constexpr uint32_t GT_D1 = 0, GT_D2 = 256, GT_C = 384;
 
-template <int HI>
-__global__ void __launch_bounds__(256)
-    bwd_rows_kernel(const uint8_t *__restrict__ q8, const float *__restrict__ q_scale, const float *__restrict__ w,
-                    const uint8_t *__restrict__ k8, const float *__restrict__ k_scale, const int32_t *__restrict__ q_pos,
-                    int T, int S, const float *__restrict__ g, int64_t ldg, float *__restrict__ cbuf, int64_t ldc,
-                    float *__restrict__ dw, float *__restrict__ dq)
+struct BwdParams {
+    const uint8_t *q8, *k8;  // FP8 codes (exact decisions)
+    const float *q_scale, *w, *k_scale;
+    const float *qb;         // [T * HI] 2^-16 x the q code row's L1 norm (rounded up)
+    const float *kinf;       // [S] largest |code| of the key row
+    const int32_t *q_pos;
+    const float *g;          // [T, ldg] dL/dI
+    int64_t ldg;
+    int T, S, HI;
+    float *dw, *dq, *dk;
+    unsigned *status;
+};
+
+// E4M3 ("fn") code times 2^9 as an integer: (8 + mantissa) << (exponent - 1), or
+// the mantissa itself for subnormals.
+__device__ __forceinline__ int e4m3_q9(uint32_t c)
 {
-    static_assert(HI == 64 || HI == 32, "heads");
-    constexpr int JT = HI / 16; // heads per thread in the a phase (16 head groups)
-    extern __shared__ __align__(16) float bsm[];
-    float *qd = bsm;                             // [HI][kBD]
-    float *kd = qd + HI * kBD;                   // [kBTile][kBKdPitch]
-    float *cs = kd + kBTile * kBKdPitch;         // [HI][kBCPitch]
-    float *gt = cs + HI * kBCPitch;              // [kBTile]
-    float *dws = gt + kBTile;                    // [HI]
-    grid_dep_wait();
-    grid_dep_launch();
-    const int t = gridDim.x - 1 - blockIdx.x;
-    int64_t qp = q_pos[t];
-    qp = qp > S - 1 ? S - 1 : qp;
-    const int pos = qp < 0 ? -1 : static_cast<int>(qp);
-    const float qs = q_scale[t];
-    for (int i = threadIdx.x; i < HI * kBD; i += 256)
-        qd[i] = e4m3_to_float(q8[(int64_t)t * HI * kBD + i]) * qs;
-    for (int i = threadIdx.x; i < HI; i += 256)
-        dws[i] = 0.f;
-    // a phase: thread (jg, sg) = heads jg * JT .. +JT, keys sg + 16 e (e < 4)
-    const int jg = threadIdx.x >> 4, sg = threadIdx.x & 15;
-    // dq phase: thread (jd, dd) = heads jd * JD .. +JD, columns 4 dd .. +4 and 64 + 4 dd .. +4
-    constexpr int JD = HI / 16;
-    const int jd = threadIdx.x >> 4, dd = threadIdx.x & 15;
-    float acc_dq[JD][8];
+    const int e = static_cast<int>((c >> 3) & 15u), m = static_cast<int>(c & 7u);
+    const int mag = e ? (8 | m) << (e - 1) : m;
+    return (c & 0x80u) ? -mag : mag;
+}
+
+// Exact sign test of <q code row, k code row> (128 codes each), by the whole warp.
+__device__ __forceinline__ bool exact_dot_positive(const uint8_t *qr, const uint8_t *kr, int lane)
+{
+    const uint32_t qw = __ldg(reinterpret_cast<const uint32_t *>(qr) + lane);
+    const uint32_t kw = __ldg(reinterpret_cast<const uint32_t *>(kr) + lane);
+    long long acc = 0;
 #pragma unroll
-    for (int i = 0; i < JD; ++i)
+    for (int b = 0; b < 4; ++b)
+        acc += static_cast<long long>(e4m3_q9((qw >> (8 * b)) & 255u)) * e4m3_q9((kw >> (8 * b)) & 255u);
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            acc_dq[i][e] = 0.f;
-    float acc_dw[JT];
-#pragma unroll
-    for (int i = 0; i < JT; ++i)
-        acc_dw[i] = 0.f;
-    float wj[JT];
-#pragma unroll
-    for (int i = 0; i < JT; ++i)
-        wj[i] = w[(int64_t)t * HI + jg * JT + i];
-    const int ntiles = pos < 0 ? 0 : pos / kBTile + 1;
-    for (int kt = 0; kt < ntiles; ++kt) {
-        const int s0 = kt * kBTile;
-        __syncthreads(); // previous tile's kd, cs, gt fully used
-        for (int i = threadIdx.x; i < kBTile * kBD; i += 256) {
-            const int s = i / kBD, d = i % kBD;
-            const int sk = s0 + s;
-            kd[s * kBKdPitch + d] = sk <= pos ? e4m3_to_float(k8[(int64_t)sk * kBD + d]) * k_scale[sk] : 0.f;
-        }
-        for (int i = threadIdx.x; i < kBTile; i += 256)
-            gt[i] = s0 + i <= pos ? g[(int64_t)t * ldg + s0 + i] : 0.f;
-        __syncthreads();
-        float a[JT][4];
-#pragma unroll
-        for (int i = 0; i < JT; ++i)
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                a[i][e] = 0.f;
-#pragma unroll 4
-        for (int d = 0; d < kBD; d += 4) {
-            float4 qv[JT], kv[4];
-#pragma unroll
-            for (int i = 0; i < JT; ++i)
-                qv[i] = *reinterpret_cast<const float4 *>(qd + (jg * JT + i) * kBD + d);
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                kv[e] = *reinterpret_cast<const float4 *>(kd + (sg + 16 * e) * kBKdPitch + d);
-#pragma unroll
-            for (int i = 0; i < JT; ++i)
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    a[i][e] = fmaf(qv[i].x, kv[e].x,
-                                   fmaf(qv[i].y, kv[e].y, fmaf(qv[i].z, kv[e].z, fmaf(qv[i].w, kv[e].w, a[i][e]))));
-        }
-#pragma unroll
-        for (int i = 0; i < JT; ++i) {
-            const int j = jg * JT + i;
-            float *crow = cbuf + ((int64_t)t * HI + j) * ldc + s0;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int sl = sg + 16 * e;
-                const float ge = gt[sl];
-                acc_dw[i] += a[i][e] > 0.f ? ge * a[i][e] : 0.f;
-                const float c = a[i][e] > 0.f ? ge * wj[i] : 0.f;
-                cs[j * kBCPitch + sl] = c;
-                if (s0 + sl < S)
-                    crow[sl] = c; // sixteen threads: 64 contiguous bytes
-            }
-        }
-        __syncthreads();
-#pragma unroll 4
-        for (int s = 0; s < kBTile; ++s) {
-            const float4 k0 = *reinterpret_cast<const float4 *>(kd + s * kBKdPitch + dd * 4);
-            const float4 k1 = *reinterpret_cast<const float4 *>(kd + s * kBKdPitch + 64 + dd * 4);
-#pragma unroll
-            for (int i = 0; i < JD; ++i) {
-                const float c = cs[(jd * JD + i) * kBCPitch + s];
-                acc_dq[i][0] = fmaf(c, k0.x, acc_dq[i][0]);
-                acc_dq[i][1] = fmaf(c, k0.y, acc_dq[i][1]);
-                acc_dq[i][2] = fmaf(c, k0.z, acc_dq[i][2]);
-                acc_dq[i][3] = fmaf(c, k0.w, acc_dq[i][3]);
-                acc_dq[i][4] = fmaf(c, k1.x, acc_dq[i][4]);
-                acc_dq[i][5] = fmaf(c, k1.y, acc_dq[i][5]);
-                acc_dq[i][6] = fmaf(c, k1.z, acc_dq[i][6]);
-                acc_dq[i][7] = fmaf(c, k1.w, acc_dq[i][7]);
-            }
-        }
+    for (int o = 16; o > 0; o >>= 1)
+        acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    return acc > 0;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ int clamp_pos(const BwdParams &p, int t)
+{
+    if (t >= p.T)
+        return -1;
+    const int qp = p.q_pos[t];
+    return qp > p.S - 1 ? p.S - 1 : qp;
+}
+
+// Largest clamped position among the tokens of row tile rt (-1: none sees a key).
+__device__ __forceinline__ int tile_maxpos(const BwdParams &p, int rt, int tpt)
+{
+    int m = -1;
+    for (int tl = 0; tl < tpt; ++tl) {
+        const int q = clamp_pos(p, rt * tpt + tl);
+        m = q > m ? q : m;
     }
-    // dw: the 16 key groups of a head group meet in shared memory
-#pragma unroll
-    for (int i = 0; i < JT; ++i)
-        atomicAdd(&dws[jg * JT + i], acc_dw[i]);
+    return m;
+}
+
+template <bool KEYS>
+__global__ void __launch_bounds__(kGThreads, 1)
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant__ CUtensorMap tm_str, BwdParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int i) { return sbase + kGOffBar + 8u * static_cast<uint32_t>(i); };
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + kGOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kGOffMisc + 4);
+    int *n_items_s = reinterpret_cast<int *>(smem + kGOffMisc + 8);
+    int *list = reinterpret_cast<int *>(smem + kGOffList);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tpt = 128 / p.HI; // tokens per row tile
+    const int nrt = (p.T * p.HI + 127) / 128;
+    // this CTA's own tile: a row tile (rows kernel) or a key tile (keys kernel)
+    const int own = KEYS ? static_cast<int>(blockIdx.x) : nrt - 1 - static_cast<int>(blockIdx.x);
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(G_RES), 1);
+        for (int i = 0; i < kGStages; ++i) {
+            mbar_init(bar(G_SF + i), 1);
+            mbar_init(bar(G_SE + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(G_DF + i), 1);
+            mbar_init(bar(G_DE + i), 4);
+            mbar_init(bar(G_CF + i), 4);
+            mbar_init(bar(G_CE + i), 1);
+        }
+        mbar_init(bar(G_D2), 1);
+        mbar_init(bar(G_DONE), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1)
+        tmem_alloc(sbase + kGOffMisc, 512);
+    tc_fence_before();
     __syncthreads();
-    for (int i = threadIdx.x; i < HI; i += 256)
-        dw[(int64_t)t * HI + i] = dws[i];
-#pragma unroll
-    for (int i = 0; i < JD; ++i) {
-        float *dst = dq + ((int64_t)t * HI + jd * JD + i) * kBD + dd * 4;
-        *reinterpret_cast<float4 *>(dst) = make_float4(acc_dq[i][0], acc_dq[i][1], acc_dq[i][2], acc_dq[i][3]);
-        *reinterpret_cast<float4 *>(dst + 64) = make_float4(acc_dq[i][4], acc_dq[i][5], acc_dq[i][6], acc_dq[i][7]);
-    }
-}
-
-template <int HI>
-size_t bwd_rows_smem()
-{
-    return (static_cast<size_t>(HI) * kBD + kBTile * kBKdPitch + HI * kBCPitch + kBTile + HI) * 4;
-}
-
-// ---------------------------------------------------------- backward: keys
-// One CTA of 256 threads per (64-key tile kt, chunk of 256 query rows): for
-// each row t of the chunk that sees the tile, dk[s][d] += sum_j c[t][j][s]
-// q[t][j][d] (thread: 4 keys x columns 4 dd .. +4 and 64 + 4 dd .. +4, so the
-// sixteen column groups of a row are 256 contiguous bytes); the partial sums
-// are added to dk with atomics.
-constexpr int kBRowChunk = 256;
-
-template <int HI>
-__global__ void __launch_bounds__(256)
-    bwd_keys_kernel(const uint8_t *__restrict__ q8, const float *__restrict__ q_scale,
-                    const int32_t *__restrict__ q_pos, int T, int S, const float *__restrict__ cbuf, int64_t ldc,
-                    float *__restrict__ dk)
-{
-    extern __shared__ __align__(16) float ksm[];
-    float *qd = ksm;                        // [HI][kBD]
-    float *ct = qd + HI * kBD;              // [HI][kBCPitch]: c[t][j][s0 .. s0 + 64)
-    grid_dep_wait();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    grid_dep_wait(); // no global memory before this: the previous kernel may still be running
     grid_dep_launch();
-    const int s0 = blockIdx.x * kBTile;
-    const int t0 = blockIdx.y * kBRowChunk;
-    const int t1 = t0 + kBRowChunk < T ? t0 + kBRowChunk : T;
-    const int sg = threadIdx.x >> 4, dd = threadIdx.x & 15; // keys sg * 4 .. +4, columns 4 dd .. +4, 64 + 4 dd .. +4
-    float acc[4][8];
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-            acc[e][c] = 0.f;
-    bool any = false;
-    for (int t = t0; t < t1; ++t) {
-        int64_t qp = q_pos[t];
-        qp = qp > S - 1 ? S - 1 : qp;
-        if (qp < s0)
-            continue; // uniform: this row sees none of the tile
-        any = true;
-        const int nvalid = static_cast<int>(qp - s0 + 1 < kBTile ? qp - s0 + 1 : kBTile);
-        __syncthreads();
-        const float qs = q_scale[t];
-        for (int i = threadIdx.x; i < HI * kBD; i += 256)
-            qd[i] = e4m3_to_float(q8[(int64_t)t * HI * kBD + i]) * qs;
-        for (int i = threadIdx.x; i < HI * kBTile; i += 256) {
-            const int j = i / kBTile, s = i % kBTile;
-            ct[j * kBCPitch + s] = s < nvalid ? cbuf[((int64_t)t * HI + j) * ldc + s0 + s] : 0.f;
+    // ---- the work list: key tiles 0 .. (rows kernel), active row tiles of the chunk (keys kernel)
+    if (warp == 0) {
+        if (!KEYS) {
+            if (lane == 0) {
+                const int mp = tile_maxpos(p, own, tpt);
+                *n_items_s = mp < 0 ? 0 : mp / 128 + 1;
+            }
+        } else {
+            const int r0 = static_cast<int>(blockIdx.y) * kGRowChunk, s0 = own * 128;
+            int n = 0;
+            for (int b = 0; b < kGRowChunk; b += 32) {
+                const int rt = r0 + b + lane;
+                const bool act = rt < nrt && tile_maxpos(p, rt, tpt) >= s0;
+                const unsigned m = __ballot_sync(0xffffffffu, act);
+                if (act)
+                    list[n + __popc(m & ((1u << lane) - 1u))] = rt;
+                n += __popc(m);
+            }
+            if (lane == 0)
+                *n_items_s = n;
         }
-        __syncthreads();
-#pragma unroll 2
-        for (int j = 0; j < HI; ++j) {
-            const float4 q0 = *reinterpret_cast<const float4 *>(qd + j * kBD + dd * 4);
-            const float4 q1 = *reinterpret_cast<const float4 *>(qd + j * kBD + 64 + dd * 4);
-            const float4 cv = *reinterpret_cast<const float4 *>(ct + j * kBCPitch + sg * 4);
-            const float cc[4] = {cv.x, cv.y, cv.z, cv.w};
+    }
+    __syncthreads();
+    const int n_items = *n_items_s;
+    bool ok = true;
+
+    if (warp == 0) {
+        // --------------------------------------------- producer: tiles by TMA, column data
+        int pos[4] = {-1, -1, -1, -1};
+        if (!KEYS)
+            for (int tl = 0; tl < tpt; ++tl)
+                pos[tl] = clamp_pos(p, own * tpt + tl);
+        if (lane == 0 && n_items > 0) {
+            tma_prefetch_desc(&tm_res);
+            tma_prefetch_desc(&tm_str);
+            mbar_arrive_expect_tx(bar(G_RES), kGTileBytes);
+            tma_load_2d(sbase + kGOffRes, &tm_res, bar(G_RES), 0, own * 128);
+            tma_load_2d(sbase + kGOffRes + kGAtom, &tm_res, bar(G_RES), 64, own * 128);
+        }
+        for (int i = 0; i < n_items; ++i) {
+            const int st = i % kGStages;
+            if (i >= kGStages && !mbar_wait_warp(bar(G_SE + st), ((i / kGStages) - 1) & 1, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            float *aux = reinterpret_cast<float *>(smem + kGOffAux + st * kGAux);
+            const int str = KEYS ? list[i] : i; // streamed tile: row tile / key tile
+            if (!KEYS) {
+                // [tl][key]: g ks of token tl (0 where the token does not see the key); [4][key]: max |k code|
+                for (int x = lane; x < 5 * 128; x += 32) {
+                    const int tl = x >> 7, s = str * 128 + (x & 127);
+                    float v = 0.f;
+                    if (tl < 4) {
+                        if (tl < tpt && s <= pos[tl])
+                            v = p.g[(int64_t)(own * tpt + tl) * p.ldg + s] * p.k_scale[s];
+                    } else if (s < p.S) {
+                        v = p.kinf[s];
+                    }
+                    aux[x] = v;
+                }
+            } else {
+                // [tl][key]: g of token tl of the row tile at this CTA's keys; [4][row]: w q_scale; [5][row]: q bound
+                for (int x = lane; x < 6 * 128; x += 32) {
+                    const int tl = x >> 7, c = x & 127;
+                    float v = 0.f;
+                    if (tl < 4) {
+                        const int t = str * tpt + tl, s = own * 128 + c;
+                        if (tl < tpt && s <= clamp_pos(p, t))
+                            v = p.g[(int64_t)t * p.ldg + s];
+                    } else {
+                        const int r = str * 128 + c, t = r / p.HI;
+                        if (t < p.T)
+                            v = tl == 4 ? p.w[r] * p.q_scale[t] : p.qb[r];
+                    }
+                    aux[x] = v;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t dst = sbase + kGOffSt + st * kGTileBytes;
+                mbar_arrive_expect_tx(bar(G_SF + st), kGTileBytes);
+                tma_load_2d(dst, &tm_str, bar(G_SF + st), 0, str * 128);
+                tma_load_2d(dst + kGAtom, &tm_str, bar(G_SF + st), 64, str * 128);
+            }
+        }
+        // every load issued has landed before the CTA exits
+        if (lane == 0 && n_items > 0) {
+            mbar_drain(bar(G_RES), 0);
+            for (int i = n_items > kGStages ? n_items - kGStages : 0; i < n_items; ++i)
+                mbar_drain(bar(G_SF + i % kGStages), (i / kGStages) & 1);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        constexpr uint32_t id1 = idesc_f32acc(128, 128, 1u, false, false);
+        constexpr uint32_t id2 = idesc_f32acc(128, 128, 1u, false, true);
+        // D2 += C(it) . tile(it): keys (rows kernel) / rows (keys kernel) 64 h .. 64 h + 63 of the
+        // streamed tile are K, its 128 columns N (MN-major); C's hi then lo pairs are A (TMEM)
+        auto mma2 = [&](int it) -> bool {
+            const int st = it % kGStages;
+            const uint32_t stg = sbase + kGOffSt + st * kGTileBytes;
+            for (int h = 0; h < 2; ++h) {
+                if (!mbar_wait_warp(bar(G_CF + h), it & 1, abort_flag, p.status))
+                    return false;
+                tc_fence_after();
+                if (lane == 0) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                acc[e][0] = fmaf(cc[e], q0.x, acc[e][0]);
-                acc[e][1] = fmaf(cc[e], q0.y, acc[e][1]);
-                acc[e][2] = fmaf(cc[e], q0.z, acc[e][2]);
-                acc[e][3] = fmaf(cc[e], q0.w, acc[e][3]);
-                acc[e][4] = fmaf(cc[e], q1.x, acc[e][4]);
-                acc[e][5] = fmaf(cc[e], q1.y, acc[e][5]);
-                acc[e][6] = fmaf(cc[e], q1.z, acc[e][6]);
-                acc[e][7] = fmaf(cc[e], q1.w, acc[e][7]);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t bd = sdesc(stg + (64 * h + 16 * kk) * 128, kGAtom, 1024, 2);
+                        const uint32_t ca = tmem + GT_C + 64 * h + 8 * kk;
+                        umma_f16_ts(tmem + GT_D2, ca, bd, id2, (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
+                        umma_f16_ts(tmem + GT_D2, ca + 32, bd, id2, 1u);
+                    }
+                    umma_commit(bar(G_CE + h));
+                    if (h == 1)
+                        umma_commit(bar(G_SE + st));
+                }
+                __syncwarp();
+            }
+            return true;
+        };
+        if (n_items > 0 && !mbar_wait_warp(bar(G_RES), 0, abort_flag, p.status))
+            ok = false;
+        for (int i = 0; ok && i < n_items; ++i) {
+            const int st = i % kGStages, b = i & 1;
+            if (!mbar_wait_warp(bar(G_SF + st), (i / kGStages) & 1, abort_flag, p.status) ||
+                (i >= 2 && !mbar_wait_warp(bar(G_DE + b), ((i >> 1) - 1) & 1, abort_flag, p.status))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t stg = sbase + kGOffSt + st * kGTileBytes, res = sbase + kGOffRes;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t off = (k >> 2) * kGAtom + 32 * (k & 3);
+                    umma_f16_ss(tmem + GT_D1 + 128 * b, sdesc(res + off, 16, 1024, 2), sdesc(stg + off, 16, 1024, 2),
+                                id1, k > 0 ? 1u : 0u);
+                }
+                umma_commit(bar(G_DF + b));
+            }
+            __syncwarp();
+            if (i >= 1 && !mma2(i - 1))
+                ok = false;
+        }
+        if (ok && n_items > 0 && !mma2(n_items - 1))
+            ok = false;
+        if (lane == 0) {
+            if (ok && n_items > 0)
+                umma_commit(bar(G_D2));
+            umma_commit(bar(G_DONE));
+            mbar_drain(bar(G_DONE), 0);
+        }
+        __syncwarp();
+    } else {
+        // --------------------------------------------------------- epilogue
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane; // TMEM lane: (t, j) row (rows kernel) / key (keys kernel)
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        const int rrow = own * 128 + row; // rows kernel: global (t, j) row; keys kernel: key
+        const int tl_own = row / p.HI;    // rows kernel: token of this row within the tile (warp-uniform)
+        const bool valid = KEYS ? rrow < p.S : rrow < p.T * p.HI;
+        const float qb_own = (!KEYS && valid) ? p.qb[rrow] : 0.f;
+        const float kinf_own = (KEYS && valid) ? p.kinf[rrow] : 0.f;
+        float dw_acc = 0.f;
+        for (int i = 0; i < n_items; ++i) {
+            const int b = i & 1, st = i % kGStages;
+            const int str = KEYS ? list[i] : i;
+            // the stage's column data (the producer's stores) and D1
+            if (!mbar_wait_warp(bar(G_SF + st), (i / kGStages) & 1, abort_flag, p.status) ||
+                !mbar_wait_warp(bar(G_DF + b), (i >> 1) & 1, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float *aux = reinterpret_cast<const float *>(smem + kGOffAux + st * kGAux);
+            float gt[4] = {0.f, 0.f, 0.f, 0.f}; // keys kernel: this key's g for each token of the row tile
+            if (KEYS)
+#pragma unroll
+                for (int tl = 0; tl < 4; ++tl)
+                    gt[tl] = aux[tl * 128 + row];
+            for (int h = 0; ok && h < 2; ++h) {
+                if (i >= 1 && !mbar_wait_warp(bar(G_CE + h), (i - 1) & 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll 1
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c = 2 * h + cc;
+                    uint32_t r[32];
+                    tmem_ld32(lane_base + GT_D1 + 128 * b + 32 * c, r);
+                    tmem_ld_wait();
+                    if (c == 3) { // D1 is in registers: release it
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(bar(G_DE + b));
+                    }
+                    // per column: the coefficient if a > 0, and whether the fp32 sign can be trusted
+                    float cv[32];
+                    uint32_t posm = 0u, ambm = 0u;
+                    const int tlc = (32 * c) / p.HI; // keys kernel: token of these columns (uniform)
+                    const float gc = tlc == 0 ? gt[0] : tlc == 1 ? gt[1] : tlc == 2 ? gt[2] : gt[3];
+#pragma unroll
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        const int col = 32 * c + 4 * e4;
+                        float4 v4, b4;
+                        if (!KEYS) {
+                            v4 = *reinterpret_cast<const float4 *>(aux + tl_own * 128 + col);
+                            b4 = *reinterpret_cast<const float4 *>(aux + 4 * 128 + col);
+                        } else {
+                            v4 = *reinterpret_cast<const float4 *>(aux + 4 * 128 + col);
+                            b4 = *reinterpret_cast<const float4 *>(aux + 5 * 128 + col);
+                        }
+                        const float vv[4] = {v4.x, v4.y, v4.z, v4.w}, bb[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int e = 4 * e4 + q;
+                            const float a = __uint_as_float(r[e]);
+                            const float v = KEYS ? gc * vv[q] : vv[q];
+                            const float bnd = KEYS ? bb[q] * kinf_own : qb_own * bb[q];
+                            cv[e] = v;
+                            posm |= (a > 0.f ? 1u : 0u) << e;
+                            ambm |= ((v != 0.f && fabsf(a) <= bnd) ? 1u : 0u) << e;
+                        }
+                    }
+                    // exact decisions where the fp32 sum is within its error bound of 0
+                    unsigned todo = __ballot_sync(0xffffffffu, ambm != 0u);
+                    while (todo) {
+                        const int L = __ffs(todo) - 1;
+                        const uint32_t mL = __shfl_sync(0xffffffffu, ambm, L);
+                        const int e = __ffs(mL) - 1;
+                        const int qrow = KEYS ? str * 128 + 32 * c + e : own * 128 + quad * 32 + L;
+                        const int key = KEYS ? own * 128 + quad * 32 + L : str * 128 + 32 * c + e;
+                        const bool pos = exact_dot_positive(p.q8 + (int64_t)qrow * 128, p.k8 + (int64_t)key * 128, lane);
+                        if (lane == L) {
+                            ambm &= ~(1u << e);
+                            posm = pos ? (posm | (1u << e)) : (posm & ~(1u << e));
+                        }
+                        todo = __ballot_sync(0xffffffffu, ambm != 0u);
+                    }
+                    // C = coefficient where a > 0, as hi + lo bf16 pairs
+                    uint32_t hi[16], lo[16];
+#pragma unroll
+                    for (int e2 = 0; e2 < 16; ++e2) {
+                        const int e0 = 2 * e2, e1 = e0 + 1;
+                        const float c0 = ((posm >> e0) & 1u) ? cv[e0] : 0.f;
+                        const float c1 = ((posm >> e1) & 1u) ? cv[e1] : 0.f;
+                        if (!KEYS)
+                            dw_acc += c0 * __uint_as_float(r[e0]) + c1 * __uint_as_float(r[e1]);
+                        const uint32_t hp = pack_bf16x2(c0, c1);
+                        hi[e2] = hp;
+                        lo[e2] = pack_bf16x2(c0 - __uint_as_float(hp << 16), c1 - __uint_as_float(hp & 0xFFFF0000u));
+                    }
+                    tmem_st16(lane_base + GT_C + 64 * h + 16 * cc, hi);
+                    tmem_st16(lane_base + GT_C + 64 * h + 32 + 16 * cc, lo);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(bar(G_CF + h));
+            }
+            if (!ok)
+                break;
+        }
+        // ---- D2 out: dq and dw (rows kernel), dk partial sums (keys kernel)
+        const bool have = ok && n_items > 0;
+        if (have && !mbar_wait_warp(bar(G_D2), 0, abort_flag, p.status))
+            ok = false;
+        tc_fence_after();
+        if (!KEYS) {
+            const float wr = valid ? p.w[rrow] : 0.f;
+#pragma unroll 1
+            for (int c0 = 0; c0 < 128; c0 += 32) {
+                uint32_t r[32];
+                if (have && ok) {
+                    tmem_ld32(lane_base + GT_D2 + c0, r);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        r[e] = 0u;
+                }
+                if (valid) {
+                    float4 *dst = reinterpret_cast<float4 *>(p.dq + (int64_t)rrow * 128 + c0);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        dst[e] = make_float4(wr * __uint_as_float(r[4 * e]), wr * __uint_as_float(r[4 * e + 1]),
+                                             wr * __uint_as_float(r[4 * e + 2]), wr * __uint_as_float(r[4 * e + 3]));
+                }
+            }
+            if (valid)
+                p.dw[rrow] = p.q_scale[rrow / p.HI] * dw_acc;
+        } else if (have && ok) { // warp-uniform: the TMEM loads are warp-collective
+#pragma unroll 1
+            for (int c0 = 0; c0 < 128; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(lane_base + GT_D2 + c0, r);
+                tmem_ld_wait();
+                if (valid) {
+                    float *dst = p.dk + (int64_t)rrow * 128 + c0;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        atomicAdd(dst + e, __uint_as_float(r[e]));
+                }
             }
         }
     }
-    if (!any)
-        return;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const int s = s0 + sg * 4 + e;
-        if (s < S)
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                atomicAdd(dk + (int64_t)s * kBD + (c < 4 ? dd * 4 + c : 64 + dd * 4 + c - 4), acc[e][c]);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
     }
 }
 
-template <int HI>
-size_t bwd_keys_smem()
+// The codes as bf16 (exact) for the tensor cores, and the decision bounds:
+// qb[row] = 2^-16 x L1 norm of a q code row (rounded up), kinf[s] = largest
+// |code| of key s.  One warp per row; rows [0, nq) are q rows, then key rows.
+__global__ void __launch_bounds__(256)
+    codes_kernel(const uint8_t *__restrict__ q8, int nq, const uint8_t *__restrict__ k8, int nk,
+                 __nv_bfloat16 *__restrict__ qc, float *__restrict__ qb, __nv_bfloat16 *__restrict__ kc,
+                 float *__restrict__ kinf)
 {
-    return (static_cast<size_t>(HI) * kBD + HI * kBCPitch) * 4;
+    grid_dep_wait();
+    grid_dep_launch();
+    const int lane = threadIdx.x & 31;
+    const int r = static_cast<int>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (r >= nq + nk)
+        return;
+    const bool isq = r < nq;
+    const uint8_t *src = isq ? q8 + (int64_t)r * 128 : k8 + (int64_t)(r - nq) * 128;
+    const uint32_t wv = reinterpret_cast<const uint32_t *>(src)[lane];
+    float v[4];
+    float l1 = 0.f, mx = 0.f;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        v[b] = e4m3_to_float((wv >> (8 * b)) & 255u);
+        l1 += fabsf(v[b]);
+        mx = fmaxf(mx, fabsf(v[b]));
+    }
+    __nv_bfloat16 *dst = isq ? qc + (int64_t)r * 128 : kc + (int64_t)(r - nq) * 128;
+    const uint32_t lo = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16(v[0]))) |
+                        (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16(v[1]))) << 16);
+    const uint32_t hi = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16(v[2]))) |
+                        (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16(v[3]))) << 16);
+    reinterpret_cast<uint2 *>(dst)[lane] = make_uint2(lo, hi);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if (lane == 0) {
+        if (isq)
+            qb[r] = l1 * (1.52587890625e-05f * 1.00390625f); // 2^-16 (1 + 2^-8): margin for this sum's rounding
+        else
+            kinf[r - nq] = mx;
+    }
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct WLayout {
-    size_t p, ig, c, total;
-    int64_t ldc; // row pitch of c, a multiple of 4 floats
+    size_t p, ig, qc, kc, qb, kinf, total;
 };
 
 WLayout wlayout(int T, int S, int HI)
@@ -576,45 +854,64 @@ WLayout wlayout(int T, int S, int HI)
     o += align256(static_cast<size_t>(T) * S * 4);
     l.ig = o;
     o += align256(static_cast<size_t>(T) * S * 4);
-    l.ldc = (S + 3) & ~3;
-    l.c = o;
-    o += align256(static_cast<size_t>(T) * HI * l.ldc * 4);
+    l.qc = o;
+    o += align256(static_cast<size_t>(T) * HI * 128 * 2);
+    l.kc = o;
+    o += align256(static_cast<size_t>(S) * 128 * 2);
+    l.qb = o;
+    o += align256(static_cast<size_t>(T) * HI * 4);
+    l.kinf = o;
+    o += align256(static_cast<size_t>(S) * 4);
     l.total = o;
     return l;
 }
 
-template <int HI>
-int launch_backward(const WarmupArgs &a, float *ig, float *cbuf, int64_t ldc, cudaStream_t stream, char *err,
-                    size_t errlen)
+int launch_backward(const WarmupArgs &a, const WLayout &l, char *ws, const float *ig, unsigned *status,
+                    cudaStream_t stream, char *err, size_t errlen)
 {
+    __nv_bfloat16 *qc = reinterpret_cast<__nv_bfloat16 *>(ws + l.qc);
+    __nv_bfloat16 *kc = reinterpret_cast<__nv_bfloat16 *>(ws + l.kc);
+    float *qb = reinterpret_cast<float *>(ws + l.qb);
+    float *kinf = reinterpret_cast<float *>(ws + l.kinf);
+    const int nq = a.T * a.HI;
+    cudaError_t e = launch_pdl(codes_kernel, dim3(static_cast<unsigned>((nq + a.S + 7) / 8)), dim3(256), 0, stream, 1,
+                               static_cast<const uint8_t *>(a.q8), nq, static_cast<const uint8_t *>(a.k8), a.S, qc, qb,
+                               kc, kinf);
+    if (e != cudaSuccess) {
+        snprintf(err, errlen, "warm-up codes launch: %s", cudaGetErrorString(e));
+        return DSA_ERR_CUDA;
+    }
     static std::atomic<bool> rows_attr[64], keys_attr[64];
-    if (cudaError_t e = raise_smem_limit_once(bwd_rows_kernel<HI>, static_cast<int>(bwd_rows_smem<HI>()), rows_attr);
-        e != cudaSuccess) {
-        snprintf(err, errlen, "cudaFuncSetAttribute(warm-up rows): %s", cudaGetErrorString(e));
+    if (cudaError_t ea = raise_smem_limit_once(bwd_tc_kernel<false>, kGSmem, rows_attr); ea != cudaSuccess) {
+        snprintf(err, errlen, "cudaFuncSetAttribute(warm-up rows): %s", cudaGetErrorString(ea));
         return DSA_ERR_CUDA;
     }
-    if (cudaError_t e = raise_smem_limit_once(bwd_keys_kernel<HI>, static_cast<int>(bwd_keys_smem<HI>()), keys_attr);
-        e != cudaSuccess) {
-        snprintf(err, errlen, "cudaFuncSetAttribute(warm-up keys): %s", cudaGetErrorString(e));
+    if (cudaError_t ea = raise_smem_limit_once(bwd_tc_kernel<true>, kGSmem, keys_attr); ea != cudaSuccess) {
+        snprintf(err, errlen, "cudaFuncSetAttribute(warm-up keys): %s", cudaGetErrorString(ea));
         return DSA_ERR_CUDA;
     }
-    cudaError_t e = launch_pdl(bwd_rows_kernel<HI>, dim3(a.T), dim3(256), bwd_rows_smem<HI>(), stream, 1,
-                               static_cast<const uint8_t *>(a.q8), a.q_scale, a.w, static_cast<const uint8_t *>(a.k8),
-                               a.k_scale, a.q_pos, a.T, a.S, static_cast<const float *>(ig), (int64_t)a.S, cbuf,
-                               ldc, a.dw, a.dq);
+    CUtensorMap tq, tk;
+    if (!encode_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, qc, 128, (uint64_t)nq, 256, 64, 128,
+                        CU_TENSOR_MAP_SWIZZLE_128B, err, errlen) ||
+        !encode_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kc, 128, (uint64_t)a.S, 256, 64, 128,
+                        CU_TENSOR_MAP_SWIZZLE_128B, err, errlen))
+        return DSA_ERR_CUDA;
+    BwdParams bp{static_cast<const uint8_t *>(a.q8), static_cast<const uint8_t *>(a.k8), a.q_scale, a.w, a.k_scale,
+                 qb, kinf, a.q_pos, ig, (int64_t)a.S, a.T, a.S, a.HI, a.dw, a.dq, a.dk, status};
+    const int nrt = (nq + 127) / 128, nkt = (a.S + 127) / 128;
+    e = launch_pdl(bwd_tc_kernel<false>, dim3(static_cast<unsigned>(nrt)), dim3(kGThreads), kGSmem, stream, 1, tq, tk,
+                   bp);
     if (e != cudaSuccess) {
         snprintf(err, errlen, "warm-up rows launch: %s", cudaGetErrorString(e));
         return DSA_ERR_CUDA;
     }
-    e = cudaMemsetAsync(a.dk, 0, static_cast<size_t>(a.S) * kBD * 4, stream);
+    e = cudaMemsetAsync(a.dk, 0, static_cast<size_t>(a.S) * 128 * 4, stream);
     if (e != cudaSuccess) {
         snprintf(err, errlen, "zeroing dk: %s", cudaGetErrorString(e));
         return DSA_ERR_CUDA;
     }
-    dim3 grid((a.S + kBTile - 1) / kBTile, (a.T + kBRowChunk - 1) / kBRowChunk);
-    e = launch_pdl(bwd_keys_kernel<HI>, grid, dim3(256), bwd_keys_smem<HI>(), stream, 1,
-                   static_cast<const uint8_t *>(a.q8), a.q_scale, a.q_pos, a.T, a.S, static_cast<const float *>(cbuf),
-                   ldc, a.dk);
+    const dim3 grid(static_cast<unsigned>(nkt), static_cast<unsigned>((nrt + kGRowChunk - 1) / kGRowChunk));
+    e = launch_pdl(bwd_tc_kernel<true>, grid, dim3(kGThreads), kGSmem, stream, 1, tk, tq, bp);
     if (e != cudaSuccess) {
         snprintf(err, errlen, "warm-up keys launch: %s", cudaGetErrorString(e));
         return DSA_ERR_CUDA;
@@ -641,7 +938,6 @@ int launch_warmup(const WarmupArgs &a, cudaStream_t stream, char *err, size_t er
     char *ws = static_cast<char *>(a.workspace);
     float *pt = reinterpret_cast<float *>(ws + l.p);
     float *ig = reinterpret_cast<float *>(ws + l.ig);
-    float *cbuf = reinterpret_cast<float *>(ws + l.c);
 
     // 1. target p
     static std::atomic<bool> target_attr[64];
@@ -675,8 +971,7 @@ int launch_warmup(const WarmupArgs &a, cudaStream_t stream, char *err, size_t er
         return DSA_ERR_CUDA;
     }
     // 4. gradients
-    return a.HI == 64 ? launch_backward<64>(a, ig, cbuf, l.ldc, stream, err, errlen)
-                      : launch_backward<32>(a, ig, cbuf, l.ldc, stream, err, errlen);
+    return launch_backward(a, l, ws, ig, status, stream, err, errlen);
 }
 
 } // namespace dsa

@@ -4,13 +4,14 @@ through the C ABI.
 The oracle computes the target (the main attention's head-averaged dense causal
 distribution) from the bf16 bits of q and kv, and the loss and gradients from the
 dequantised FP8 indexer inputs (codes decoded by the oracle's own E4M3 decoder,
-times their scales; the gradients' ReLU decisions are taken on the dot products
-formed as the kernel forms them in fp32, since rounding can flip a decision near
-a = 0).  Sizes span several 128-key target tiles and 64-key backward
-tiles with ragged tails; a chunk of rows over a longer prefix, fewer heads, both
-indexer head counts, and positions past the keys are covered.  Tolerances: loss
-per row within 1e-4 + 1e-3 |loss|; each gradient tensor within 1e-3 of its largest
-magnitude, element by element (fp32 arithmetic after the tensor-core products).
+times their scales).  The kernels take each gradient's ReLU decision on the exact
+dot product of the codes, as the oracle does; a planted row pair whose products
+cancel to a tiny or zero sum checks that where fp32 would lose the sign.  Sizes
+span several 128-row and 128-key backward tiles with ragged tails; a chunk of rows
+over a longer prefix, fewer heads, both indexer head counts, and positions past the
+keys are covered.  Tolerances: loss per row within 1e-4 + 1e-3 |loss|; each
+gradient tensor within 1e-3 of its largest magnitude, element by element (fp32
+arithmetic after the tensor-core products).
 """
 import dataclasses
 
@@ -48,9 +49,7 @@ def _run(x, q_pos, S, H):
     kd = tab[x["k8"][:S].cpu().numpy()] * x["ks"][:S].cpu().double().numpy()[:, None]
     qp = q_pos.cpu().numpy()
     p = oracle.attn_target(bits16(q), bits16(x["kv"][:S]), qp, 1 / 24, ld=S)
-    # ReLU decisions on the fp32 dot products the kernel forms (a discrete outcome that rounding
-    # can flip near a = 0); every value of the oracle stays fp64
-    ref = oracle.indexer_kl(qd, x["w"].cpu().double().numpy(), qp, kd, p, mask_fp32=True)
+    ref = oracle.indexer_kl(qd, x["w"].cpu().double().numpy(), qp, kd, p)
     got = [t.cpu().double().numpy() for t in (loss, dw, dq, dk)]
     return status, got, ref
 
@@ -97,3 +96,31 @@ def test_warmup_position_past_keys_is_clamped_and_flagged():
     status, got, ref = _run(x, q_pos, S, 64)
     assert status & 0x2  # DSA_DEV_BAD_POSITION
     _check(got, ref)     # the oracle clamps the same way
+
+
+def test_warmup_exact_relu_decision_at_cancellation():
+    """Rows whose code products cancel: (448, 448, 2^-9) . (448, -448, +-2^-9) is +-2^-18 and
+    (448, 448) . (448, -448) is 0, all of which an fp32 sum of the products in the wrong order
+    rounds to 0, and a three-term sum that is exactly 0.  The gradient terms of those (row, key)
+    pairs are included exactly when the exact sum is positive."""
+    L = 300
+    x = W.prefill_inputs(W.CONFIGS["prefill_4k"], DEV, L=L, seed=12)
+    q8, k8 = x["q8"].clone(), x["k8"].clone()
+    big, tiny, neg = 0x7E, 0x01, 0x80  # E4M3 codes of 448 and 2^-9; the sign bit
+    for (t, j, s, sign) in [(250, 3, 40, 0), (250, 7, 41, neg), (251, 60, 42, None), (299, 0, 298, 0)]:
+        q8[t, j].zero_()
+        q8[t, j, :3] = torch.tensor([big, big, tiny], dtype=torch.uint8)
+        k8[s].zero_()
+        k8[s, :2] = torch.tensor([big, big | neg], dtype=torch.uint8)
+        if sign is not None:
+            k8[s, 2] = tiny | sign
+    # (15, 15, 15) . (15, -16, 1) = 225 - 240 + 15 = 0 exactly, which a plain fp64 sum of the
+    # dequantised products need not return
+    q8[200, 9].zero_()
+    q8[200, 9, :3] = torch.tensor([0x57, 0x57, 0x57], dtype=torch.uint8)
+    k8[77].zero_()
+    k8[77, :3] = torch.tensor([0x57, 0xD8, 0x38], dtype=torch.uint8)
+    x = dict(x, q8=q8, k8=k8)
+    status, got, ref = _run(x, x["q_pos"], L, 128)
+    assert status == 0
+    _check(got, ref)

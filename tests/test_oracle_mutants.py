@@ -58,7 +58,9 @@ MUTANTS = {
     # indexer warm-up (training path)
     "kl_grad_sign": ("g[s] = exp(g[s] - lse) - ps;", "g[s] = ps - exp(g[s] - lse);"),
     "kl_lse_dropped": ("L += ps * (log(ps) - (g[s] - lse));", "L += ps * (log(ps) - g[s]);"),
-    "kl_grad_relu_mask_dropped": ("        return a > 0.0;", "        return 1;"),
+    "kl_grad_relu_mask_dropped": ("        return a > 0.0;\n", "        return 1;\n"),
+    "kl_dk_relu_mask_dropped": ("sabs))\n                    for", "sabs) || 1)\n                    for"),
+    "kl_relu_fp64_sign_at_zero": ("    return acc > 0;\n", "    return a > 0.0;\n"),
     "kl_dw_relu_dropped": ("dw[(int64_t)r * HI + j] += g[s] * a;", "dw[(int64_t)r * HI + j] += g[s];"),
     "kl_dk_weight_dropped": ("dk[(int64_t)s * dI + d] += gs * w[(int64_t)r * HI + j] * qr[(int64_t)j * dI + d];",
                              "dk[(int64_t)s * dI + d] += gs * qr[(int64_t)j * dI + d];"),
@@ -94,6 +96,7 @@ PINS = [
     lambda: tpins.test_uniform_indexer_closed_form(),
     lambda: tpins.test_target_one_head_is_the_library_softmax(),
     lambda: tpins.test_target_is_the_head_mean_and_sums_to_one(),
+    lambda: tpins.test_relu_decision_is_exact_at_cancellation(),
 ]
 
 

@@ -126,13 +126,31 @@ def test_target_is_the_head_mean_and_sums_to_one():
     assert np.allclose(np.mean(heads, axis=0), p, rtol=1e-12, equal_nan=True)
 
 
-def test_fp32_mask_changes_only_decisions_near_the_kink():
-    """The fp32 ReLU decision (the kernel's precision) agrees with the exact one away from
-    a = 0: on inputs with no dot product near 0 both options give the same gradients."""
-    q, w, qp, k, p = _case(6)
-    exact = oracle.indexer_kl(q, w, qp, k, p)
-    f32 = oracle.indexer_kl(q, w, qp, k, p, mask_fp32=True)
-    a = np.einsum("rjd,sd->rjs", q, k)
-    assert np.abs(a).min() > 1e-3  # no decision near the kink in this case
-    for x, y in zip(exact, f32):
-        assert np.array_equal(x, y)
+def test_relu_decision_is_exact_at_cancellation():
+    """[a > 0] is taken on the exact dot product (ReLU'(0) = 0).  Codes (15, 15, 15) . (15, -16, 1)
+    cancel to exactly 0 (225 - 240 + 15); times the fp32 scales 0.3 and 0.7 the fp64 products
+    round so that their plain fp64 sum is +3.6e-15.  That key must be masked, so dq and dk come
+    from the other key alone, by hand."""
+    qs, ks = float(np.float32(0.3)), float(np.float32(0.7))
+    dI = 128
+    qrow = np.zeros(dI)
+    qrow[:3] = 15 * qs
+    k0 = np.zeros(dI)
+    k0[:3] = np.array([15.0, -16.0, 1.0]) * ks
+    naive = 0.0
+    for d in range(3):
+        naive += qrow[d] * k0[d]
+    assert naive > 0.0  # the plain fp64 sum would switch the term on
+    k1 = np.zeros(dI)
+    k1[0] = 2.0 * ks
+    w = np.array([[0.5]])
+    p = np.array([[0.3, 0.7]])
+    loss, dw, dq, dk = oracle.indexer_kl(qrow[None, None, :], w, np.array([1], dtype=np.int32), np.stack([k0, k1]), p)
+    a1 = float(qrow @ k1)
+    I = np.array([0.0, 0.5 * a1])
+    sm = np.exp(I - I.max()) / np.exp(I - I.max()).sum()
+    g = sm - p[0]
+    assert np.allclose(dq[0, 0], g[1] * 0.5 * k1, rtol=1e-12, atol=0.0)
+    assert np.array_equal(dk[0], np.zeros(dI))
+    assert np.allclose(dk[1], g[1] * 0.5 * qrow, rtol=1e-12, atol=0.0)
+    assert np.isclose(dw[0, 0], g[1] * a1, rtol=1e-12)
