@@ -352,7 +352,7 @@ __device__ __forceinline__ float e4m3_to_float(uint32_t c)
 // contributes), the warp forms the exact sum of the code products as a 64-bit
 // integer (codes times 2^9 are integers, products below 2^36, 128 of them
 // below 2^43) and takes its sign.
-constexpr int kGThreads = 192;             // producer, MMA issuer, four epilogue warps
+constexpr int kGThreads = 320;             // producer, MMA issuer, eight epilogue warps (two per TMEM quadrant)
 constexpr int kGStages = 3;                // streamed code tiles
 constexpr int kGAtom = 128 * 128;          // one 64-column SW128 atom of a 128-row bf16 tile
 constexpr int kGTileBytes = 2 * kGAtom;    // 128 rows x 128 codes
@@ -363,12 +363,13 @@ constexpr int kGOffSt = kGOffRes + kGTileBytes;               // streamed tiles
 constexpr int kGOffAux = kGOffSt + kGStages * kGTileBytes;
 constexpr int kGOffList = kGOffAux + kGStages * kGAux;        // active row tiles (keys kernel)
 constexpr int kGOffBar = kGOffList + kGRowChunk * 4;
-constexpr int kGNBar = 17;
+constexpr int kGNBar = 18;
 constexpr int kGOffMisc = kGOffBar + kGNBar * 8;
 constexpr int kGSmem = kGOffMisc + 64 + 1024;
 static_assert(kGSmem <= 232448, "backward kernel shared memory");
 // barriers
-constexpr int G_RES = 0, G_SF = 1, G_SE = 4, G_DF = 7, G_DE = 9, G_CF = 11, G_CE = 13, G_D2 = 15, G_DONE = 16;
+constexpr int G_RES = 0, G_SF = 1, G_SE = 4, G_DF = 7, G_DE = 9, G_CF = 11, G_CE = 13, G_D2 = 15, G_DONE = 16,
+              G_DW = 17; // the second key half's dw partial sums are in shared memory
 // TMEM columns: D1 (two buffers), D2, C (two slots of 64 keys: hi then lo bf16 pairs)
 constexpr uint32_t GT_D1 = 0, GT_D2 = 256, GT_C = 384;
 
@@ -376,6 +377,7 @@ struct BwdParams {
     const uint8_t *q8, *k8;  // FP8 codes (exact decisions)
     const float *q_scale, *w, *k_scale;
     const float *qb;         // [T * HI] 2^-16 x the q code row's L1 norm (rounded up)
+    const float *wq;         // [T * HI] w[t,j] q_scale[t]
     const float *kinf;       // [S] largest |code| of the key row
     const int32_t *q_pos;
     const float *g;          // [T, ldg] dL/dI
@@ -461,12 +463,13 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(G_DF + i), 1);
-            mbar_init(bar(G_DE + i), 4);
+            mbar_init(bar(G_DE + i), 8);
             mbar_init(bar(G_CF + i), 4);
             mbar_init(bar(G_CE + i), 1);
         }
         mbar_init(bar(G_D2), 1);
         mbar_init(bar(G_DONE), 1);
+        mbar_init(bar(G_DW), 4);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -506,10 +509,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
 
     if (warp == 0) {
         // --------------------------------------------- producer: tiles by TMA, column data
-        int pos[4] = {-1, -1, -1, -1};
-        if (!KEYS)
-            for (int tl = 0; tl < tpt; ++tl)
-                pos[tl] = clamp_pos(p, own * tpt + tl);
+        int pos[4];
+#pragma unroll
+        for (int tl = 0; tl < 4; ++tl)
+            pos[tl] = (!KEYS && tl < tpt) ? clamp_pos(p, own * tpt + tl) : -1;
         if (lane == 0 && n_items > 0) {
             tma_prefetch_desc(&tm_res);
             tma_prefetch_desc(&tm_str);
@@ -527,32 +530,47 @@ __global__ void __launch_bounds__(kGThreads, 1)
             const int str = KEYS ? list[i] : i; // streamed tile: row tile / key tile
             if (!KEYS) {
                 // [tl][key]: g ks of token tl (0 where the token does not see the key); [4][key]: max |k code|
-                for (int x = lane; x < 5 * 128; x += 32) {
-                    const int tl = x >> 7, s = str * 128 + (x & 127);
-                    float v = 0.f;
-                    if (tl < 4) {
-                        if (tl < tpt && s <= pos[tl])
-                            v = p.g[(int64_t)(own * tpt + tl) * p.ldg + s] * p.k_scale[s];
-                    } else if (s < p.S) {
-                        v = p.kinf[s];
-                    }
-                    aux[x] = v;
+                float v[4][4], kv[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int s = str * 128 + 32 * m + lane;
+                    kv[m] = s < p.S ? p.kinf[s] : 0.f;
+#pragma unroll
+                    for (int tl = 0; tl < 4; ++tl)
+                        v[tl][m] = (tl < tpt && s <= pos[tl])
+                                       ? p.g[(int64_t)(own * tpt + tl) * p.ldg + s] * p.k_scale[s] : 0.f;
+                }
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+#pragma unroll
+                    for (int tl = 0; tl < 4; ++tl)
+                        aux[tl * 128 + 32 * m + lane] = v[tl][m];
+                    aux[4 * 128 + 32 * m + lane] = kv[m];
                 }
             } else {
                 // [tl][key]: g of token tl of the row tile at this CTA's keys; [4][row]: w q_scale; [5][row]: q bound
-                for (int x = lane; x < 6 * 128; x += 32) {
-                    const int tl = x >> 7, c = x & 127;
-                    float v = 0.f;
-                    if (tl < 4) {
-                        const int t = str * tpt + tl, s = own * 128 + c;
-                        if (tl < tpt && s <= clamp_pos(p, t))
-                            v = p.g[(int64_t)t * p.ldg + s];
-                    } else {
-                        const int r = str * 128 + c, t = r / p.HI;
-                        if (t < p.T)
-                            v = tl == 4 ? p.w[r] * p.q_scale[t] : p.qb[r];
-                    }
-                    aux[x] = v;
+                int pt[4];
+#pragma unroll
+                for (int tl = 0; tl < 4; ++tl)
+                    pt[tl] = tl < tpt ? clamp_pos(p, str * tpt + tl) : -1;
+                float v[4][4], wv[4], bv[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int s = own * 128 + 32 * m + lane, r = str * 128 + 32 * m + lane;
+                    const bool rv = r < p.T * p.HI;
+                    wv[m] = rv ? p.wq[r] : 0.f;
+                    bv[m] = rv ? p.qb[r] : 0.f;
+#pragma unroll
+                    for (int tl = 0; tl < 4; ++tl)
+                        v[tl][m] = s <= pt[tl] ? p.g[(int64_t)(str * tpt + tl) * p.ldg + s] : 0.f;
+                }
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+#pragma unroll
+                    for (int tl = 0; tl < 4; ++tl)
+                        aux[tl * 128 + 32 * m + lane] = v[tl][m];
+                    aux[4 * 128 + 32 * m + lane] = wv[m];
+                    aux[5 * 128 + 32 * m + lane] = bv[m];
                 }
             }
             __syncwarp();
@@ -634,7 +652,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
         __syncwarp();
     } else {
         // --------------------------------------------------------- epilogue
-        const int quad = warp & 3;
+        // Two warps per TMEM lane quadrant: half hh takes keys (rows kernel) / rows (keys
+        // kernel) 64 hh .. 64 hh + 63 of each streamed tile, i.e. C slot hh, and D2's
+        // columns 64 hh .. 64 hh + 63.
+        const int quad = warp & 3, hh = (warp - 2) >> 2;
         const int row = quad * 32 + lane; // TMEM lane: (t, j) row (rows kernel) / key (keys kernel)
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         const int rrow = own * 128 + row; // rows kernel: global (t, j) row; keys kernel: key
@@ -648,7 +669,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
             const int str = KEYS ? list[i] : i;
             // the stage's column data (the producer's stores) and D1
             if (!mbar_wait_warp(bar(G_SF + st), (i / kGStages) & 1, abort_flag, p.status) ||
-                !mbar_wait_warp(bar(G_DF + b), (i >> 1) & 1, abort_flag, p.status)) {
+                !mbar_wait_warp(bar(G_DF + b), (i >> 1) & 1, abort_flag, p.status) ||
+                (i >= 1 && !mbar_wait_warp(bar(G_CE + hh), (i - 1) & 1, abort_flag, p.status))) {
                 ok = false;
                 break;
             }
@@ -659,93 +681,84 @@ __global__ void __launch_bounds__(kGThreads, 1)
 #pragma unroll
                 for (int tl = 0; tl < 4; ++tl)
                     gt[tl] = aux[tl * 128 + row];
-            for (int h = 0; ok && h < 2; ++h) {
-                if (i >= 1 && !mbar_wait_warp(bar(G_CE + h), (i - 1) & 1, abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
 #pragma unroll 1
-                for (int cc = 0; cc < 2; ++cc) {
-                    const int c = 2 * h + cc;
-                    uint32_t r[32];
-                    tmem_ld32(lane_base + GT_D1 + 128 * b + 32 * c, r);
-                    tmem_ld_wait();
-                    if (c == 3) { // D1 is in registers: release it
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0)
-                            mbar_arrive(bar(G_DE + b));
-                    }
-                    // per column: the coefficient if a > 0, and whether the fp32 sign can be trusted
-                    float cv[32];
-                    uint32_t posm = 0u, ambm = 0u;
-                    const int tlc = (32 * c) / p.HI; // keys kernel: token of these columns (uniform)
-                    const float gc = tlc == 0 ? gt[0] : tlc == 1 ? gt[1] : tlc == 2 ? gt[2] : gt[3];
-#pragma unroll
-                    for (int e4 = 0; e4 < 8; ++e4) {
-                        const int col = 32 * c + 4 * e4;
-                        float4 v4, b4;
-                        if (!KEYS) {
-                            v4 = *reinterpret_cast<const float4 *>(aux + tl_own * 128 + col);
-                            b4 = *reinterpret_cast<const float4 *>(aux + 4 * 128 + col);
-                        } else {
-                            v4 = *reinterpret_cast<const float4 *>(aux + 4 * 128 + col);
-                            b4 = *reinterpret_cast<const float4 *>(aux + 5 * 128 + col);
-                        }
-                        const float vv[4] = {v4.x, v4.y, v4.z, v4.w}, bb[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int e = 4 * e4 + q;
-                            const float a = __uint_as_float(r[e]);
-                            const float v = KEYS ? gc * vv[q] : vv[q];
-                            const float bnd = KEYS ? bb[q] * kinf_own : qb_own * bb[q];
-                            cv[e] = v;
-                            posm |= (a > 0.f ? 1u : 0u) << e;
-                            ambm |= ((v != 0.f && fabsf(a) <= bnd) ? 1u : 0u) << e;
-                        }
-                    }
-                    // exact decisions where the fp32 sum is within its error bound of 0
-                    unsigned todo = __ballot_sync(0xffffffffu, ambm != 0u);
-                    while (todo) {
-                        const int L = __ffs(todo) - 1;
-                        const uint32_t mL = __shfl_sync(0xffffffffu, ambm, L);
-                        const int e = __ffs(mL) - 1;
-                        const int qrow = KEYS ? str * 128 + 32 * c + e : own * 128 + quad * 32 + L;
-                        const int key = KEYS ? own * 128 + quad * 32 + L : str * 128 + 32 * c + e;
-                        const bool pos = exact_dot_positive(p.q8 + (int64_t)qrow * 128, p.k8 + (int64_t)key * 128, lane);
-                        if (lane == L) {
-                            ambm &= ~(1u << e);
-                            posm = pos ? (posm | (1u << e)) : (posm & ~(1u << e));
-                        }
-                        todo = __ballot_sync(0xffffffffu, ambm != 0u);
-                    }
-                    // C = coefficient where a > 0, as hi + lo bf16 pairs
-                    uint32_t hi[16], lo[16];
-#pragma unroll
-                    for (int e2 = 0; e2 < 16; ++e2) {
-                        const int e0 = 2 * e2, e1 = e0 + 1;
-                        const float c0 = ((posm >> e0) & 1u) ? cv[e0] : 0.f;
-                        const float c1 = ((posm >> e1) & 1u) ? cv[e1] : 0.f;
-                        if (!KEYS)
-                            dw_acc += c0 * __uint_as_float(r[e0]) + c1 * __uint_as_float(r[e1]);
-                        const uint32_t hp = pack_bf16x2(c0, c1);
-                        hi[e2] = hp;
-                        lo[e2] = pack_bf16x2(c0 - __uint_as_float(hp << 16), c1 - __uint_as_float(hp & 0xFFFF0000u));
-                    }
-                    tmem_st16(lane_base + GT_C + 64 * h + 16 * cc, hi);
-                    tmem_st16(lane_base + GT_C + 64 * h + 32 + 16 * cc, lo);
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = 2 * hh + cc;
+                uint32_t r[32];
+                tmem_ld32(lane_base + GT_D1 + 128 * b + 32 * c, r);
+                tmem_ld_wait();
+                if (cc == 1) { // this warp's part of D1 is in registers: release it
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(bar(G_DE + b));
                 }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(bar(G_CF + h));
+                // per column: the coefficient if a > 0, and whether the fp32 sign can be trusted
+                float cv[32];
+                uint32_t posm = 0u, ambm = 0u;
+                const int tlc = (32 * c) / p.HI; // keys kernel: token of these columns (uniform)
+                const float gc = tlc == 0 ? gt[0] : tlc == 1 ? gt[1] : tlc == 2 ? gt[2] : gt[3];
+#pragma unroll
+                for (int e4 = 0; e4 < 8; ++e4) {
+                    const int col = 32 * c + 4 * e4;
+                    float4 v4, b4;
+                    if (!KEYS) {
+                        v4 = *reinterpret_cast<const float4 *>(aux + tl_own * 128 + col);
+                        b4 = *reinterpret_cast<const float4 *>(aux + 4 * 128 + col);
+                    } else {
+                        v4 = *reinterpret_cast<const float4 *>(aux + 4 * 128 + col);
+                        b4 = *reinterpret_cast<const float4 *>(aux + 5 * 128 + col);
+                    }
+                    const float vv[4] = {v4.x, v4.y, v4.z, v4.w}, bb[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int e = 4 * e4 + q;
+                        const float a = __uint_as_float(r[e]);
+                        const float v = KEYS ? gc * vv[q] : vv[q];
+                        const float bnd = KEYS ? bb[q] * kinf_own : qb_own * bb[q];
+                        cv[e] = v;
+                        posm |= (a > 0.f ? 1u : 0u) << e;
+                        ambm |= ((v != 0.f && fabsf(a) <= bnd) ? 1u : 0u) << e;
+                    }
+                }
+                // exact decisions where the fp32 sum is within its error bound of 0
+                unsigned todo = __ballot_sync(0xffffffffu, ambm != 0u);
+                while (todo) {
+                    const int L = __ffs(todo) - 1;
+                    const uint32_t mL = __shfl_sync(0xffffffffu, ambm, L);
+                    const int e = __ffs(mL) - 1;
+                    const int qrow = KEYS ? str * 128 + 32 * c + e : own * 128 + quad * 32 + L;
+                    const int key = KEYS ? own * 128 + quad * 32 + L : str * 128 + 32 * c + e;
+                    const bool pos = exact_dot_positive(p.q8 + (int64_t)qrow * 128, p.k8 + (int64_t)key * 128, lane);
+                    if (lane == L) {
+                        ambm &= ~(1u << e);
+                        posm = pos ? (posm | (1u << e)) : (posm & ~(1u << e));
+                    }
+                    todo = __ballot_sync(0xffffffffu, ambm != 0u);
+                }
+                // C = coefficient where a > 0, as hi + lo bf16 pairs
+                uint32_t hi[16], lo[16];
+#pragma unroll
+                for (int e2 = 0; e2 < 16; ++e2) {
+                    const int e0 = 2 * e2, e1 = e0 + 1;
+                    const float c0 = ((posm >> e0) & 1u) ? cv[e0] : 0.f;
+                    const float c1 = ((posm >> e1) & 1u) ? cv[e1] : 0.f;
+                    if (!KEYS)
+                        dw_acc += c0 * __uint_as_float(r[e0]) + c1 * __uint_as_float(r[e1]);
+                    const uint32_t hp = pack_bf16x2(c0, c1);
+                    hi[e2] = hp;
+                    lo[e2] = pack_bf16x2(c0 - __uint_as_float(hp << 16), c1 - __uint_as_float(hp & 0xFFFF0000u));
+                }
+                tmem_st16(lane_base + GT_C + 64 * hh + 16 * cc, hi);
+                tmem_st16(lane_base + GT_C + 64 * hh + 32 + 16 * cc, lo);
             }
-            if (!ok)
-                break;
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar(G_CF + hh));
         }
-        // ---- D2 out: dq and dw (rows kernel), dk partial sums (keys kernel)
+        // ---- D2 out: dq and dw (rows kernel), dk partial sums (keys kernel); D2 columns 64 hh ..
         const bool have = ok && n_items > 0;
         if (have && !mbar_wait_warp(bar(G_D2), 0, abort_flag, p.status))
             ok = false;
@@ -753,7 +766,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         if (!KEYS) {
             const float wr = valid ? p.w[rrow] : 0.f;
 #pragma unroll 1
-            for (int c0 = 0; c0 < 128; c0 += 32) {
+            for (int c0 = 64 * hh; c0 < 64 * hh + 64; c0 += 32) {
                 uint32_t r[32];
                 if (have && ok) {
                     tmem_ld32(lane_base + GT_D2 + c0, r);
@@ -771,11 +784,22 @@ __global__ void __launch_bounds__(kGThreads, 1)
                                              wr * __uint_as_float(r[4 * e + 2]), wr * __uint_as_float(r[4 * e + 3]));
                 }
             }
-            if (valid)
-                p.dw[rrow] = p.q_scale[rrow / p.HI] * dw_acc;
+            // dw: the second half's partial sums meet the first's in shared memory
+            float *dwp = reinterpret_cast<float *>(smem + kGOffAux); // the stages' column data are no longer read
+            if (hh == 1) {
+                if (have && ok)
+                    dwp[row] = dw_acc;
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(bar(G_DW));
+            } else {
+                const bool got = !(have && ok) || mbar_wait_warp(bar(G_DW), 0, abort_flag, p.status);
+                if (valid)
+                    p.dw[rrow] = p.q_scale[rrow / p.HI] * (dw_acc + (have && ok && got ? dwp[row] : 0.f));
+            }
         } else if (have && ok) { // warp-uniform: the TMEM loads are warp-collective
 #pragma unroll 1
-            for (int c0 = 0; c0 < 128; c0 += 32) {
+            for (int c0 = 64 * hh; c0 < 64 * hh + 64; c0 += 32) {
                 uint32_t r[32];
                 tmem_ld32(lane_base + GT_D2 + c0, r);
                 tmem_ld_wait();
@@ -796,13 +820,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
     }
 }
 
-// The codes as bf16 (exact) for the tensor cores, and the decision bounds:
-// qb[row] = 2^-16 x L1 norm of a q code row (rounded up), kinf[s] = largest
-// |code| of key s.  One warp per row; rows [0, nq) are q rows, then key rows.
+// The codes as bf16 (exact) for the tensor cores, the decision bounds (qb[row]
+// = 2^-16 x L1 norm of a q code row, rounded up; kinf[s] = largest |code| of
+// key s) and wq[row] = w q_scale.  One warp per row; rows [0, nq) are q rows
+// (nq = T H_I), then key rows.
 __global__ void __launch_bounds__(256)
     codes_kernel(const uint8_t *__restrict__ q8, int nq, const uint8_t *__restrict__ k8, int nk,
-                 __nv_bfloat16 *__restrict__ qc, float *__restrict__ qb, __nv_bfloat16 *__restrict__ kc,
-                 float *__restrict__ kinf)
+                 const float *__restrict__ w, const float *__restrict__ q_scale, int HI,
+                 __nv_bfloat16 *__restrict__ qc, float *__restrict__ qb, float *__restrict__ wq,
+                 __nv_bfloat16 *__restrict__ kc, float *__restrict__ kinf)
 {
     grid_dep_wait();
     grid_dep_launch();
@@ -833,17 +859,19 @@ __global__ void __launch_bounds__(256)
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     }
     if (lane == 0) {
-        if (isq)
+        if (isq) {
             qb[r] = l1 * (1.52587890625e-05f * 1.00390625f); // 2^-16 (1 + 2^-8): margin for this sum's rounding
-        else
+            wq[r] = w[r] * q_scale[r / HI];
+        } else {
             kinf[r - nq] = mx;
+        }
     }
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct WLayout {
-    size_t p, ig, qc, kc, qb, kinf, total;
+    size_t p, ig, qc, kc, qb, wq, kinf, total;
 };
 
 WLayout wlayout(int T, int S, int HI)
@@ -860,6 +888,8 @@ WLayout wlayout(int T, int S, int HI)
     o += align256(static_cast<size_t>(S) * 128 * 2);
     l.qb = o;
     o += align256(static_cast<size_t>(T) * HI * 4);
+    l.wq = o;
+    o += align256(static_cast<size_t>(T) * HI * 4);
     l.kinf = o;
     o += align256(static_cast<size_t>(S) * 4);
     l.total = o;
@@ -872,11 +902,12 @@ int launch_backward(const WarmupArgs &a, const WLayout &l, char *ws, const float
     __nv_bfloat16 *qc = reinterpret_cast<__nv_bfloat16 *>(ws + l.qc);
     __nv_bfloat16 *kc = reinterpret_cast<__nv_bfloat16 *>(ws + l.kc);
     float *qb = reinterpret_cast<float *>(ws + l.qb);
+    float *wq = reinterpret_cast<float *>(ws + l.wq);
     float *kinf = reinterpret_cast<float *>(ws + l.kinf);
     const int nq = a.T * a.HI;
     cudaError_t e = launch_pdl(codes_kernel, dim3(static_cast<unsigned>((nq + a.S + 7) / 8)), dim3(256), 0, stream, 1,
-                               static_cast<const uint8_t *>(a.q8), nq, static_cast<const uint8_t *>(a.k8), a.S, qc, qb,
-                               kc, kinf);
+                               static_cast<const uint8_t *>(a.q8), nq, static_cast<const uint8_t *>(a.k8), a.S, a.w,
+                               a.q_scale, a.HI, qc, qb, wq, kc, kinf);
     if (e != cudaSuccess) {
         snprintf(err, errlen, "warm-up codes launch: %s", cudaGetErrorString(e));
         return DSA_ERR_CUDA;
@@ -897,7 +928,7 @@ int launch_backward(const WarmupArgs &a, const WLayout &l, char *ws, const float
                         CU_TENSOR_MAP_SWIZZLE_128B, err, errlen))
         return DSA_ERR_CUDA;
     BwdParams bp{static_cast<const uint8_t *>(a.q8), static_cast<const uint8_t *>(a.k8), a.q_scale, a.w, a.k_scale,
-                 qb, kinf, a.q_pos, ig, (int64_t)a.S, a.T, a.S, a.HI, a.dw, a.dq, a.dk, status};
+                 qb, wq, kinf, a.q_pos, ig, (int64_t)a.S, a.T, a.S, a.HI, a.dw, a.dq, a.dk, status};
     const int nrt = (nq + 127) / 128, nkt = (a.S + 127) / 128;
     e = launch_pdl(bwd_tc_kernel<false>, dim3(static_cast<unsigned>(nrt)), dim3(kGThreads), kGSmem, stream, 1, tq, tk,
                    bp);
