@@ -236,10 +236,14 @@ size_t dsa_indexer_topk_workspace_size(int T, int S, int H_I, int d_I, int k);
  *   contiguous keys, (H_I, d_I) = (64, 128) or (32, 128);
  *   outputs fp32: loss [T], dw [T, H_I], dq [T, H_I, d_I], dk [S, d_I].
  *   workspace: dsa_indexer_warmup_workspace_size(T, S, H_I, d_I) bytes, 256-byte
- *   aligned, owned by the caller (it holds p, I and then g, and the per-(t, j, s)
- *   coefficients of dk: about 4 (2 + H_I) T S bytes).
+ *   aligned, owned by the caller (it holds p, I and then g, 8 T S bytes, and the
+ *   FP8 codes as bf16 with per-row bounds, about 264 (T H_I + S) bytes).
  * Precision: the target's scores on BF16 tensor cores with fp32 accumulation,
- * the index scores as dsa_indexer_logits, everything after in fp32.
+ * the index scores as dsa_indexer_logits; the gradient contractions on BF16
+ * tensor cores (the codes exact, the coefficients g w [a > 0] as bf16 hi + lo
+ * pairs, fp32 accumulation); the ReLU decision [a > 0] exact (the sign of the
+ * exact dot product of the codes).  dk is summed with atomics across chunks of
+ * rows, so its last bits may differ from call to call.
  */
 int dsa_indexer_warmup(const void *q, const void *kv, int H, float sm_scale,
                        const void *q8, const float *q_scale, const float *w, int H_I, int d_I,

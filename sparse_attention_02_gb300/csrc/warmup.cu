@@ -49,11 +49,12 @@ constexpr int kTChunkBytes = 128 * 128;        // 128 rows x 64 bf16
 constexpr int kTOffQ = 0;
 constexpr int kTOffKV = kTOffQ + kTChunks * kTChunkBytes;   // 144 KB
 constexpr int kTOffLse = kTOffKV + kTStages * kTChunkBytes; // 208 KB
-constexpr int kTOffBar = kTOffLse + 128 * 4;
-constexpr int kTNBar = 2 * kTStages + 4 + 2;
+constexpr int kTOffMl = kTOffLse + 128 * 4;                  // the second key half's (max, sum) per head
+constexpr int kTOffBar = kTOffMl + 128 * 8;
+constexpr int kTNBar = 2 * kTStages + 4 + 4;
 constexpr int kTOffMisc = kTOffBar + kTNBar * 8;
 constexpr int kTSmem = kTOffMisc + 64 + 1024;
-constexpr int kTThreads = 6 * 32;              // producer, MMA, four epilogue warps
+constexpr int kTThreads = 10 * 32;             // producer, MMA, eight epilogue warps (two per TMEM quadrant)
 static_assert(kTSmem <= 232448, "target kernel shared memory");
 
 struct TargetParams {
@@ -80,6 +81,9 @@ __global__ void __launch_bounds__(kTThreads, 1)
     auto acce_bar = [&](int a) { return bar0 + 8u * (2 * kTStages + 2 + a); };
     const uint32_t q_bar = bar0 + 8u * (2 * kTStages + 4);
     const uint32_t done_bar = bar0 + 8u * (2 * kTStages + 5);
+    const uint32_t ml_bar = bar0 + 8u * (2 * kTStages + 6);  // the second halves' (max, sum) are in shared memory
+    const uint32_t lse_bar = bar0 + 8u * (2 * kTStages + 7); // every head's LSE is in shared memory
+    float *mls = reinterpret_cast<float *>(smem + kTOffMl);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + kTOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kTOffMisc + 4);
     int *pos_s = reinterpret_cast<int *>(smem + kTOffMisc + 8);
@@ -94,10 +98,12 @@ __global__ void __launch_bounds__(kTThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(accf_bar(a), 1);
-            mbar_init(acce_bar(a), 4);
+            mbar_init(acce_bar(a), 8);
         }
         mbar_init(q_bar, 1);
         mbar_init(done_bar, 1);
+        mbar_init(ml_bar, 4);
+        mbar_init(lse_bar, 4);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -121,6 +127,10 @@ __global__ void __launch_bounds__(kTThreads, 1)
     const int pos = *pos_s;
     const int ntiles = pos < 0 ? 0 : pos / kTTile + 1;
     const int items = 2 * ntiles; // pass 0 tiles, then pass 1 tiles
+    // p's row is summed from the two head halves of pass 1
+    for (int s = threadIdx.x; s <= pos; s += kTThreads)
+        p.p[(int64_t)t * p.ld + s] = 0.f;
+    __syncthreads();
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -198,7 +208,9 @@ __global__ void __launch_bounds__(kTThreads, 1)
         __syncwarp();
     } else {
         // --------------------------------------------------------- epilogue
-        const int quad = warp & 3;
+        // Two warps per TMEM lane quadrant: half hh takes columns 64 hh .. 64 hh + 63 of
+        // each accumulator (pass 0: keys of the tile; pass 1: heads).
+        const int quad = warp & 3, hh = (warp - 2) >> 2;
         const int row = quad * 32 + lane; // pass 0: head; pass 1: key within the tile
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         float m = -INFINITY, l = 0.f;
@@ -207,21 +219,39 @@ __global__ void __launch_bounds__(kTThreads, 1)
             const bool pass1 = it >= ntiles;
             const int kt = it % ntiles;
             if (it == ntiles) {
-                // pass 0 done: every head's LSE (log2 units) into shared memory
-                lse2[row] = l > 0.f ? m + __log2f(l) : INFINITY;
-                named_bar_sync(1, 128);
+                // pass 0 done: the halves' (max, sum) of each head meet, its LSE (log2 units)
+                // goes to shared memory, and every warp waits for all of them
+                if (hh == 1) {
+                    mls[2 * row] = m;
+                    mls[2 * row + 1] = l;
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(ml_bar);
+                } else {
+                    if (!mbar_wait_warp(ml_bar, 0, abort_flag, p.status))
+                        break;
+                    const float m1 = mls[2 * row], l1 = mls[2 * row + 1];
+                    const float mm = fmaxf(m, m1);
+                    const float ll = (m == -INFINITY ? 0.f : l * exp2f(m - mm)) + (m1 == -INFINITY ? 0.f : l1 * exp2f(m1 - mm));
+                    lse2[row] = ll > 0.f ? mm + __log2f(ll) : INFINITY;
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(lse_bar);
+                }
+                if (!mbar_wait_warp(lse_bar, 0, abort_flag, p.status))
+                    break;
             }
             if (!mbar_wait_warp(accf_bar(a), use & 1, abort_flag, p.status))
                 break;
             tc_fence_after();
-            float bsum = 0.f; // pass 1: this key's sum over the heads
+            float bsum = 0.f; // pass 1: this key's sum over the half's heads
 #pragma unroll 1
-            for (int c0 = 0; c0 < 128; c0 += 32) {
+            for (int c0 = 64 * hh; c0 < 64 * hh + 64; c0 += 32) {
                 uint32_t r[32];
                 tmem_ld32(lane_base + 128 * a + c0, r);
                 tmem_ld_wait();
-                if (c0 == 96) {
-                    // every column of the accumulator is in registers: release it
+                if (c0 == 64 * hh + 32) {
+                    // this warp's columns of the accumulator are in registers: release it
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0)
@@ -254,8 +284,8 @@ __global__ void __launch_bounds__(kTThreads, 1)
             }
             if (pass1) {
                 const int s = kt * kTTile + row;
-                if (s <= pos)
-                    p.p[(int64_t)t * p.ld + s] = bsum / static_cast<float>(p.H);
+                if (s <= pos) // two additions onto 0: the same sum in either order
+                    atomicAdd(p.p + (int64_t)t * p.ld + s, bsum / static_cast<float>(p.H));
             }
         }
     }
