@@ -189,3 +189,17 @@ def test_fused_indexer_topk_validation(lib):
     assert call(ws=P((1 << 20) + 64)) == 3
     assert call(ws_bytes=need - 1) == 4
     assert "workspace" in _err(lib)
+
+
+def test_warmup_workspace_size(lib):
+    """The warm-up's workspace: p and I/g (T x S fp32 each), the FP8 codes as bf16 with one
+    bound and one w q_scale per (t, j) row and one bound per key: no per-(t, j, s) buffer."""
+    lib.dsa_indexer_warmup_workspace_size.restype = ctypes.c_size_t
+    ws = lib.dsa_indexer_warmup_workspace_size
+    T, S, HI = 4096, 4096, 64
+    need = ws(T, S, HI, 128)
+    floor = 8 * T * S + 256 * T * HI + 8 * T * HI + 256 * S + 4 * S
+    assert floor <= need <= floor + 6 * 256                        # each region rounded up to 256 bytes
+    assert need < 4 * HI * T * S // 8                              # far below a coefficient buffer
+    assert ws(T, 2 * S, HI, 128) > need and ws(T, S, 32, 128) < need
+    assert ws(T, S, 48, 128) == 0 and ws(T, S, 64, 64) == 0 and ws(-1, S, HI, 128) == 0 and ws(T, 0, HI, 128) == 0
