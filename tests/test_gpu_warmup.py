@@ -124,3 +124,20 @@ def test_warmup_exact_relu_decision_at_cancellation():
     status, got, ref = _run(x, x["q_pos"], L, 128)
     assert status == 0
     _check(got, ref)
+
+
+def test_warmup_tiny_rows_and_a_row_with_no_keys():
+    """Three rows over a 5-key prefix: positions -1 (no keys: zero loss and gradients), 0 (one
+    key) and 4 (all five): single partial row and key tiles, most of them past the data."""
+    S = 5
+    x = W.prefill_inputs(W.CONFIGS["prefill_4k"], DEV, L=S, seed=21)
+    rows = torch.tensor([0, 1, 4], device=DEV)
+    xc = dict(x)
+    for key in ("q8", "qs", "w", "q"):
+        xc[key] = x[key][rows].contiguous()
+    q_pos = torch.tensor([-1, 0, 4], dtype=torch.int32, device=DEV)
+    status, got, ref = _run(xc, q_pos, S, 128)
+    assert status == 0
+    loss, dw, dq, dk = got
+    assert loss[0] == 0.0 and np.all(dw[0] == 0.0) and np.all(dq[0] == 0.0)
+    _check(got, ref)
