@@ -705,13 +705,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp < kSoftWarp0) {
         // -------------------------------- score senders
-        // Thread = head (TMEM lane), all 64 keys of each block.  This CTA's fp32
-        // partial scores go to the peer one 16-key quarter at a time: staged in
-        // shared memory (two slots per warp), then a bulk copy of the warp's 32
-        // head rows (completion counted in bytes on the peer's per-quarter
-        // mbarrier, which the peer's softmax warps wait on and re-arm).  The
-        // next block's copies wait until the peer's softmax warps have read this
-        // one's.  Per-warp handshakes per quarter measured slower (the waits
+        // Thread = head (TMEM lane), all 64 keys of each block.  The block's 64
+        // partial-score columns are read first (two TMEM loads, one wait), which
+        // frees the S buffer, then go to the peer one 16-key quarter at a time:
+        // staged in shared memory (two slots per warp), then a bulk copy of the
+        // warp's 32 head rows (completion counted in bytes on the peer's
+        // per-quarter mbarrier, which the peer's softmax warps wait on and
+        // re-arm).  The next block's copies wait until the peer's softmax warps
+        // have read this one's.  Per-warp handshakes per quarter measured slower (the waits
         // inside the copy loop cost more than the coupling they remove).
         const int quad = warp & 3;
         const int h = quad * 32 + lane;
@@ -752,20 +753,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-#pragma unroll 1
+                uint32_t ra[32], rb[32];
+                tmem_ld32(s_cols, ra);
+                tmem_ld32(s_cols + 32, rb);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(bar(B_SE + b)); // this warp has read the block's partials
+#pragma unroll
                 for (int qq = 0; qq < 4; ++qq) {
                     // slot qq & 1 is free once the copy issued two quarters ago has read it
                     if (lane == 0)
                         bulk_wait_read1();
                     __syncwarp();
-                    uint32_t r[16];
-                    tmem_ld16(s_cols + 16 * qq, r);
-                    tmem_ld_wait();
                     uint8_t *srow = stg_row + (qq & 1) * 2048;
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc)
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int e = 16 * (qq & 1) + 4 * cc;
+                        const uint32_t *r = qq < 2 ? ra : rb;
                         *reinterpret_cast<uint4 *>(srow + ((static_cast<uint32_t>(cc) ^ qsw) << 4)) =
-                            make_uint4(r[4 * cc], r[4 * cc + 1], r[4 * cc + 2], r[4 * cc + 3]);
+                            make_uint4(r[e], r[e + 1], r[e + 2], r[e + 3]);
+                    }
                     fence_proxy_async_smem(); // the copy engine reads what the generic stores wrote
                     __syncwarp();
                     if (lane == 0) {
@@ -775,10 +784,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         bulk_commit();
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(bar(B_SE + b)); // this warp has read the block's partials
             }
         }
         if (lane == 0)
