@@ -56,11 +56,12 @@
 //                   per instruction whatever N is, so the N=64 score MMAs need
 //                   two issuing warps to keep the tensor pipe fed;
 //   sender warps    thread = head, one warp per TMEM lane quadrant: the
-//                   block's 64 partial scores from TMEM into shared memory,
-//                   then a bulk copy per 16-key quarter to the peer (completion
-//                   counted in bytes on the peer's per-quarter mbarrier) as
-//                   soon as the peer's softmax warps have read the previous
-//                   block's;
+//                   block's 64 partial scores from TMEM in two loads (the S
+//                   buffer is then free for them), into shared memory one
+//                   16-key quarter at a time, and a bulk copy per quarter to
+//                   the peer (completion counted in bytes on the peer's
+//                   per-quarter mbarrier) as soon as the peer's softmax warps
+//                   have read the previous block's;
 //   softmax warps   thread = head, two warps per TMEM lane quadrant, each with
 //                   32 of the block's keys: own partial from the S buffer
 //                   (then free for the next score MMAs once the senders have
