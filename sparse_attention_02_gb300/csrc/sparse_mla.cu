@@ -876,16 +876,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(bar(B_SE + b));
-                // the peer's partials of this warp's two quarters: (own + peer) * scale in fp32
-                // (the add commutes: both CTAs hold the same bits)
+                // the peer's partials of this warp's two quarters, each added as it lands:
+                // (own + peer) * scale in fp32 (the add commutes: both CTAs hold the same bits)
                 const int xb = J % kNX;
-                if (!mbar_wait_warp<true>(bar(B_XQ + 4 * xb + 2 * hf), (J / kNX) & 1, abort_flag, p.status) ||
-                    !mbar_wait_warp<true>(bar(B_XQ + 4 * xb + 2 * hf + 1), (J / kNX) & 1, abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
+                bool got = true;
 #pragma unroll
                 for (int qh = 0; qh < 2; ++qh) {
+                    if (!mbar_wait_warp<true>(bar(B_XQ + 4 * xb + 2 * hf + qh), (J / kNX) & 1, abort_flag, p.status)) {
+                        got = false;
+                        break;
+                    }
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const float4 pv = *reinterpret_cast<const float4 *>(
@@ -896,6 +896,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         sc[e0 + 2] = (sc[e0 + 2] + pv.z) * p.scale_log2;
                         sc[e0 + 3] = (sc[e0 + 3] + pv.w) * p.scale_log2;
                     }
+                }
+                if (!got) {
+                    ok = false;
+                    break;
                 }
                 __syncwarp(); // every lane has read its rows of the two quarters
                 if (lane == 0) {
