@@ -599,16 +599,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 mbar_arrive(bar(B_QA));
             for (int j = 0; j < nb; ++j, ++J) {
                 const int pb = J % kNP, st = J % kNStage;
-                if (!mbar_wait_warp(bar(B_PF + pb), (J / kNP) & 1, abort_flag, p.status) ||
-                    !mbar_wait_warp(bar(B_KVF + st), (J / kNStage) & 1, abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
-                if (j == 0 && v >= 1 && !mbar_wait_warp(bar(B_OE), (v - 1) & 1, abort_flag, p.status)) {
+                // the stage (landed long before P) first, so its proxy fence is off the P -> PV hop
+                if (!mbar_wait_warp(bar(B_KVF + st), (J / kNStage) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 fence_proxy_async_smem(); // the stage was written by cp.async (generic proxy)
+                if ((j == 0 && v >= 1 && !mbar_wait_warp(bar(B_OE), (v - 1) & 1, abort_flag, p.status)) ||
+                    !mbar_wait_warp(bar(B_PF + pb), (J / kNP) & 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
                 if (lane == 0) {
                     const uint64_t vd = pv_desc0 + static_cast<uint64_t>((st * kStage) >> 4);
