@@ -550,6 +550,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
             tma_load_2d(sbase + kGOffRes, &tm_res, bar(G_RES), 0, own * 128);
             tma_load_2d(sbase + kGOffRes + kGAtom, &tm_res, bar(G_RES), 64, own * 128);
         }
+        int issued = 0; // streamed tiles whose loads were issued (all n_items unless a wait gave up)
         for (int i = 0; i < n_items; ++i) {
             const int st = i % kGStages;
             if (i >= kGStages && !mbar_wait_warp(bar(G_SE + st), ((i / kGStages) - 1) & 1, abort_flag, p.status)) {
@@ -610,11 +611,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 tma_load_2d(dst, &tm_str, bar(G_SF + st), 0, str * 128);
                 tma_load_2d(dst + kGAtom, &tm_str, bar(G_SF + st), 64, str * 128);
             }
+            ++issued;
         }
         // every load issued has landed before the CTA exits
         if (lane == 0 && n_items > 0) {
             mbar_drain(bar(G_RES), 0);
-            for (int i = n_items > kGStages ? n_items - kGStages : 0; i < n_items; ++i)
+            for (int i = issued > kGStages ? issued - kGStages : 0; i < issued; ++i)
                 mbar_drain(bar(G_SF + i % kGStages), (i / kGStages) & 1);
         }
         __syncwarp();
