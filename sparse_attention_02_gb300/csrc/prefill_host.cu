@@ -61,17 +61,41 @@ struct HostPipe {
 HostPipe g_pipe[kMaxDev];
 std::mutex g_pipe_mu[kMaxDev];
 
+// Releases what a partly built pipe holds, so that the next call starts clean.
+void drop_pipe(HostPipe &p)
+{
+    for (cudaStream_t *st : {&p.h2d, &p.d2h}) {
+        if (*st)
+            cudaStreamDestroy(*st);
+        *st = nullptr;
+    }
+    for (cudaEvent_t *e : {&p.start, &p.end}) {
+        if (*e)
+            cudaEventDestroy(*e);
+        *e = nullptr;
+    }
+    for (int s = 0; s < kSlots; ++s)
+        for (cudaEvent_t *e : {&p.in_ready[s], &p.slot_done[s], &p.out_copied[s]}) {
+            if (*e)
+                cudaEventDestroy(*e);
+            *e = nullptr;
+        }
+    p.ready = false;
+}
+
 bool make_pipe(HostPipe &p)
 {
     if (p.ready)
         return true;
     auto ev = [](cudaEvent_t *e) { return cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess; };
-    if (cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaStreamCreateWithFlags(&p.d2h, cudaStreamNonBlocking) != cudaSuccess || !ev(&p.start) || !ev(&p.end))
+    bool ok = cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&p.d2h, cudaStreamNonBlocking) == cudaSuccess && ev(&p.start) && ev(&p.end);
+    for (int s = 0; ok && s < kSlots; ++s)
+        ok = ev(&p.in_ready[s]) && ev(&p.slot_done[s]) && ev(&p.out_copied[s]);
+    if (!ok) {
+        drop_pipe(p);
         return false;
-    for (int s = 0; s < kSlots; ++s)
-        if (!ev(&p.in_ready[s]) || !ev(&p.slot_done[s]) || !ev(&p.out_copied[s]))
-            return false;
+    }
     p.ready = true;
     return true;
 }
